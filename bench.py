@@ -1,0 +1,379 @@
+"""Benchmark of the MoE-LoRA expert layer (route + forward + backward) on GB300.
+
+One step = moe_route + moe_lora_fwd + moe_lora_bwd over one synthetic batch of
+the GPT-OSS-20B-shaped layer (T=4096, H=2880, E=32, top-4, I=2880, LoRA r=16)
+unless --config says otherwise.  Prints ONE JSON line (rank 0).
+
+  value        tokens/s of the whole job, device-timed (CUDA events around every
+               step, inputs resident in HBM, L2 flushed between steps)
+  e2e          the same metric with the step's inputs copied from pinned host
+               memory and its results copied back inside the timed region
+  roofline     the dominant kernel (largest share of the step), its algorithmic
+               flops (or bytes) per launch over its event-timed duration
+  gemm         all grouped-GEMM kernels together: algorithmic TFLOP/s and the
+               fraction of the measured dense bf16 peak
+  cpu_baseline the CPU oracle timed on a bounded token sample (rank 0, N=1)
+
+--impl reference times the CPU oracle (the only reference this layer has) on
+the host cores, on bounded token samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE-layer fwd+bwd tokens/s; grouped-GEMM TFLOP/s as % of GB300 BF16 peak"
+UNIT = "tokens/s"
+GEMM_KERNELS = ("gemm_gate_up_fwd", "gemm_down_fwd", "gemm_down_bwd", "gemm_gate_up_bwd")
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+def kernel_work(cfg: mi.MoEConfig) -> dict:
+    """Algorithmic flops and HBM bytes of one launch of each kernel (bf16 = 2 B).
+
+    N = T*k routed rows.  GEMM flops count the base and the LoRA product the
+    kernel performs; bytes count each operand once (weights of all experts)."""
+    T, H, I, E, k, r = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r
+    N = T * k
+    rp = 16 if r <= 16 else (32 if r <= 32 else 64)
+    b = 2
+    w = {
+        "gemm_gate_up_fwd": dict(flops=2 * N * H * 2 * I + 2 * N * r * 2 * I,
+                                 bytes=b * (N * H + E * H * 2 * I + E * r * 2 * I + N * rp + N * 2 * I + N * I)),
+        "gemm_down_fwd": dict(flops=2 * N * I * H + 2 * N * r * H,
+                              bytes=b * (N * I + E * I * H + E * r * H + N * rp) + 4 * N * H),
+        "gemm_down_bwd": dict(flops=2 * N * H * I + 2 * N * r * I,
+                              bytes=b * (N * H + E * I * H + E * r * I + N * rp + N * 2 * I + N * 2 * I)),
+        "gemm_gate_up_bwd": dict(flops=2 * N * 2 * I * H + 2 * N * r * H,
+                                 bytes=b * (N * 2 * I + E * H * 2 * I + E * r * H + N * rp) + 4 * N * H),
+        "gather_x": dict(flops=0, bytes=b * (T * H + N * H) + 4 * N),
+        "gather_dy": dict(flops=N * H, bytes=b * (T * H + N * H) + 8 * N),
+        "proj_xa": dict(flops=2 * N * H * r, bytes=b * (N * H + E * r * H + N * rp)),
+        "proj_ha": dict(flops=2 * N * I * r, bytes=b * (N * I + E * r * I + N * rp)),
+        "proj_g": dict(flops=2 * N * H * r, bytes=b * (N * H + E * r * H + N * rp)),
+        "proj_gg": dict(flops=2 * N * 2 * I * r, bytes=b * (N * 2 * I + E * r * 2 * I + N * rp)),
+        "combine_y": dict(flops=N * H, bytes=4 * N * H + b * T * H + 4 * N),
+        "combine_dx": dict(flops=N * H, bytes=4 * N * H + b * T * H + 4 * N),
+        "wgrad_dA_d": dict(flops=2 * N * r * I, bytes=b * (N * rp + N * I + E * r * I)),
+        "wgrad_dB_d": dict(flops=2 * N * r * H, bytes=b * (N * rp + N * H + E * r * H)),
+        "wgrad_dA_gu": dict(flops=2 * N * r * H, bytes=b * (N * rp + N * H + E * r * H)),
+        "wgrad_dB_gu": dict(flops=2 * N * r * 2 * I, bytes=b * (N * rp + N * 2 * I + E * r * 2 * I)),
+        "route": dict(flops=0, bytes=N * (8 + 4) * 2 + N * 12 + 8 * (E + 1)),
+    }
+    for v in w.values():
+        v["bound"] = "tensor" if v["flops"] >= 64 * v["bytes"] else "hbm"
+    return w
+
+
+def step_flops(cfg: mi.MoEConfig) -> int:
+    """Algorithmic fwd+bwd flops of the layer: N (12 H I + 12 H r + 18 I r)."""
+    N = cfg.T * cfg.k
+    return N * (12 * cfg.H * cfg.I + 12 * cfg.H * cfg.r + 18 * cfg.I * cfg.r)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=p["hbm_gbs"], bf16_tflops=p["bf16_tflops"],
+                    bf16_tflops_sustained=p.get("bf16_tflops_sustained", p["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "200", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None, "samples": len(rows), "reasons": reasons}
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, S: int) -> float:
+    """Route the full batch and run forward + backward of the oracle on the first
+    S tokens as a batch of their own; returns seconds."""
+    from oracle import moe_oracle as orc
+    t0 = time.perf_counter()
+    orc.route(idx, cfg.E)
+    sub_idx, sub_w = idx[:S], w[:S]
+    orc.lora_fwd(x_cpu[:S], sub_idx, sub_w, *wts_cpu, cfg.scale)
+    orc.lora_bwd(dy_cpu[:S], x_cpu[:S], sub_idx, sub_w, *wts_cpu, cfg.scale)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, budget_s: float = 20.0) -> dict:
+    t_small = oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, 2)
+    S = int(max(2, min(cfg.T, 2 * budget_s / max(t_small, 1e-6))))
+    S = min(S, cfg.T)
+    t = oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, S)
+    return {"value": S / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"route of all {cfg.T} tokens + fp64 forward and backward of the first {S} tokens "
+                      f"as a batch ({t:.1f} s)"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, cfg):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+    idx, w = mi.make_routing(cfg, args.seed)
+    ts = mi.make_tensors(cfg, args.seed, "cuda" if torch.cuda.is_available() else "cpu")
+    wts = [ts[n].cpu() for n in ("W_gu", "A_gu", "B_gu", "W_d", "A_d", "B_d")]
+    x_cpu, dy_cpu = ts["x"].cpu(), ts["dy"].cpu()
+    del ts
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    t2 = oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts, 1)
+    S = int(max(1, min(cfg.T, budget / max(t2, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts, S)
+    times = [oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts, S) for _ in range(args.steps)]
+    total = sum(times)
+    value = S * args.steps / total
+    sample = f"route of all {cfg.T} tokens + fp64 forward and backward of the first {S} tokens per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(cfg),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(cfg):
+    return {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} E={cfg.E} top-{cfg.k} I={cfg.I} LoRA r={cfg.r} "
+                        f"alpha={cfg.alpha:g}" + (f" zipf={cfg.zipf_s}" if cfg.zipf_s else ""),
+            "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "r": cfg.r,
+            "l2": "flushed between steps (256 MiB write); inputs+weights also exceed L2"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="gptoss20b", choices=list(mi.CONFIGS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--breakdown", action="store_true", help="print per-kernel times to stderr")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    cfg = mi.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    import moe_expert_dispatch_stable_gb300 as moe
+
+    # inputs: weights shared by all replicas, activations per replica
+    idx, w = mi.make_routing(cfg, args.seed + rank)
+    ts = mi.make_tensors(cfg, args.seed, dev, names=("W_gu", "A_gu", "B_gu", "W_d", "A_d", "B_d"))
+    ts.update(mi.make_tensors(cfg, args.seed + rank, dev, names=("x", "dy")))
+    d = moe.Dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r, cfg.scale)
+    layer = moe.MoELoRALayer(d, ts, dev)
+    t_idx = torch.from_numpy(idx).to(dev)
+    t_w = torch.from_numpy(w).to(dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        layer.step(t_idx, t_w, ts["x"], ts["dy"])
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0, "device status flag set during warm-up"
+
+    # ---- device-timed region
+    clocks = ClockSampler(local)
+    clocks.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = moe.moe_launch_count()
+    moe.moe_timing_enable(True)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        layer.step(t_idx, t_w, ts["x"], ts["dy"])
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    moe.moe_timing_enable(False)
+    launches = moe.moe_launch_count() - launches0
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kt = moe.moe_timing_read()
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = cfg.T * args.steps * world / (total_ms / 1e3)
+
+    # ---- end to end through host buffers
+    h_x = ts["x"].cpu().pin_memory(); h_dy = ts["dy"].cpu().pin_memory()
+    h_idx = torch.from_numpy(idx).pin_memory(); h_w = torch.from_numpy(w).pin_memory()
+    h_y = torch.empty_like(h_x).pin_memory(); h_dx = torch.empty_like(h_x).pin_memory()
+    h_g = [torch.empty(g.shape, dtype=g.dtype).pin_memory() for g in layer.grads]
+    d_x = torch.empty_like(ts["x"]); d_dy = torch.empty_like(ts["dy"])
+    d_idx = torch.empty_like(t_idx); d_w = torch.empty_like(t_w)
+    bytes_in = sum(t.numel() * t.element_size() for t in (h_x, h_dy, h_idx, h_w))
+    bytes_out = sum(t.numel() * t.element_size() for t in (h_y, h_dx, *h_g))
+    def e2e_step():
+        d_x.copy_(h_x, non_blocking=True); d_dy.copy_(h_dy, non_blocking=True)
+        d_idx.copy_(h_idx, non_blocking=True); d_w.copy_(h_w, non_blocking=True)
+        layer.step(d_idx, d_w, d_x, d_dy)
+        h_y.copy_(layer.y, non_blocking=True); h_dx.copy_(layer.dx, non_blocking=True)
+        for h, g in zip(h_g, layer.grads):
+            h.copy_(g, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e_s[i].record(stream)
+        e2e_step()
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e))
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = cfg.T * args.steps * world / (e2e_ms / 1e3)
+    assert int(layer.dev_status.item()) == 0, "device status flag set"
+
+    # ---- roofline of the dominant kernel and the GEMM aggregate
+    peaks = load_peaks()
+    work = kernel_work(cfg)
+    kernel_ms_step = {n: ms / max(1, args.steps) for n, (ms, cnt) in kt.items()}
+    dom = max(kt, key=lambda n: kt[n][0])
+    ms_launch = kt[dom][0] / kt[dom][1]
+    wk = work[dom]
+    if wk["bound"] == "tensor":
+        ach = wk["flops"] / (ms_launch / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"], "traffic": None,
+                "algorithmic_flops_per_launch": wk["flops"], "ms_per_launch": ms_launch,
+                "peak_source": f"{peaks['source']} bf16 sustained"}
+    else:
+        ach = wk["bytes"] / (ms_launch / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": wk["bytes"],
+                "ms_per_launch": ms_launch, "peak_source": f"{peaks['source']} hbm copy"}
+    g_ms = sum(kt[n][0] for n in GEMM_KERNELS if n in kt) / args.steps
+    g_fl = sum(work[n]["flops"] for n in GEMM_KERNELS)
+    g_tf = g_fl / (g_ms / 1e3) / 1e12 if g_ms > 0 else 0.0
+    gemm = {"tflops": g_tf, "frac_of_bf16_peak": g_tf / peaks["bf16_tflops_sustained"],
+            "peak": peaks["bf16_tflops_sustained"], "ms_per_step": g_ms, "flops_per_step": g_fl}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(cfg), "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out},
+        "gpu_launches": int(launches),
+        "roofline": roof, "gemm": gemm,
+        "layer_tflops": step_flops(cfg) / (total_ms / args.steps / 1e3) / 1e12,
+        "wall_s_timed": wall,
+        "kernels_ms_per_step": {n: round(v, 4) for n, v in sorted(kernel_ms_step.items(), key=lambda kv: -kv[1])},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        wts = [ts[n].cpu() for n in ("W_gu", "A_gu", "B_gu", "W_d", "A_d", "B_d")]
+        line["cpu_baseline"] = cpu_baseline(cfg, idx, w, ts["x"].cpu(), ts["dy"].cpu(), wts)
+    if args.breakdown and rank == 0:
+        for n, v in line["kernels_ms_per_step"].items():
+            print(f"{n:20s} {v:9.4f} ms/step", file=sys.stderr)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * moe_lora.h -- C ABI of the GB300 (sm_103a) MoE-LoRA expert layer.
+ *
+ * Three operations, all enqueued on the caller's CUDA stream, none of which
+ * synchronises with the host or copies anything back to it:
+ *
+ *   moe_route     group the T*k routed slots by expert (histogram, exclusive
+ *                 scan to offsets, stable scatter).
+ *   moe_lora_fwd  y = sum_j w[t,j] * SwiGLU-expert_{e(t,j)}(x[t]) with
+ *                 Split-LoRA on both projections.
+ *   moe_lora_bwd  dx and the per-expert LoRA gradients dA_gu, dB_gu, dA_d,
+ *                 dB_d for L = <dy, y> (the base weights are frozen).
+ *
+ * Sources.  Routing: the blog post on Unsloth x NVIDIA training speed-ups
+ * (d9249.github.io, section "core idea / structure / how it works", GPT-OSS MoE
+ * routing paragraphs): flatten the top-k assignment, stable-sort by expert id,
+ * bincount once, slice by offsets, instead of one torch.where query per
+ * expert.  Grouped matmul and Split-LoRA: the Unsloth 2026 wiki page on GRPO,
+ * MoE and memory-efficient fine-tuning, section "Optimisation 3: grouped_mm and
+ * Split-LoRA for MoE training": all experts' weights stacked in one tensor,
+ * group sizes equal to the routing counts, and the LoRA product applied after
+ * the base product (x W + s (x A) B) instead of materialising W + BA.
+ *
+ * Conventions for every function:
+ *  - All tensors are dense row-major; bf16 tensors are passed as uint16_t*.
+ *  - Every pointer is a DEVICE pointer unless stated otherwise, 16-byte aligned,
+ *    owned by the caller.  The library allocates no device memory and keeps no
+ *    state beyond a per-device cache of the SM count and of a driver entry point.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - A non-zero return is a host-side error found before anything was enqueued
+ *    (bad argument, unsupported size, workspace too small) or a CUDA launch
+ *    error; nothing is launched in the first three cases.
+ *  - Errors only the device can see are OR-ed into *dev_status (a device int32
+ *    the caller zeroes and reads when it wants): MOE_DEV_BAD_EXPERT_ID for an
+ *    expert id outside [0, E), MOE_DEV_TIMEOUT when a bounded wait inside a
+ *    kernel gave up.  When a bit is set the outputs are unspecified.
+ *  - No function blocks the host; all of them can be captured in a CUDA graph.
+ *
+ * Sizes supported: 1 <= k <= E <= 1024, H and I multiples of 64, 1 <= r <= 64,
+ * T >= 0 and T*k < 2^31.
+ */
+#ifndef MOE_LORA_H
+#define MOE_LORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t moe_status;
+
+enum {
+    MOE_OK = 0,
+    MOE_ERR_NULL_ARG = 1,      /* a required pointer is NULL */
+    MOE_ERR_BAD_DIMS = 2,      /* sizes outside the supported range */
+    MOE_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+    MOE_ERR_WORKSPACE = 4,     /* workspace / saved buffer smaller than required */
+    MOE_ERR_CUDA = 5,          /* a CUDA runtime / driver call failed */
+    MOE_ERR_UNSUPPORTED = 6    /* device is not sm_103 or a needed driver entry point is missing */
+};
+
+enum {
+    MOE_DEV_BAD_EXPERT_ID = 1,
+    MOE_DEV_TIMEOUT = 2
+};
+
+/* Row tile of the grouped GEMMs; tile_offsets counts tiles of this many rows. */
+#define MOE_TILE_M 128
+
+typedef struct moe_dims {
+    int64_t T;      /* tokens */
+    int32_t H;      /* hidden size (x, y rows) */
+    int32_t I;      /* expert intermediate size (gate_up: H -> 2I, down: I -> H) */
+    int32_t E;      /* number of experts */
+    int32_t k;      /* experts per token */
+    int32_t r;      /* LoRA rank */
+    float scale;    /* LoRA scale s (alpha / r) */
+} moe_dims;
+
+/* Outputs of moe_route, inputs of moe_lora_fwd / moe_lora_bwd (device pointers). */
+typedef struct moe_routing {
+    int32_t* perm;          /* [T*k]  perm[p] = flat slot t*k+j at sorted position p */
+    int32_t* inv_perm;      /* [T*k]  inv_perm[perm[p]] = p */
+    int32_t* counts;        /* [E]    rows routed to each expert */
+    int32_t* offsets;       /* [E+1]  exclusive prefix sum of counts */
+    int32_t* tile_offsets;  /* [E+1]  exclusive prefix sum of ceil(counts / MOE_TILE_M) */
+    float* w_sorted;        /* [T*k]  w_sorted[p] = topk_w_flat[perm[p]] (bit copy) */
+} moe_routing;
+
+/* ABI version of this header (bumped on any signature change). */
+MOE_API int32_t moe_abi_version(void);
+
+/* Static string for a status code. */
+MOE_API const char* moe_status_string(moe_status s);
+
+/* ---------------------------------------------------------------- routing
+ * Bytes of device workspace moe_route needs for T tokens, k slots, E experts. */
+MOE_API moe_status moe_route_workspace_size(int64_t T, int32_t k, int32_t E, size_t* bytes);
+
+/* Group the routed slots by expert.
+ *  topk_idx   [T, k] expert ids, int32 (idx_bytes = 4) or int64 (idx_bytes = 8)
+ *  topk_w     [T, k] float32 routing weights (only copied, reordered)
+ *  out        device pointers of the outputs (see moe_routing)
+ * The order inside an expert is the ascending flat slot index t*k + j, i.e. a
+ * stable sort of the flattened assignment by expert id.  Bit-exact and
+ * deterministic.  An id outside [0, E) sets MOE_DEV_BAD_EXPERT_ID and that slot
+ * is left out of every output.  Three stream operations: a 4-byte memset and
+ * two kernels. */
+MOE_API moe_status moe_route(const void* topk_idx, int32_t idx_bytes, const float* topk_w,
+                     int64_t T, int32_t k, int32_t E, const moe_routing* out,
+                     void* workspace, size_t workspace_bytes,
+                     int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------- forward
+ * Bytes of the `saved` buffer (activations kept for the backward pass) and of
+ * the forward workspace. */
+MOE_API moe_status moe_lora_fwd_sizes(const moe_dims* d, size_t* saved_bytes, size_t* workspace_bytes);
+
+/* Byte offsets inside `saved` of: x_perm [N,H], GU [N,2I], h [N,I],
+ * XA_s [N,RP], HA_s [N,RP] (all bf16, N = T*k rows in sorted order,
+ * RP = r rounded up to 16, 32 or 64, padding columns zero;
+ * XA_s = s * x_perm A_gu^T, HA_s = s * h A_d^T).  For inspection and tests. */
+MOE_API moe_status moe_lora_saved_layout(const moe_dims* d, size_t offsets[5], int32_t* rp);
+
+/* Forward of the MoE-LoRA expert layer (Split-LoRA, SwiGLU, weighted combine).
+ *  x     [T, H]                  W_gu [E, H, 2I] (gate = cols [0,I), up = [I,2I))
+ *  A_gu  [E, r, H] (A^T, the PEFT lora_A layout)   B_gu [E, r, 2I]
+ *  W_d   [E, I, H]   A_d [E, r, I]   B_d [E, r, H]
+ *  y     [T, H] output, bf16
+ * For every slot (t, j) with e = topk_idx[t, j]:
+ *   GU = x[t] W_gu[e] + s (x[t] A_gu[e]^T) B_gu[e];  h = silu(GU[:I]) * GU[I:]
+ *   o  = h W_d[e] + s (h A_d[e]^T) B_d[e];           y[t] = sum_j w[t,j] o_j
+ * with bf16 operands, fp32 accumulation, and the k slots of a token summed in
+ * the fixed order j = 0..k-1 (bitwise reproducible). */
+MOE_API moe_status moe_lora_fwd(const moe_dims* d, const moe_routing* rt,
+                        const uint16_t* x,
+                        const uint16_t* W_gu, const uint16_t* A_gu, const uint16_t* B_gu,
+                        const uint16_t* W_d, const uint16_t* A_d, const uint16_t* B_d,
+                        uint16_t* y,
+                        void* saved, size_t saved_bytes,
+                        void* workspace, size_t workspace_bytes,
+                        int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------- backward */
+MOE_API moe_status moe_lora_bwd_workspace_size(const moe_dims* d, size_t* bytes);
+
+/* Backward of moe_lora_fwd for L = <dy, y> with the base weights frozen.
+ *  dy [T, H]; saved = the buffer moe_lora_fwd filled (same d, rt, weights).
+ *  Outputs (bf16, same layouts as the parameters):
+ *   dx [T, H], dA_gu [E, r, H], dB_gu [E, r, 2I], dA_d [E, r, I], dB_d [E, r, H]
+ * Per slot: dO = w dy[t]; dh = dO W_d^T + s (dO B_d^T) A_d;
+ *   dGU = SwiGLU'(GU) dh;  dx[t] += dGU W_gu^T + s (dGU B_gu^T) A_gu
+ * Per expert (sums over its rows, fixed order, no float atomics):
+ *   dA_d = s (dO B_d^T)^T h,  dB_d = s (h A_d^T)^T dO,
+ *   dA_gu = s (dGU B_gu^T)^T x,  dB_gu = s (x A_gu^T)^T dGU.
+ * Experts with no rows get exact zeros. */
+MOE_API moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt,
+                        const uint16_t* dy,
+                        const uint16_t* W_gu, const uint16_t* A_gu, const uint16_t* B_gu,
+                        const uint16_t* W_d, const uint16_t* A_d, const uint16_t* B_d,
+                        const void* saved, size_t saved_bytes,
+                        uint16_t* dx, uint16_t* dA_gu, uint16_t* dB_gu,
+                        uint16_t* dA_d, uint16_t* dB_d,
+                        void* workspace, size_t workspace_bytes,
+                        int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------- diagnostics
+ * Per-kernel timing.  moe_timing_enable(1) clears the record and makes every
+ * later kernel launch of moe_route / moe_lora_fwd / moe_lora_bwd bracketed by
+ * two CUDA events recorded on the caller's stream (the events are created on
+ * first use and reused; no device memory is allocated).  moe_timing_enable(0)
+ * stops recording.  moe_timing_read(i, ...) reports, for the i-th distinct
+ * kernel name recorded, the summed elapsed milliseconds and the number of
+ * launches; it WAITS for those events (host-blocking, diagnostics only) and
+ * returns MOE_ERR_BAD_DIMS once i is past the last name. */
+MOE_API moe_status moe_timing_enable(int32_t on);
+MOE_API moe_status moe_timing_read(int32_t index, char* name, size_t name_len,
+                                   double* total_ms, int32_t* launches);
+
+/* Number of launch operations (kernels, plus the route's 4-byte memset) the
+ * library has issued since it was loaded, counted on the host. */
+MOE_API uint64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LORA_H */

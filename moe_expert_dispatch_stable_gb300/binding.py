@@ -1,0 +1,318 @@
+"""Thin Python binding of the MoE-LoRA C ABI (``include/moe_lora.h``).
+
+Argument marshalling only: torch tensors are checked for device, dtype,
+contiguity and shape, and their data pointers, sizes and the current CUDA
+stream are handed to the C functions of the same names.  Every step of the
+layer runs in the library's kernels; there is no fallback of any kind -- if
+the shared library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_lora_gb300.so")
+
+MOE_OK = 0
+MOE_DEV_BAD_EXPERT_ID = 1
+MOE_DEV_TIMEOUT = 2
+TILE_M = 128
+
+
+class MoEError(RuntimeError):
+    pass
+
+
+class moe_dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("r", ctypes.c_int32),
+                ("scale", ctypes.c_float)]
+
+
+class moe_routing(ctypes.Structure):
+    _fields_ = [("perm", ctypes.c_void_p), ("inv_perm", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("tile_offsets", ctypes.c_void_p), ("w_sorted", ctypes.c_void_p)]
+
+
+EXPORTED = ("moe_abi_version", "moe_status_string", "moe_launch_count", "moe_route_workspace_size", "moe_route",
+            "moe_lora_fwd_sizes", "moe_lora_saved_layout", "moe_lora_fwd",
+            "moe_lora_bwd_workspace_size", "moe_lora_bwd", "moe_timing_enable", "moe_timing_read")
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise MoEError(f"MoE-LoRA CUDA library not built: {path} is missing "
+                       "(run moe_expert_dispatch_stable_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    P = ctypes.POINTER
+    lib.moe_abi_version.restype = i32
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_status_string.argtypes = [i32]
+    lib.moe_route_workspace_size.argtypes = [i64, i32, i32, P(sz)]
+    lib.moe_route.argtypes = [vp, i32, vp, i64, i32, i32, P(moe_routing), vp, sz, vp, vp]
+    lib.moe_lora_fwd_sizes.argtypes = [P(moe_dims), P(sz), P(sz)]
+    lib.moe_lora_saved_layout.argtypes = [P(moe_dims), P(sz), P(i32)]
+    lib.moe_lora_fwd.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 8 + [vp, sz, vp, sz, vp, vp]
+    lib.moe_lora_bwd_workspace_size.argtypes = [P(moe_dims), P(sz)]
+    lib.moe_lora_bwd.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 7 + [vp, sz] + [vp] * 5 + [vp, sz, vp, vp]
+    lib.moe_launch_count.restype = ctypes.c_uint64
+    lib.moe_timing_enable.argtypes = [i32]
+    lib.moe_timing_read.argtypes = [i32, ctypes.c_char_p, sz, P(ctypes.c_double), P(i32)]
+    for name in EXPORTED[3:]:
+        getattr(lib, name).restype = i32
+    if lib.moe_abi_version() != 1:
+        raise MoEError("MoE-LoRA library ABI version mismatch")
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        msg = load_library().moe_status_string(status).decode()
+        raise MoEError(f"MoE-LoRA call failed with status {status}: {msg}")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise MoEError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise MoEError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise MoEError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise MoEError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+@dataclass
+class Routing:
+    perm: torch.Tensor
+    inv_perm: torch.Tensor
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    tile_offsets: torch.Tensor
+    w_sorted: torch.Tensor
+
+    def c_struct(self) -> moe_routing:
+        return moe_routing(self.perm.data_ptr(), self.inv_perm.data_ptr(), self.counts.data_ptr(),
+                           self.offsets.data_ptr(), self.tile_offsets.data_ptr(), self.w_sorted.data_ptr())
+
+    @staticmethod
+    def empty(T: int, k: int, E: int, device) -> "Routing":
+        N = T * k
+        i32 = dict(dtype=torch.int32, device=device)
+        return Routing(torch.empty(max(N, 4), **i32)[:N], torch.empty(max(N, 4), **i32)[:N],
+                       torch.empty(E, **i32), torch.empty(E + 1, **i32), torch.empty(E + 1, **i32),
+                       torch.empty(max(N, 4), dtype=torch.float32, device=device)[:N])
+
+
+@dataclass(frozen=True)
+class Dims:
+    T: int
+    H: int
+    I: int
+    E: int
+    k: int
+    r: int
+    scale: float
+
+    def c_struct(self) -> moe_dims:
+        return moe_dims(self.T, self.H, self.I, self.E, self.k, self.r, self.scale)
+
+
+def moe_route_workspace_size(T: int, k: int, E: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().moe_route_workspace_size(T, k, E, ctypes.byref(n)))
+    return n.value
+
+
+def moe_route(topk_idx: torch.Tensor, topk_w: torch.Tensor, E: int, out: Routing | None = None,
+              workspace: torch.Tensor | None = None, dev_status: torch.Tensor | None = None,
+              stream=None) -> Routing:
+    """Group the T*k routed slots by expert (see moe_route in moe_lora.h)."""
+    lib = load_library()
+    if topk_idx.dtype not in (torch.int32, torch.int64):
+        raise MoEError("topk_idx must be int32 or int64")
+    _need(topk_idx, "topk_idx", topk_idx.dtype)
+    if topk_idx.dim() != 2:
+        raise MoEError("topk_idx must be [T, k]")
+    T, k = topk_idx.shape
+    _need(topk_w, "topk_w", torch.float32, (T, k))
+    dev = topk_idx.device
+    if out is None:
+        out = Routing.empty(T, k, E, dev)
+    if workspace is None:
+        workspace = torch.empty(moe_route_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    rt = out.c_struct()
+    _check(lib.moe_route(_ptr(topk_idx), topk_idx.element_size(), _ptr(topk_w), T, k, E, ctypes.byref(rt),
+                         _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def moe_lora_fwd_sizes(d: Dims):
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load_library().moe_lora_fwd_sizes(ctypes.byref(d.c_struct()), ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def moe_lora_saved_layout(d: Dims):
+    offs = (ctypes.c_size_t * 5)()
+    rp = ctypes.c_int32()
+    _check(load_library().moe_lora_saved_layout(ctypes.byref(d.c_struct()), offs, ctypes.byref(rp)))
+    return list(offs), rp.value
+
+
+def moe_lora_bwd_workspace_size(d: Dims) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().moe_lora_bwd_workspace_size(ctypes.byref(d.c_struct()), ctypes.byref(n)))
+    return n.value
+
+
+def _check_weights(d: Dims, W_gu, A_gu, B_gu, W_d, A_d, B_d):
+    bf = torch.bfloat16
+    _need(W_gu, "W_gu", bf, (d.E, d.H, 2 * d.I))
+    _need(A_gu, "A_gu", bf, (d.E, d.r, d.H))
+    _need(B_gu, "B_gu", bf, (d.E, d.r, 2 * d.I))
+    _need(W_d, "W_d", bf, (d.E, d.I, d.H))
+    _need(A_d, "A_d", bf, (d.E, d.r, d.I))
+    _need(B_d, "B_d", bf, (d.E, d.r, d.H))
+
+
+def moe_lora_fwd(d: Dims, rt: Routing, x, W_gu, A_gu, B_gu, W_d, A_d, B_d, y=None, saved=None,
+                 workspace=None, dev_status=None, stream=None):
+    """Forward of the layer; returns (y, saved)."""
+    lib = load_library()
+    _need(x, "x", torch.bfloat16, (d.T, d.H))
+    _check_weights(d, W_gu, A_gu, B_gu, W_d, A_d, B_d)
+    dev = x.device
+    saved_b, ws_b = moe_lora_fwd_sizes(d)
+    if y is None:
+        y = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
+    if saved is None:
+        saved = torch.empty(max(saved_b, 16), dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(ws_b, 16), dtype=torch.uint8, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _need(y, "y", torch.bfloat16, (d.T, d.H))
+    dd, rr = d.c_struct(), rt.c_struct()
+    _check(lib.moe_lora_fwd(ctypes.byref(dd), ctypes.byref(rr), _ptr(x), _ptr(W_gu), _ptr(A_gu), _ptr(B_gu),
+                            _ptr(W_d), _ptr(A_d), _ptr(B_d), _ptr(y), _ptr(saved), saved.numel(),
+                            _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream)))
+    return y, saved
+
+
+def moe_lora_bwd(d: Dims, rt: Routing, dy, W_gu, A_gu, B_gu, W_d, A_d, B_d, saved, dx=None, grads=None,
+                 workspace=None, dev_status=None, stream=None):
+    """Backward of the layer; returns (dx, dA_gu, dB_gu, dA_d, dB_d)."""
+    lib = load_library()
+    _need(dy, "dy", torch.bfloat16, (d.T, d.H))
+    _check_weights(d, W_gu, A_gu, B_gu, W_d, A_d, B_d)
+    dev = dy.device
+    if dx is None:
+        dx = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
+    if grads is None:
+        grads = (torch.empty_like(A_gu), torch.empty_like(B_gu), torch.empty_like(A_d), torch.empty_like(B_d))
+    if workspace is None:
+        workspace = torch.empty(max(moe_lora_bwd_workspace_size(d), 16), dtype=torch.uint8, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    dA_gu, dB_gu, dA_d, dB_d = grads
+    dd, rr = d.c_struct(), rt.c_struct()
+    _check(lib.moe_lora_bwd(ctypes.byref(dd), ctypes.byref(rr), _ptr(dy), _ptr(W_gu), _ptr(A_gu), _ptr(B_gu),
+                            _ptr(W_d), _ptr(A_d), _ptr(B_d), _ptr(saved), saved.numel(), _ptr(dx),
+                            _ptr(dA_gu), _ptr(dB_gu), _ptr(dA_d), _ptr(dB_d), _ptr(workspace), workspace.numel(),
+                            _ptr(dev_status), _stream(stream)))
+    return dx, dA_gu, dB_gu, dA_d, dB_d
+
+
+def moe_launch_count() -> int:
+    """Launch operations the library has issued so far (host-side count)."""
+    return int(load_library().moe_launch_count())
+
+
+def moe_timing_enable(on: bool) -> None:
+    """Start (clearing the record) or stop per-kernel event timing."""
+    _check(load_library().moe_timing_enable(1 if on else 0))
+
+
+def moe_timing_read() -> dict:
+    """{kernel name: (total ms, launches)} of the launches recorded since the last
+    moe_timing_enable(True).  Waits for the recorded events."""
+    lib = load_library()
+    out = {}
+    buf = ctypes.create_string_buffer(64)
+    ms, n = ctypes.c_double(), ctypes.c_int32()
+    i = 0
+    while True:
+        st = lib.moe_timing_read(i, buf, 64, ctypes.byref(ms), ctypes.byref(n))
+        if st == 2:
+            break
+        _check(st)
+        out[buf.value.decode()] = (ms.value, n.value)
+        i += 1
+    return out
+
+
+class MoELoRALayer:
+    """Preallocated buffers for repeated route + forward + backward calls on one
+    stream (no allocation inside a step, so a step can be graph-captured)."""
+
+    def __init__(self, d: Dims, weights: dict, device="cuda"):
+        self.d = d
+        self.w = weights
+        dev = torch.device(device)
+        self.rt = Routing.empty(d.T, d.k, d.E, dev)
+        self.route_ws = torch.empty(moe_route_workspace_size(d.T, d.k, d.E), dtype=torch.uint8, device=dev)
+        sb, wb = moe_lora_fwd_sizes(d)
+        self.saved = torch.empty(max(sb, 16), dtype=torch.uint8, device=dev)
+        self.fwd_ws = torch.empty(max(wb, 16), dtype=torch.uint8, device=dev)
+        self.bwd_ws = torch.empty(max(moe_lora_bwd_workspace_size(d), 16), dtype=torch.uint8, device=dev)
+        self.y = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
+        self.grads = tuple(torch.empty_like(weights[n]) for n in ("A_gu", "B_gu", "A_d", "B_d"))
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def _wts(self):
+        w = self.w
+        return w["W_gu"], w["A_gu"], w["B_gu"], w["W_d"], w["A_d"], w["B_d"]
+
+    def route(self, topk_idx, topk_w, stream=None):
+        return moe_route(topk_idx, topk_w, self.d.E, out=self.rt, workspace=self.route_ws,
+                         dev_status=self.dev_status, stream=stream)
+
+    def forward(self, x, stream=None):
+        return moe_lora_fwd(self.d, self.rt, x, *self._wts(), y=self.y, saved=self.saved,
+                            workspace=self.fwd_ws, dev_status=self.dev_status, stream=stream)[0]
+
+    def backward(self, dy, stream=None):
+        return moe_lora_bwd(self.d, self.rt, dy, *self._wts(), self.saved, dx=self.dx, grads=self.grads,
+                            workspace=self.bwd_ws, dev_status=self.dev_status, stream=stream)
+
+    def step(self, topk_idx, topk_w, x, dy, stream=None):
+        self.route(topk_idx, topk_w, stream)
+        self.forward(x, stream)
+        return self.backward(dy, stream)

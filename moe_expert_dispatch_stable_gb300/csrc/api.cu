@@ -1,0 +1,375 @@
+// C ABI of the MoE-LoRA expert layer: argument checks, buffer carving and the
+// launch sequences of route / forward / backward.  Nothing here waits on the
+// device or copies to the host.
+#include "common.cuh"
+#include "kernels.h"
+
+#include <mutex>
+#include <string.h>
+#include <vector>
+
+using namespace moe;
+
+namespace {
+
+// ---- diagnostics: per-kernel CUDA-event timing and a launch counter
+struct TimedLaunch {
+    const char* name;
+    cudaEvent_t start, stop;
+};
+
+struct Timing {
+    std::mutex mu;
+    bool on = false;
+    std::vector<TimedLaunch> pool;   // events are created once and reused
+    size_t used = 0;
+    unsigned long long launches = 0;
+};
+
+Timing& timing() {
+    static Timing t;
+    return t;
+}
+
+// Run one kernel-launching expression, bracketed by events when timing is on.
+template <typename F>
+cudaError_t timed(const char* name, cudaStream_t s, F&& f, int n_ops = 1) {
+    Timing& t = timing();
+    TimedLaunch* slot = nullptr;
+    {
+        std::lock_guard<std::mutex> g(t.mu);
+        t.launches += n_ops;
+        if (t.on) {
+            if (t.used == t.pool.size()) {
+                TimedLaunch tl{name, nullptr, nullptr};
+                if (cudaEventCreate(&tl.start) != cudaSuccess || cudaEventCreate(&tl.stop) != cudaSuccess)
+                    return cudaErrorMemoryAllocation;
+                t.pool.push_back(tl);
+            }
+            slot = &t.pool[t.used++];
+            slot->name = name;
+        }
+    }
+    if (slot) cudaEventRecord(slot->start, s);
+    cudaError_t e = f();
+    if (slot) cudaEventRecord(slot->stop, s);
+    return e;
+}
+
+constexpr size_t kAlign = 256;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_dims(const moe_dims* d) {
+    if (d == nullptr) return MOE_ERR_NULL_ARG;
+    if (d->T < 0 || d->k < 1 || d->E < 1 || d->k > d->E || d->E > 1024) return MOE_ERR_BAD_DIMS;
+    if (d->H <= 0 || d->I <= 0 || d->H % 64 != 0 || d->I % 64 != 0) return MOE_ERR_BAD_DIMS;
+    if (d->r < 1 || d->r > 64) return MOE_ERR_BAD_DIMS;
+    if (d->T * (int64_t)d->k >= (int64_t(1) << 31)) return MOE_ERR_BAD_DIMS;
+    return MOE_OK;
+}
+
+moe_status check_routing(const moe_routing* rt) {
+    if (rt == nullptr || rt->perm == nullptr || rt->inv_perm == nullptr || rt->counts == nullptr ||
+        rt->offsets == nullptr || rt->tile_offsets == nullptr || rt->w_sorted == nullptr)
+        return MOE_ERR_NULL_ARG;
+    if (!aligned16(rt->perm) || !aligned16(rt->inv_perm) || !aligned16(rt->w_sorted))
+        return MOE_ERR_MISALIGNED;
+    return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+struct SavedLayout {
+    size_t x_perm, gu, h, xa, ha, total;
+    int rp;
+};
+
+SavedLayout saved_layout(const moe_dims* d) {
+    const size_t N = (size_t)d->T * d->k;
+    SavedLayout L;
+    L.rp = lora_rp(d->r);
+    size_t o = 0;
+    L.x_perm = o; o = align_up(o + N * d->H * 2, kAlign);
+    L.gu = o;     o = align_up(o + N * 2 * d->I * 2, kAlign);
+    L.h = o;      o = align_up(o + N * d->I * 2, kAlign);
+    L.xa = o;     o = align_up(o + N * L.rp * 2, kAlign);
+    L.ha = o;     o = align_up(o + N * L.rp * 2, kAlign);
+    L.total = o;
+    return L;
+}
+
+struct FwdWs {
+    size_t o_perm, total;
+};
+
+FwdWs fwd_ws(const moe_dims* d) {
+    const size_t N = (size_t)d->T * d->k;
+    FwdWs W;
+    W.o_perm = 0;
+    W.total = align_up(N * d->H * 4, kAlign);
+    return W;
+}
+
+struct BwdWs {
+    size_t d_o, g_s, dgu, gg_s, dx_perm, total;
+};
+
+BwdWs bwd_ws(const moe_dims* d) {
+    const size_t N = (size_t)d->T * d->k;
+    const int rp = lora_rp(d->r);
+    BwdWs W;
+    size_t o = 0;
+    W.d_o = o;     o = align_up(o + N * d->H * 2, kAlign);
+    W.g_s = o;     o = align_up(o + N * rp * 2, kAlign);
+    W.dgu = o;     o = align_up(o + N * 2 * d->I * 2, kAlign);
+    W.gg_s = o;    o = align_up(o + N * rp * 2, kAlign);
+    W.dx_perm = o; o = align_up(o + N * d->H * 4, kAlign);
+    W.total = o;
+    return W;
+}
+
+#define MOE_TRY(expr)                                  \
+    do {                                               \
+        cudaError_t _e = (expr);                       \
+        if (_e != cudaSuccess) return MOE_ERR_CUDA;    \
+    } while (0)
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return 1; }
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_NULL_ARG: return "a required pointer is NULL";
+        case MOE_ERR_BAD_DIMS: return "sizes outside the supported range";
+        case MOE_ERR_MISALIGNED: return "a pointer is not 16-byte aligned";
+        case MOE_ERR_WORKSPACE: return "workspace or saved buffer too small";
+        case MOE_ERR_CUDA: return "a CUDA call failed";
+        case MOE_ERR_UNSUPPORTED: return "unsupported device or driver";
+        default: return "unknown status";
+    }
+}
+
+moe_status moe_route_workspace_size(int64_t T, int32_t k, int32_t E, size_t* bytes) {
+    if (bytes == nullptr) return MOE_ERR_NULL_ARG;
+    if (T < 0 || k < 1 || E < 1 || k > E || E > 1024 || T * (int64_t)k >= (int64_t(1) << 31))
+        return MOE_ERR_BAD_DIMS;
+    *bytes = route_workspace_bytes(T * (int64_t)k, E);
+    return MOE_OK;
+}
+
+moe_status moe_route(const void* topk_idx, int32_t idx_bytes, const float* topk_w, int64_t T, int32_t k,
+                     int32_t E, const moe_routing* out, void* workspace, size_t workspace_bytes,
+                     int32_t* dev_status, void* stream) {
+    size_t need = 0;
+    moe_status st = moe_route_workspace_size(T, k, E, &need);
+    if (st != MOE_OK) return st;
+    if (idx_bytes != 4 && idx_bytes != 8) return MOE_ERR_BAD_DIMS;
+    if ((T > 0 && (topk_idx == nullptr || topk_w == nullptr)) || workspace == nullptr || dev_status == nullptr)
+        return MOE_ERR_NULL_ARG;
+    if ((st = check_routing(out)) != MOE_OK) return st;
+    if (!aligned16(workspace) || (T > 0 && (!aligned16(topk_idx) || !aligned16(topk_w))))
+        return MOE_ERR_MISALIGNED;
+    if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
+    return cuda_status(timed("route", (cudaStream_t)stream, [&] {
+        return launch_route(topk_idx, idx_bytes, topk_w, T * (int64_t)k, E, *out, workspace, dev_status,
+                            (cudaStream_t)stream);
+    }, T > 0 ? 3 : 2));
+}
+
+moe_status moe_lora_fwd_sizes(const moe_dims* d, size_t* saved_bytes, size_t* workspace_bytes) {
+    moe_status st = check_dims(d);
+    if (st != MOE_OK) return st;
+    if (saved_bytes == nullptr || workspace_bytes == nullptr) return MOE_ERR_NULL_ARG;
+    *saved_bytes = saved_layout(d).total;
+    *workspace_bytes = fwd_ws(d).total;
+    return MOE_OK;
+}
+
+moe_status moe_lora_saved_layout(const moe_dims* d, size_t offsets[5], int32_t* rp) {
+    moe_status st = check_dims(d);
+    if (st != MOE_OK) return st;
+    if (offsets == nullptr || rp == nullptr) return MOE_ERR_NULL_ARG;
+    const SavedLayout L = saved_layout(d);
+    offsets[0] = L.x_perm; offsets[1] = L.gu; offsets[2] = L.h; offsets[3] = L.xa; offsets[4] = L.ha;
+    *rp = L.rp;
+    return MOE_OK;
+}
+
+moe_status moe_lora_bwd_workspace_size(const moe_dims* d, size_t* bytes) {
+    moe_status st = check_dims(d);
+    if (st != MOE_OK) return st;
+    if (bytes == nullptr) return MOE_ERR_NULL_ARG;
+    *bytes = bwd_ws(d).total;
+    return MOE_OK;
+}
+
+moe_status moe_lora_fwd(const moe_dims* d, const moe_routing* rt, const uint16_t* x, const uint16_t* W_gu,
+                        const uint16_t* A_gu, const uint16_t* B_gu, const uint16_t* W_d, const uint16_t* A_d,
+                        const uint16_t* B_d, uint16_t* y, void* saved, size_t saved_bytes, void* workspace,
+                        size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    moe_status st = check_dims(d);
+    if (st != MOE_OK) return st;
+    if ((st = check_routing(rt)) != MOE_OK) return st;
+    const void* ptrs[] = {x, W_gu, A_gu, B_gu, W_d, A_d, B_d, y, saved, workspace, dev_status};
+    for (const void* p : ptrs) if (p == nullptr) return MOE_ERR_NULL_ARG;
+    for (const void* p : ptrs) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    const SavedLayout L = saved_layout(d);
+    const FwdWs W = fwd_ws(d);
+    if (saved_bytes < L.total || workspace_bytes < W.total) return MOE_ERR_WORKSPACE;
+    const int64_t N = d->T * (int64_t)d->k;
+    if (N == 0) return MOE_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* sv = (char*)saved;
+    void* x_perm = sv + L.x_perm;
+    void* GU = sv + L.gu;
+    void* h = sv + L.h;
+    void* XA = sv + L.xa;
+    void* HA = sv + L.ha;
+    float* O = (float*)((char*)workspace + W.o_perm);
+    const int H = d->H, I = d->I, E = d->E, r = d->r;
+
+    MOE_TRY(timed("gather_x", s, [&] { return launch_gather_rows(x, H, rt->perm, nullptr, N, d->k, x_perm, s); }));
+    MOE_TRY(timed("proj_xa", s, [&] { return launch_lora_project(x_perm, H, A_gu, r, L.rp, d->scale, rt->offsets, E, N, XA, s); }));
+
+    GroupedGemm g{};
+    g.N = N; g.E = E; g.offsets = rt->offsets; g.tile_offsets = rt->tile_offsets; g.dev_status = dev_status;
+    // gate_up: GU = x_perm W_gu[e] + XA_s B_gu[e]; h = silu(g) * u
+    g.K = H; g.Ncols = I; g.A = x_perm;
+    g.B = W_gu; g.b_mn_major = true; g.ldb = 2 * I; g.b_expert_stride = (int64_t)H * 2 * I;
+    g.A2 = XA; g.rp = L.rp; g.r = r; g.B2 = B_gu; g.ldb2 = 2 * I; g.b2_expert_stride = (int64_t)r * 2 * I;
+    g.out0 = GU; g.out1 = h; g.epi = EPI_SWIGLU;
+    MOE_TRY(timed("gemm_gate_up_fwd", s, [&] { return launch_grouped_gemm(g, s); }));
+
+    MOE_TRY(timed("proj_ha", s, [&] { return launch_lora_project(h, I, A_d, r, L.rp, d->scale, rt->offsets, E, N, HA, s); }));
+    // down: O = w * (h W_d[e] + HA_s B_d[e])
+    GroupedGemm g2{};
+    g2.N = N; g2.E = E; g2.offsets = rt->offsets; g2.tile_offsets = rt->tile_offsets; g2.dev_status = dev_status;
+    g2.K = I; g2.Ncols = H; g2.A = h;
+    g2.B = W_d; g2.b_mn_major = true; g2.ldb = H; g2.b_expert_stride = (int64_t)I * H;
+    g2.A2 = HA; g2.rp = L.rp; g2.r = r; g2.B2 = B_d; g2.ldb2 = H; g2.b2_expert_stride = (int64_t)r * H;
+    g2.w_sorted = rt->w_sorted; g2.out0 = O; g2.ldo = H; g2.epi = EPI_ROWSCALE_F32;
+    MOE_TRY(timed("gemm_down_fwd", s, [&] { return launch_grouped_gemm(g2, s); }));
+
+    MOE_TRY(timed("combine_y", s, [&] { return launch_combine(O, rt->inv_perm, d->T, d->k, H, y, s); }));
+    return MOE_OK;
+}
+
+moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt, const uint16_t* dy, const uint16_t* W_gu,
+                        const uint16_t* A_gu, const uint16_t* B_gu, const uint16_t* W_d, const uint16_t* A_d,
+                        const uint16_t* B_d, const void* saved, size_t saved_bytes, uint16_t* dx,
+                        uint16_t* dA_gu, uint16_t* dB_gu, uint16_t* dA_d, uint16_t* dB_d, void* workspace,
+                        size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    moe_status st = check_dims(d);
+    if (st != MOE_OK) return st;
+    if ((st = check_routing(rt)) != MOE_OK) return st;
+    const void* ptrs[] = {dy, W_gu, A_gu, B_gu, W_d, A_d, B_d, saved, dx, dA_gu, dB_gu, dA_d, dB_d,
+                          workspace, dev_status};
+    for (const void* p : ptrs) if (p == nullptr) return MOE_ERR_NULL_ARG;
+    for (const void* p : ptrs) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    const SavedLayout L = saved_layout(d);
+    const BwdWs W = bwd_ws(d);
+    if (saved_bytes < L.total || workspace_bytes < W.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int64_t N = d->T * (int64_t)d->k;
+    const int H = d->H, I = d->I, E = d->E, r = d->r;
+    if (N == 0) {
+        MOE_TRY(cudaMemsetAsync(dA_gu, 0, (size_t)E * r * H * 2, s));
+        MOE_TRY(cudaMemsetAsync(dB_gu, 0, (size_t)E * r * 2 * I * 2, s));
+        MOE_TRY(cudaMemsetAsync(dA_d, 0, (size_t)E * r * I * 2, s));
+        MOE_TRY(cudaMemsetAsync(dB_d, 0, (size_t)E * r * H * 2, s));
+        return MOE_OK;
+    }
+    const char* sv = (const char*)saved;
+    const void* x_perm = sv + L.x_perm;
+    const void* GU = sv + L.gu;
+    const void* h = sv + L.h;
+    const void* XA = sv + L.xa;
+    const void* HA = sv + L.ha;
+    char* ws = (char*)workspace;
+    void* dO = ws + W.d_o;
+    void* G = ws + W.g_s;
+    void* dGU = ws + W.dgu;
+    void* Gg = ws + W.gg_s;
+    float* dXp = (float*)(ws + W.dx_perm);
+
+    // dO = w * dy[token]
+    MOE_TRY(timed("gather_dy", s, [&] { return launch_gather_rows(dy, H, rt->perm, rt->w_sorted, N, d->k, dO, s); }));
+    // G_s = s * dO B_d^T
+    MOE_TRY(timed("proj_g", s, [&] { return launch_lora_project(dO, H, B_d, r, L.rp, d->scale, rt->offsets, E, N, G, s); }));
+    // dh = dO W_d[e]^T + G_s A_d[e]  ->  dGU = SwiGLU'(GU) dh
+    GroupedGemm g{};
+    g.N = N; g.E = E; g.offsets = rt->offsets; g.tile_offsets = rt->tile_offsets; g.dev_status = dev_status;
+    g.K = H; g.Ncols = I; g.A = dO;
+    g.B = W_d; g.b_mn_major = false; g.ldb = H; g.b_expert_stride = (int64_t)I * H;
+    g.A2 = G; g.rp = L.rp; g.r = r; g.B2 = A_d; g.ldb2 = I; g.b2_expert_stride = (int64_t)r * I;
+    g.gu_in = GU; g.out0 = dGU; g.epi = EPI_DSWIGLU;
+    MOE_TRY(timed("gemm_down_bwd", s, [&] { return launch_grouped_gemm(g, s); }));
+    // dA_d = G_s^T h ; dB_d = HA_s^T dO
+    MOE_TRY(timed("wgrad_dA_d", s, [&] { return launch_lora_wgrad(G, L.rp, r, h, I, rt->offsets, E, N, dA_d, nullptr, 0, s); }));
+    MOE_TRY(timed("wgrad_dB_d", s, [&] { return launch_lora_wgrad(HA, L.rp, r, dO, H, rt->offsets, E, N, dB_d, nullptr, 0, s); }));
+    // Gg_s = s * dGU B_gu^T
+    MOE_TRY(timed("proj_gg", s, [&] { return launch_lora_project(dGU, 2 * I, B_gu, r, L.rp, d->scale, rt->offsets, E, N, Gg, s); }));
+    // dX_perm = dGU W_gu[e]^T + Gg_s A_gu[e]
+    GroupedGemm g2{};
+    g2.N = N; g2.E = E; g2.offsets = rt->offsets; g2.tile_offsets = rt->tile_offsets; g2.dev_status = dev_status;
+    g2.K = 2 * I; g2.Ncols = H; g2.A = dGU;
+    g2.B = W_gu; g2.b_mn_major = false; g2.ldb = 2 * I; g2.b_expert_stride = (int64_t)H * 2 * I;
+    g2.A2 = Gg; g2.rp = L.rp; g2.r = r; g2.B2 = A_gu; g2.ldb2 = H; g2.b2_expert_stride = (int64_t)r * H;
+    g2.out0 = dXp; g2.ldo = H; g2.epi = EPI_F32;
+    MOE_TRY(timed("gemm_gate_up_bwd", s, [&] { return launch_grouped_gemm(g2, s); }));
+    MOE_TRY(timed("combine_dx", s, [&] { return launch_combine(dXp, rt->inv_perm, d->T, d->k, H, dx, s); }));
+    // dA_gu = Gg_s^T x_perm ; dB_gu = XA_s^T dGU
+    MOE_TRY(timed("wgrad_dA_gu", s, [&] { return launch_lora_wgrad(Gg, L.rp, r, x_perm, H, rt->offsets, E, N, dA_gu, nullptr, 0, s); }));
+    MOE_TRY(timed("wgrad_dB_gu", s, [&] { return launch_lora_wgrad(XA, L.rp, r, dGU, 2 * I, rt->offsets, E, N, dB_gu, nullptr, 0, s); }));
+    return MOE_OK;
+}
+
+moe_status moe_timing_enable(int32_t on) {
+    Timing& t = timing();
+    std::lock_guard<std::mutex> g(t.mu);
+    t.on = on != 0;
+    t.used = 0;
+    return MOE_OK;
+}
+
+moe_status moe_timing_read(int32_t index, char* name, size_t name_len, double* total_ms, int32_t* launches) {
+    if (name == nullptr || total_ms == nullptr || launches == nullptr || name_len == 0) return MOE_ERR_NULL_ARG;
+    Timing& t = timing();
+    std::lock_guard<std::mutex> g(t.mu);
+    // distinct names in first-seen order
+    std::vector<const char*> names;
+    for (size_t i = 0; i < t.used; ++i) {
+        bool seen = false;
+        for (const char* n : names) seen = seen || strcmp(n, t.pool[i].name) == 0;
+        if (!seen) names.push_back(t.pool[i].name);
+    }
+    if (index < 0 || (size_t)index >= names.size()) return MOE_ERR_BAD_DIMS;
+    double ms = 0.0;
+    int32_t n = 0;
+    for (size_t i = 0; i < t.used; ++i) {
+        if (strcmp(t.pool[i].name, names[index]) != 0) continue;
+        if (cudaEventSynchronize(t.pool[i].stop) != cudaSuccess) return MOE_ERR_CUDA;
+        float e = 0.f;
+        if (cudaEventElapsedTime(&e, t.pool[i].start, t.pool[i].stop) != cudaSuccess) return MOE_ERR_CUDA;
+        ms += e;
+        ++n;
+    }
+    strncpy(name, names[index], name_len - 1);
+    name[name_len - 1] = 0;
+    *total_ms = ms;
+    *launches = n;
+    return MOE_OK;
+}
+
+uint64_t moe_launch_count(void) {
+    Timing& t = timing();
+    std::lock_guard<std::mutex> g(t.mu);
+    return t.launches;
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// Internal launch interface between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_lora.h"
+
+namespace moe {
+
+// ---- routing (route.cu)
+size_t route_workspace_bytes(int64_t N, int E);
+cudaError_t launch_route(const void* idx, int idx_bytes, const float* topk_w, int64_t N, int E,
+                         const moe_routing& out, void* ws, int32_t* dev_status, cudaStream_t s);
+
+// ---- row kernels (rowops.cu)
+// dst[p, :] = src[perm[p] / k, :]   (optionally scaled by w_sorted[p], rounded to bf16)
+cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, const float* w_sorted,
+                               int64_t N, int k, void* dst, cudaStream_t s);
+// out[t, :] = bf16( sum_{j<k} src[inv_perm[t*k+j], :] )  (fp32 src, fixed j order)
+cudaError_t launch_combine(const float* src, const int32_t* inv_perm, int64_t T, int k, int H,
+                           void* out, cudaStream_t s);
+// P[p, j] = s * sum_c In[p, c] * Wt[e(p), j, c] for j < r, 0 for r <= j < RP  (bf16 out)
+cudaError_t launch_lora_project(const void* In, int K, const void* Wt, int r, int rp, float scale,
+                                const int32_t* offsets, int E, int64_t N, void* P, cudaStream_t s);
+// D[e, j, m] = sum_{p in e} Small[p, j] * Big[p, m]  (bf16 out [E, r, M]); fixed row order
+cudaError_t launch_lora_wgrad(const void* Small, int rp, int r, const void* Big, int M,
+                              const int32_t* offsets, int E, int64_t N, void* D, float* partial,
+                              size_t partial_elems, cudaStream_t s);
+size_t lora_wgrad_partial_elems(int64_t N, int E, int M, int rp);
+
+// ---- grouped GEMMs
+enum GemmEpi : int {
+    EPI_SWIGLU = 0,     // paired gate/up accumulators -> GU (bf16, [N,2I]) and h (bf16, [N,I])
+    EPI_ROWSCALE_F32 = 1,  // out_f32[p, n] = w_sorted[p] * acc
+    EPI_DSWIGLU = 2,    // acc = dh; reads GU, writes dGU (bf16 [N,2I])
+    EPI_F32 = 3         // out_f32[p, n] = acc
+};
+
+struct GroupedGemm {
+    // problem: for every expert e and sorted row p in [offsets[e], offsets[e+1]):
+    //   acc[p, n] = sum_c A[p, c] B_e(c, n) + sum_j A2[p, j] B2_e(j, n),  n < Ncols
+    // (for EPI_SWIGLU a second accumulator uses B columns n + Ncols: the "up" half)
+    int64_t N;            // total sorted rows
+    int E;
+    int K;                // contraction length of the main product
+    int Ncols;            // logical output columns
+    const void* A;        // [N, K] bf16, K contiguous
+    const void* B;        // bf16 expert stack
+    bool b_mn_major;      // true: B_e(c, n) = B[e][c][n] (row length ldb); false: B[e][n][c]
+    int ldb;              // elements per row of B[e]
+    int64_t b_expert_stride;  // elements between experts
+    const void* A2;       // [N, RP] bf16 (LoRA rank activations, pre-scaled by s), or null
+    int rp;               // row length of A2
+    int r;                // contraction length of the LoRA product
+    const void* B2;       // [E][r][ldb2] bf16 (MN-major), or null
+    int ldb2;
+    int64_t b2_expert_stride;
+    const int32_t* offsets;      // [E+1]
+    const int32_t* tile_offsets; // [E+1], 128-row tiles
+    const float* w_sorted;       // EPI_ROWSCALE_F32
+    const void* gu_in;           // EPI_DSWIGLU: GU [N, 2*Ncols]
+    void* out0;                  // EPI_SWIGLU: GU; EPI_DSWIGLU: dGU; F32 epilogues: float out
+    void* out1;                  // EPI_SWIGLU: h
+    int ldo;                     // row length of the fp32 output
+    int epi;
+    int32_t* dev_status;
+};
+
+// Product engine (tcgen05 / TMEM / TMA persistent kernel).
+cudaError_t launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s);
+// CUDA-core engine with the same semantics (numerics reference for tests).
+cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,217 @@
+// Routing: group the T*k routed slots by expert, on the device, with no host sync.
+//
+// The Unsloth x NVIDIA blog post (section "core idea / structure / how it
+// works", GPT-OSS MoE routing paragraphs) replaces one torch.where query per
+// expert by: flatten the top-k assignment, stable-sort it by expert id,
+// bincount once, slice by offsets.  Here the three steps are two kernels:
+//
+//   route_count   each CTA histograms a 4096-slot chunk (warp-aggregated with
+//                 __match_any_sync into shared-memory counters) and writes its
+//                 per-expert counts; the last CTA to finish (atomic ticket after
+//                 a fence; no spinning) sums them, scans them to offsets and
+//                 tile offsets and turns the per-CTA counts into each CTA's
+//                 starting position inside every expert segment.
+//   route_scatter each CTA re-reads its chunk; every warp owns a contiguous
+//                 256-slot sub-chunk, so a slot's position is
+//                   CTA base[e] + earlier warps' count[e] + earlier rounds' count[e]
+//                   + lanes below it with the same expert (popc of the match mask)
+//                 which is exactly its rank among equal keys in flat order: a
+//                 stable counting sort.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kRouteChunk = 4096;
+constexpr int kCountThreads = 1024;
+constexpr int kScatterThreads = 512;                  // 16 warps x 256 slots
+constexpr int kScatterWarps = kScatterThreads / 32;
+constexpr int kSlotsPerWarp = kRouteChunk / kScatterWarps;
+
+template <typename IdxT>
+__device__ __forceinline__ int load_expert(const IdxT* idx, int64_t i, int64_t end, int E, bool& bad) {
+    if (i >= end) return -1;
+    long long v = (long long)idx[i];
+    if (v < 0 || v >= E) { bad = true; return -1; }
+    return (int)v;
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
+__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += n;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = (blockDim.x + 31) >> 5;
+        int s = lane < nw ? warp_sums[lane] : 0;
+        int si = s;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, si, d);
+            if (lane >= d) si += n;
+        }
+        if (lane < nw) warp_sums[lane] = si - s;      // exclusive warp offsets
+        if (lane == nw - 1) *total = si;
+    }
+    __syncthreads();
+    int out = warp_sums[warp] + incl - v;
+    __syncthreads();
+    return out;
+}
+
+template <typename IdxT>
+__global__ void __launch_bounds__(kCountThreads)
+route_count_kernel(const IdxT* __restrict__ idx, int64_t N, int E,
+                   int32_t* __restrict__ block_counts, unsigned int* __restrict__ ticket,
+                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                   int32_t* __restrict__ tile_offsets, int32_t* __restrict__ dev_status) {
+    extern __shared__ int32_t hist[];                  // [E]
+    __shared__ int warp_sums[32];
+    __shared__ int scan_total;
+    __shared__ bool is_last;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+
+    const int64_t beg = (int64_t)blockIdx.x * kRouteChunk;
+    const int64_t end = min(N, beg + kRouteChunk);
+    bool bad = false;
+    for (int64_t base = beg; base < end; base += blockDim.x) {   // uniform trip count
+        const int e = load_expert(idx, base + threadIdx.x, end, E, bad);
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[e], __popc(peers));
+    }
+    if (bad) atomicOr(dev_status, MOE_DEV_BAD_EXPERT_ID);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) block_counts[(int64_t)blockIdx.x * E + e] = hist[e];
+
+    // last CTA to arrive does the scan (threadFenceReduction pattern, no waiting)
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = (atomicAdd(ticket, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+
+    const int nb = gridDim.x;
+    const int e = threadIdx.x;                         // E <= blockDim.x
+    int run = 0;
+    if (e < E) {
+        for (int b = 0; b < nb; ++b) {
+            int32_t* p = block_counts + (int64_t)b * E + e;
+            const int c = __ldcg(p);
+            *p = run;                                  // exclusive within expert e
+            run += c;
+        }
+    }
+    const int off = block_exclusive_scan(e < E ? run : 0, warp_sums, &scan_total);
+    const int tiles = e < E ? (run + kTileM - 1) / kTileM : 0;
+    const int toff = block_exclusive_scan(tiles, warp_sums, &scan_total);
+    if (e < E) {
+        counts[e] = run;
+        offsets[e] = off;
+        tile_offsets[e] = toff;
+        for (int b = 0; b < nb; ++b) block_counts[(int64_t)b * E + e] += off;   // absolute CTA base
+    }
+    if (e == E - 1) {
+        offsets[E] = off + run;
+        tile_offsets[E] = toff + tiles;
+    }
+    if (threadIdx.x == 0) *ticket = 0u;                // leave the ticket ready for the next call
+}
+
+template <typename IdxT>
+__global__ void __launch_bounds__(kScatterThreads)
+route_scatter_kernel(const IdxT* __restrict__ idx, const float* __restrict__ topk_w, int64_t N, int E,
+                     const int32_t* __restrict__ block_base,
+                     int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm,
+                     float* __restrict__ w_sorted) {
+    extern __shared__ int32_t wcnt[];                  // [kScatterWarps][E]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) wcnt[i] = 0;
+    __syncthreads();
+
+    const int64_t beg = (int64_t)blockIdx.x * kRouteChunk;
+    const int64_t end = min(N, beg + kRouteChunk);
+    const int64_t wbeg = beg + (int64_t)warp * kSlotsPerWarp;
+    int32_t* my = wcnt + warp * E;
+    bool bad = false;
+    // 1) per-warp histogram of its sub-chunk
+    for (int rr = 0; rr < kSlotsPerWarp; rr += 32) {
+        const int e = load_expert(idx, wbeg + rr + lane, min(end, wbeg + kSlotsPerWarp), E, bad);
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    // 2) exclusive scan over warps, seeded with this CTA's base inside each segment
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = block_base[(int64_t)blockIdx.x * E + e];
+        for (int w = 0; w < kScatterWarps; ++w) {
+            const int c = wcnt[w * E + e];
+            wcnt[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    // 3) rank = running base + lanes below with the same expert
+    const unsigned lt = (1u << lane) - 1u;
+    for (int rr = 0; rr < kSlotsPerWarp; rr += 32) {
+        const int64_t i = wbeg + rr + lane;
+        const int e = load_expert(idx, i, min(end, wbeg + kSlotsPerWarp), E, bad);
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        int pos = 0;
+        if (e >= 0) pos = my[e] + __popc(peers & lt);
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+        __syncwarp();
+        if (e >= 0) {
+            perm[pos] = (int32_t)i;
+            inv_perm[i] = pos;
+            w_sorted[pos] = topk_w[i];
+        }
+    }
+}
+
+size_t route_workspace_bytes(int64_t N, int E) {
+    const int64_t nb = N > 0 ? (N + kRouteChunk - 1) / kRouteChunk : 1;
+    return align_up((size_t)nb * E * sizeof(int32_t), 256) + 256;
+}
+
+cudaError_t launch_route(const void* idx, int idx_bytes, const float* topk_w, int64_t N, int E,
+                         const moe_routing& out, void* ws, int32_t* dev_status, cudaStream_t s) {
+    const int nb = N > 0 ? (int)((N + kRouteChunk - 1) / kRouteChunk) : 1;
+    int32_t* block_counts = (int32_t*)ws;
+    unsigned int* ticket = (unsigned int*)((char*)ws + align_up((size_t)nb * E * sizeof(int32_t), 256));
+    cudaError_t err = cudaMemsetAsync(ticket, 0, sizeof(unsigned int), s);
+    if (err != cudaSuccess) return err;
+    const size_t sm_count = (size_t)E * sizeof(int32_t);
+    const size_t sm_scatter = (size_t)kScatterWarps * E * sizeof(int32_t);
+    if (idx_bytes == 8) {
+        auto kc = route_count_kernel<long long>;
+        auto ks = route_scatter_kernel<long long>;
+        cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scatter);
+        kc<<<nb, kCountThreads, sm_count, s>>>((const long long*)idx, N, E, block_counts, ticket,
+                                                 out.counts, out.offsets, out.tile_offsets, dev_status);
+        if (N > 0)
+            ks<<<nb, kScatterThreads, sm_scatter, s>>>((const long long*)idx, topk_w, N, E, block_counts,
+                                                       out.perm, out.inv_perm, out.w_sorted);
+    } else {
+        auto kc = route_count_kernel<int32_t>;
+        auto ks = route_scatter_kernel<int32_t>;
+        cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scatter);
+        kc<<<nb, kCountThreads, sm_count, s>>>((const int32_t*)idx, N, E, block_counts, ticket,
+                                                 out.counts, out.offsets, out.tile_offsets, dev_status);
+        if (N > 0)
+            ks<<<nb, kScatterThreads, sm_scatter, s>>>((const int32_t*)idx, topk_w, N, E, block_counts,
+                                                       out.perm, out.inv_perm, out.w_sorted);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

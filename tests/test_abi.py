@@ -1,0 +1,108 @@
+"""The C-ABI library builds, loads and exports every symbol its header declares;
+host-side argument checks return their status codes without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")]
+
+
+def _declared_symbols():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        names.update(re.findall(r"^MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from moe_expert_dispatch_stable_gb300 import build
+    path = build.build()
+    from moe_expert_dispatch_stable_gb300 import binding
+    return binding.load_library(path)
+
+
+def test_header_declares_the_three_operations():
+    names = _declared_symbols()
+    assert {"moe_route", "moe_lora_fwd", "moe_lora_bwd"} <= names
+    assert len(names) >= 9
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in sorted(_declared_symbols()):
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.moe_abi_version() == 1
+    for code in range(0, 7):
+        assert lib.moe_status_string(code)
+
+
+def test_size_queries_and_dim_checks(lib):
+    from moe_expert_dispatch_stable_gb300 import binding as b
+    n = ctypes.c_size_t()
+    assert lib.moe_route_workspace_size(4096, 4, 32, ctypes.byref(n)) == 0 and n.value > 0
+    assert lib.moe_route_workspace_size(4096, 4, 2048, ctypes.byref(n)) == 2       # E > 1024
+    assert lib.moe_route_workspace_size(4096, 5, 4, ctypes.byref(n)) == 2          # k > E
+    assert lib.moe_route_workspace_size(-1, 1, 4, ctypes.byref(n)) == 2
+    assert lib.moe_route_workspace_size(4096, 4, 32, None) == 1
+    ok = b.Dims(T=4096, H=2880, I=2880, E=32, k=4, r=16, scale=2.0)
+    saved, ws = b.moe_lora_fwd_sizes(ok)
+    N = 4096 * 4
+    assert saved >= N * 2880 * 2 + N * 5760 * 2 + N * 2880 * 2 + 2 * N * 16 * 2
+    assert ws >= N * 2880 * 4
+    assert b.moe_lora_bwd_workspace_size(ok) >= N * (2880 * 2 + 5760 * 2 + 2880 * 4)
+    offs, rp = b.moe_lora_saved_layout(ok)
+    assert rp == 16 and offs[0] == 0 and all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert b.moe_lora_saved_layout(b.Dims(64, 128, 256, 8, 2, 8, 2.0))[1] == 16
+    assert b.moe_lora_saved_layout(b.Dims(64, 128, 256, 8, 2, 32, 2.0))[1] == 32
+    for bad in [dict(H=100), dict(I=96 + 1), dict(r=0), dict(r=65), dict(k=40), dict(E=0)]:
+        d = b.Dims(**{**ok.__dict__, **bad})
+        with pytest.raises(b.MoEError):
+            b.moe_lora_fwd_sizes(d)
+
+
+def test_null_and_misaligned_arguments_rejected_before_launch(lib):
+    from moe_expert_dispatch_stable_gb300 import binding as b
+    rt = b.moe_routing(16, 16, 16, 16, 16, 16)
+    # NULL topk_idx with T > 0
+    assert lib.moe_route(None, 4, ctypes.c_void_p(16), 8, 2, 4, ctypes.byref(rt), ctypes.c_void_p(16), 1 << 20,
+                         ctypes.c_void_p(16), None) == 1
+    # a NULL routing output
+    rt_bad = b.moe_routing(16, 0, 16, 16, 16, 16)
+    assert lib.moe_route(ctypes.c_void_p(16), 4, ctypes.c_void_p(16), 8, 2, 4, ctypes.byref(rt_bad),
+                         ctypes.c_void_p(16), 1 << 20, ctypes.c_void_p(16), None) == 1
+    # misaligned topk_idx
+    assert lib.moe_route(ctypes.c_void_p(18), 4, ctypes.c_void_p(16), 8, 2, 4, ctypes.byref(rt),
+                         ctypes.c_void_p(16), 1 << 20, ctypes.c_void_p(16), None) == 3
+    # workspace too small
+    assert lib.moe_route(ctypes.c_void_p(16), 4, ctypes.c_void_p(16), 8, 2, 4, ctypes.byref(rt),
+                         ctypes.c_void_p(16), 4, ctypes.c_void_p(16), None) == 4
+    # bad index width
+    assert lib.moe_route(ctypes.c_void_p(16), 2, ctypes.c_void_p(16), 8, 2, 4, ctypes.byref(rt),
+                         ctypes.c_void_p(16), 1 << 20, ctypes.c_void_p(16), None) == 2
+    d = b.Dims(8, 64, 64, 4, 2, 4, 2.0).c_struct()
+    p = [ctypes.c_void_p(16)] * 8
+    assert lib.moe_lora_fwd(ctypes.byref(d), ctypes.byref(rt), *p[:7], None, ctypes.c_void_p(16), 1 << 30,
+                            ctypes.c_void_p(16), 1 << 30, ctypes.c_void_p(16), None) == 1
+    assert lib.moe_lora_fwd(ctypes.byref(d), ctypes.byref(rt), *p, ctypes.c_void_p(16), 1,
+                            ctypes.c_void_p(16), 1 << 30, ctypes.c_void_p(16), None) == 4
+    assert lib.moe_lora_bwd(ctypes.byref(d), ctypes.byref(rt), *p[:7], ctypes.c_void_p(16), 1 << 30,
+                            ctypes.c_void_p(24), *p[:4], ctypes.c_void_p(16), 1 << 30, ctypes.c_void_p(16),
+                            None) == 3
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from moe_expert_dispatch_stable_gb300 import binding as b
+    saved = b._lib
+    try:
+        b._lib = None
+        with pytest.raises(b.MoEError):
+            b.load_library(str(tmp_path / "missing.so"))
+    finally:
+        b._lib = saved

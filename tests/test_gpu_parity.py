@@ -1,0 +1,246 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Routing is compared bit for bit; outputs and gradients within rel-L2 <= 5e-3
+and max-abs <= 2e-2 * max|oracle|.  Small layers are compared element by
+element in full; the five workload shapes at full size are compared on
+sampled tokens (y, dx) and sampled experts (LoRA gradients), which the oracle
+computes exactly per token / per expert.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from oracle import moe_oracle as orc
+from tests.gpu_common import (WEIGHT_NAMES, LazyExperts, assert_close, make_case, run_layer, to64)
+
+pytestmark = pytest.mark.gpu
+
+SMALL_CASES = {
+    "tiny": mi.CONFIGS["tiny"],
+    # several 128-row tiles per expert, ragged row tails, ragged 128-column tail (I = 320)
+    "ragged": mi.MoEConfig("ragged", T=700, H=256, E=6, k=2, I=320, r=16, alpha=32),
+    # E = 1, k = 1: a dense SwiGLU MLP
+    "dense": mi.MoEConfig("dense", T=200, H=192, E=1, k=1, I=128, r=4, alpha=8),
+    # rank 32 (two K=16 LoRA steps), k = E
+    "r32_k_eq_E": mi.MoEConfig("r32", T=90, H=128, E=3, k=3, I=192, r=32, alpha=64),
+    # skewed router: many experts without rows
+    "skew_small": mi.MoEConfig("skew", T=300, H=128, E=32, k=2, I=128, r=8, alpha=16, zipf_s=1.2),
+    # one token
+    "one_token": mi.MoEConfig("one", T=1, H=64, E=4, k=2, I=64, r=2, alpha=4),
+    # rank 64
+    "r64": mi.MoEConfig("r64", T=130, H=128, E=4, k=2, I=128, r=64, alpha=64),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _check_route(layer, idx, E):
+    counts, offsets, perm, inv = orc.route(idx, E)
+    rt = layer.rt
+    assert np.array_equal(rt.counts.cpu().numpy(), counts)
+    assert np.array_equal(rt.offsets.cpu().numpy(), offsets)
+    assert np.array_equal(rt.perm.cpu().numpy(), perm)
+    assert np.array_equal(rt.inv_perm.cpu().numpy(), inv)
+    assert np.array_equal(rt.tile_offsets.cpu().numpy(), orc.tile_offsets(counts, 128))
+    return counts, perm
+
+
+# ------------------------------------------------------------------ routing
+@pytest.mark.parametrize("name", list(mi.CONFIGS))
+@pytest.mark.parametrize("idx_dtype", [torch.int64, torch.int32])
+def test_route_bit_exact(name, idx_dtype):
+    import moe_expert_dispatch_stable_gb300 as moe
+    cfg = mi.CONFIGS[name]
+    for seed in (0, 1):
+        idx, w = mi.make_routing(cfg, seed)
+        rt = moe.moe_route(torch.from_numpy(idx).cuda().to(idx_dtype), torch.from_numpy(w).cuda(), cfg.E)
+        torch.cuda.synchronize()
+        counts, offsets, perm, inv = orc.route(idx, cfg.E)
+        assert np.array_equal(rt.counts.cpu().numpy(), counts)
+        assert np.array_equal(rt.offsets.cpu().numpy(), offsets)
+        assert np.array_equal(rt.tile_offsets.cpu().numpy(), orc.tile_offsets(counts, 128))
+        assert np.array_equal(rt.perm.cpu().numpy(), perm)
+        assert np.array_equal(rt.inv_perm.cpu().numpy(), inv)
+        # routing weights are copied bit for bit
+        assert np.array_equal(rt.w_sorted.cpu().numpy().view(np.uint32), w.reshape(-1)[perm].view(np.uint32))
+
+
+def test_route_edge_cases():
+    import moe_expert_dispatch_stable_gb300 as moe
+    # empty input
+    rt = moe.moe_route(torch.zeros((0, 2), dtype=torch.int64, device="cuda"),
+                       torch.zeros((0, 2), dtype=torch.float32, device="cuda"), 5)
+    torch.cuda.synchronize()
+    assert rt.counts.cpu().tolist() == [0] * 5 and rt.offsets.cpu().tolist() == [0] * 6
+    # E = 1; all slots on one expert; sizes straddling the 4096-slot chunks
+    for N in (1, 4095, 4096, 4097, 3 * 4096 + 5):
+        idx = np.zeros((N, 1), dtype=np.int64)
+        rt = moe.moe_route(torch.from_numpy(idx).cuda(), torch.ones((N, 1), device="cuda"), 1)
+        torch.cuda.synchronize()
+        assert np.array_equal(rt.perm.cpu().numpy(), np.arange(N))
+    # random ids with a heavy expert and E = 1024
+    rng = np.random.default_rng(7)
+    idx = rng.integers(0, 1024, size=(9000, 3))
+    idx[::3, 0] = 1023
+    rt = moe.moe_route(torch.from_numpy(idx).cuda(), torch.rand((9000, 3), device="cuda"), 1024)
+    torch.cuda.synchronize()
+    counts, offsets, perm, inv = orc.route(idx, 1024)
+    assert np.array_equal(rt.perm.cpu().numpy(), perm) and np.array_equal(rt.offsets.cpu().numpy(), offsets)
+
+
+def test_route_out_of_range_id_sets_status_flag():
+    import moe_expert_dispatch_stable_gb300 as moe
+    idx = torch.tensor([[0, 1], [2, 7]], dtype=torch.int64, device="cuda")   # 7 >= E = 4
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rt = moe.moe_route(idx, torch.ones((2, 2), device="cuda"), 4, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & moe.binding.MOE_DEV_BAD_EXPERT_ID
+    assert rt.counts.cpu().tolist() == [1, 1, 1, 0]
+
+
+# ------------------------------------------------------------------ full parity on small layers
+def _oracle_full(cfg, idx, w, ts):
+    c = {k: v.cpu() for k, v in ts.items()}
+    wts = [c[n] for n in WEIGHT_NAMES]
+    y = orc.lora_fwd(c["x"], idx, w, *wts, cfg.scale)
+    grads = orc.lora_bwd(c["dy"], c["x"], idx, w, *wts, cfg.scale)
+    return y, grads
+
+
+@pytest.mark.parametrize("name", list(SMALL_CASES))
+def test_layer_parity_full(name):
+    cfg = SMALL_CASES[name]
+    idx, w, ts = make_case(cfg, seed=0)
+    layer, grads = run_layer(cfg, idx, w, ts)
+    assert int(layer.dev_status.item()) == 0
+    counts, _ = _check_route(layer, idx, cfg.E)
+    y_ref, g_ref = _oracle_full(cfg, idx, w, ts)
+    assert_close("y", to64(layer.y), y_ref)
+    for nm, got, ref in zip(["dx", "dA_gu", "dB_gu", "dA_d", "dB_d"], grads, g_ref):
+        assert_close(nm, to64(got), ref)
+    for e in np.where(counts == 0)[0]:                       # experts without rows: exact zeros
+        for got in grads[1:]:
+            assert torch.count_nonzero(got[e]).item() == 0
+
+
+def test_B_zero_gives_exactly_zero_dA():
+    cfg = SMALL_CASES["ragged"]
+    idx, w, ts = make_case(cfg, seed=3, zero_B=True)
+    layer, grads = run_layer(cfg, idx, w, ts)
+    assert torch.count_nonzero(grads[1]).item() == 0 and torch.count_nonzero(grads[3]).item() == 0
+    y_ref, g_ref = _oracle_full(cfg, idx, w, ts)
+    assert_close("y", to64(layer.y), y_ref)
+    assert_close("dB_gu", to64(grads[2]), g_ref[2])
+    assert_close("dB_d", to64(grads[4]), g_ref[4])
+
+
+def test_intermediates_match_oracle_pieces():
+    """Saved GU and h (sorted row order) against the oracle's per-expert pieces."""
+    import moe_expert_dispatch_stable_gb300 as moe
+    cfg = SMALL_CASES["ragged"]
+    idx, w, ts = make_case(cfg, seed=1)
+    layer, _ = run_layer(cfg, idx, w, ts)
+    d = layer.d
+    offs, rp = moe.moe_lora_saved_layout(d)
+    N = cfg.T * cfg.k
+    sv = layer.saved
+    GU = sv[offs[1]:offs[1] + N * 2 * cfg.I * 2].view(torch.bfloat16).view(N, 2 * cfg.I)
+    h = sv[offs[2]:offs[2] + N * cfg.I * 2].view(torch.bfloat16).view(N, cfg.I)
+    c = {k: v.cpu() for k, v in ts.items()}
+    counts, offsets, perm, _ = orc.route(idx, cfg.E)
+    x = to64(c["x"])
+    for e in range(cfg.E):
+        rows = perm[offsets[e]:offsets[e + 1]] // cfg.k
+        M = orc.merged(to64(c["W_gu"][e]), to64(c["A_gu"][e]), to64(c["B_gu"][e]), cfg.scale)
+        gu_ref = x[rows] @ M
+        assert_close(f"GU[{e}]", to64(GU[offsets[e]:offsets[e + 1]]), gu_ref)
+        assert_close(f"h[{e}]", to64(h[offsets[e]:offsets[e + 1]]), orc.swiglu(gu_ref, cfg.I))
+
+
+def test_bitwise_deterministic_across_runs():
+    cfg = SMALL_CASES["skew_small"]
+    idx, w, ts = make_case(cfg, seed=2)
+    l1, g1 = run_layer(cfg, idx, w, ts)
+    y1 = l1.y.clone(); g1 = [g.clone() for g in g1]
+    l2, g2 = run_layer(cfg, idx, w, ts)
+    assert torch.equal(y1, l2.y)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+
+
+def test_zero_tokens():
+    cfg = mi.MoEConfig("empty", T=0, H=64, E=4, k=2, I=64, r=4, alpha=8)
+    import moe_expert_dispatch_stable_gb300 as moe
+    ts = {n: mi.make_tensor(cfg, n, 0, "cpu").cuda() for n in mi.TENSOR_NAMES}
+    d = moe.Dims(0, 64, 64, 4, 2, 4, 2.0)
+    layer = moe.MoELoRALayer(d, ts)
+    for g in layer.grads:
+        g.fill_(1.0)
+    grads = layer.step(torch.zeros((0, 2), dtype=torch.int64, device="cuda"),
+                       torch.zeros((0, 2), device="cuda"), ts["x"], ts["dy"])
+    torch.cuda.synchronize()
+    for g in grads[1:]:
+        assert torch.count_nonzero(g).item() == 0
+
+
+def test_graph_capture_route_fwd_bwd():
+    """The whole route + forward + backward captures into one CUDA graph (a host
+    sync inside would make capture fail) and replays to the eager result."""
+    cfg = SMALL_CASES["ragged"]
+    idx, w, ts = make_case(cfg, seed=0)
+    import moe_expert_dispatch_stable_gb300 as moe
+    d = moe.Dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r, cfg.scale)
+    layer = moe.MoELoRALayer(d, ts)
+    ti = torch.from_numpy(idx).cuda(); tw = torch.from_numpy(w).cuda()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.step(ti, tw, ts["x"], ts["dy"])                    # warm-up (lazy init outside capture)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    ref = [layer.y.clone()] + [g.clone() for g in (layer.dx, *layer.grads)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.step(ti, tw, ts["x"], ts["dy"])
+    layer.y.zero_(); layer.dx.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    got = [layer.y] + [layer.dx, *layer.grads]
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled
+FULL = ["gptoss20b", "qwen3_30b", "gptoss120b_skew", "dsv3"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_parity_sampled(name):
+    cfg = mi.CONFIGS[name]
+    idx, w, ts = make_case(cfg, seed=0)
+    layer, grads = run_layer(cfg, idx, w, ts)
+    assert int(layer.dev_status.item()) == 0
+    counts, _ = _check_route(layer, idx, cfg.E)
+    rng = np.random.default_rng(0)
+    n_tok = 16 if cfg.H * cfg.I > 10_000_000 else 32
+    toks = np.sort(rng.choice(cfg.T, n_tok, replace=False))
+    nz = np.where(counts > 0)[0]
+    experts = sorted({int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])]), int(rng.choice(nz))})
+    lazy = {n: LazyExperts(ts[n]) for n in WEIGHT_NAMES}
+    x = ts["x"].cpu(); dy = ts["dy"].cpu()
+    wts = [lazy[n] for n in WEIGHT_NAMES]
+    y_ref = orc.lora_fwd(x, idx, w, *wts, cfg.scale, token_subset=toks)
+    assert_close("y[sample]", to64(layer.y)[toks], y_ref[toks])
+    g_ref = orc.lora_bwd(dy, x, idx, w, *wts, cfg.scale, token_subset=toks, expert_subset=experts)
+    assert_close("dx[sample]", to64(grads[0])[toks], g_ref[0][toks])
+    for nm, got, ref in zip(["dA_gu", "dB_gu", "dA_d", "dB_d"], grads[1:], g_ref[1:]):
+        assert_close(f"{nm}[{experts}]", to64(got[experts]), ref[experts])
+    for e in np.where(counts == 0)[0]:
+        for got in grads[1:]:
+            assert torch.count_nonzero(got[e]).item() == 0
