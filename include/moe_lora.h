@@ -24,7 +24,8 @@
  * Conventions for every function:
  *  - All tensors are dense row-major; bf16 tensors are passed as uint16_t*.
  *  - Every pointer is a DEVICE pointer unless stated otherwise, 16-byte aligned,
- *    owned by the caller.  The library allocates no device memory and keeps no
+ *    owned by the caller.  Buffers whose size is a multiple of T (x, y, dy, dx,
+ *    perm, inv_perm, w_sorted, saved, workspaces) may be NULL when T == 0.  The library allocates no device memory and keeps no
  *    state beyond a per-device cache of the SM count and of a driver entry point.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *  - A non-zero return is a host-side error found before anything was enqueued

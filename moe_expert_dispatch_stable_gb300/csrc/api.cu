@@ -69,9 +69,11 @@ moe_status check_dims(const moe_dims* d) {
     return MOE_OK;
 }
 
-moe_status check_routing(const moe_routing* rt) {
-    if (rt == nullptr || rt->perm == nullptr || rt->inv_perm == nullptr || rt->counts == nullptr ||
-        rt->offsets == nullptr || rt->tile_offsets == nullptr || rt->w_sorted == nullptr)
+// perm / inv_perm / w_sorted have N = T*k entries and may be NULL when N == 0.
+moe_status check_routing(const moe_routing* rt, int64_t N) {
+    if (rt == nullptr || rt->counts == nullptr || rt->offsets == nullptr || rt->tile_offsets == nullptr)
+        return MOE_ERR_NULL_ARG;
+    if (N > 0 && (rt->perm == nullptr || rt->inv_perm == nullptr || rt->w_sorted == nullptr))
         return MOE_ERR_NULL_ARG;
     if (!aligned16(rt->perm) || !aligned16(rt->inv_perm) || !aligned16(rt->w_sorted))
         return MOE_ERR_MISALIGNED;
@@ -171,7 +173,7 @@ moe_status moe_route(const void* topk_idx, int32_t idx_bytes, const float* topk_
     if (idx_bytes != 4 && idx_bytes != 8) return MOE_ERR_BAD_DIMS;
     if ((T > 0 && (topk_idx == nullptr || topk_w == nullptr)) || workspace == nullptr || dev_status == nullptr)
         return MOE_ERR_NULL_ARG;
-    if ((st = check_routing(out)) != MOE_OK) return st;
+    if ((st = check_routing(out, T * (int64_t)k)) != MOE_OK) return st;
     if (!aligned16(workspace) || (T > 0 && (!aligned16(topk_idx) || !aligned16(topk_w))))
         return MOE_ERR_MISALIGNED;
     if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
@@ -214,10 +216,15 @@ moe_status moe_lora_fwd(const moe_dims* d, const moe_routing* rt, const uint16_t
                         size_t workspace_bytes, int32_t* dev_status, void* stream) {
     moe_status st = check_dims(d);
     if (st != MOE_OK) return st;
-    if ((st = check_routing(rt)) != MOE_OK) return st;
-    const void* ptrs[] = {x, W_gu, A_gu, B_gu, W_d, A_d, B_d, y, saved, workspace, dev_status};
-    for (const void* p : ptrs) if (p == nullptr) return MOE_ERR_NULL_ARG;
-    for (const void* p : ptrs) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    const int64_t Nr = d->T * (int64_t)d->k;
+    if ((st = check_routing(rt, Nr)) != MOE_OK) return st;
+    // token-sized buffers may be NULL when T == 0
+    const void* tok[] = {x, y, saved, workspace};
+    const void* always[] = {W_gu, A_gu, B_gu, W_d, A_d, B_d, dev_status};
+    for (const void* p : always) if (p == nullptr) return MOE_ERR_NULL_ARG;
+    if (Nr > 0) for (const void* p : tok) if (p == nullptr) return MOE_ERR_NULL_ARG;
+    for (const void* p : always) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    for (const void* p : tok) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
     const SavedLayout L = saved_layout(d);
     const FwdWs W = fwd_ws(d);
     if (saved_bytes < L.total || workspace_bytes < W.total) return MOE_ERR_WORKSPACE;
@@ -266,11 +273,15 @@ moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt, const uint16_t
                         size_t workspace_bytes, int32_t* dev_status, void* stream) {
     moe_status st = check_dims(d);
     if (st != MOE_OK) return st;
-    if ((st = check_routing(rt)) != MOE_OK) return st;
-    const void* ptrs[] = {dy, W_gu, A_gu, B_gu, W_d, A_d, B_d, saved, dx, dA_gu, dB_gu, dA_d, dB_d,
-                          workspace, dev_status};
-    for (const void* p : ptrs) if (p == nullptr) return MOE_ERR_NULL_ARG;
-    for (const void* p : ptrs) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    const int64_t Nr = d->T * (int64_t)d->k;
+    if ((st = check_routing(rt, Nr)) != MOE_OK) return st;
+    // token-sized buffers may be NULL when T == 0
+    const void* tok[] = {dy, saved, dx, workspace};
+    const void* always[] = {W_gu, A_gu, B_gu, W_d, A_d, B_d, dA_gu, dB_gu, dA_d, dB_d, dev_status};
+    for (const void* p : always) if (p == nullptr) return MOE_ERR_NULL_ARG;
+    if (Nr > 0) for (const void* p : tok) if (p == nullptr) return MOE_ERR_NULL_ARG;
+    for (const void* p : always) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    for (const void* p : tok) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
     const SavedLayout L = saved_layout(d);
     const BwdWs W = bwd_ws(d);
     if (saved_bytes < L.total || workspace_bytes < W.total) return MOE_ERR_WORKSPACE;

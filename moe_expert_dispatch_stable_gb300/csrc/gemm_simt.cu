@@ -114,6 +114,4 @@ cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) { return launch_grouped_gemm_simt(g, s); }
-
 }  // namespace moe

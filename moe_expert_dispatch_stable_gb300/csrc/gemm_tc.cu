@@ -1,0 +1,453 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// All experts' weights are one stacked tensor and the group sizes are the
+// routing counts (the Unsloth 2026 wiki page, section "Optimisation 3:
+// grouped_mm and Split-LoRA for MoE training"): one persistent launch covers
+// every (expert, 128-row tile, output-column tile).  The scheduler reads the
+// expert offsets and tile offsets that moe_route wrote to device memory, so
+// the host never learns the group sizes.  Split-LoRA: the rank-r product is
+// one more K step of the same accumulator (A2 = s * x A^T rows, B2 = B), so
+// W + BA is never formed.
+//
+// CTA = 6 warps, one CTA per SM, grid = #SMs:
+//   warp 0      TMA producer (one lane): A [128 x 64] and B [256 x 64] per stage,
+//               4 stages of 48 KB, 128-byte swizzle; the LoRA step loads A2 / B2
+//   warp 1      TMEM allocator + MMA issuer (one lane): 4 x tcgen05.mma
+//               M=128 N=256 K=16 per stage into one of two 256-column fp32
+//               accumulators (double buffer: the epilogue of tile i overlaps
+//               the MMAs of tile i+1)
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 16 columns, fused SwiGLU /
+//               routing-weight scale / SwiGLU backward, masked stores
+// Every mbarrier wait is bounded; a wait that gives up sets MOE_DEV_TIMEOUT.
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kABytes = BM * BK * 2;         // 16 KB
+constexpr int kBBytes = BN * BK * 2;         // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBoxMN = 64 * BK * 2;          // one 64-column MN-major box of B: 8 KB
+constexpr int kAccCols = BN;
+constexpr int kTmemCols = 2 * kAccCols;
+
+struct TcParams {
+    CUtensorMap tm_a, tm_b, tm_a2, tm_b2;
+    GroupedGemm g;
+    int num_kb;         // K / 64
+    int lora_k16;       // RP / 16 (0: no LoRA step)
+    int n_tiles;        // output-column tiles
+    int a2_bytes;       // bytes of the A2 tile
+    int b2_box_bytes;   // bytes of one B2 box (64 columns x RP rows)
+    uint32_t a2_sbo, a2_swz;
+};
+
+__device__ __forceinline__ void decode_tile(int t, int n_tiles, const int32_t* s_toff, int E, int& e, int& mt,
+                                            int& nt) {
+    const int mg = t / n_tiles;
+    nt = t - mg * n_tiles;
+    e = expert_of_row(s_toff, E, mg);
+    mt = mg - s_toff[e];
+}
+
+__device__ __forceinline__ void set_timeout(const GroupedGemm& g, volatile int* s_abort) {
+    *s_abort = 1;
+    atomicOr(g.dev_status, MOE_DEV_TIMEOUT);
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* f) {
+    uint4 v;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    return v;
+}
+
+__device__ __forceinline__ void unpack8_bf16(const uint4& v, float* f) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+template <bool PAIRED>
+__device__ __forceinline__ int b_col(int j, int nt, int ncols) {
+    if (PAIRED) return (j < 2 ? 0 : ncols) + nt * (BN / 2) + (j & 1) * 64;
+    return nt * BN + j * 64;
+}
+
+template <int EPI, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams P) {
+    constexpr bool PAIRED = (EPI == EPI_SWIGLU);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint64_t* empty_bar = full_bar + kStages;
+    uint64_t* tfull_bar = empty_bar + kStages;
+    uint64_t* tempty_bar = tfull_bar + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty_bar + 2);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int32_t* s_off = reinterpret_cast<int32_t*>(tmem_slot + 4);
+    const GroupedGemm& g = P.g;
+    const int E = g.E;
+    int32_t* s_toff = s_off + (E + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+        s_off[i] = g.offsets[i];
+        s_toff[i] = g.tile_offsets[i];
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(tc::smem_u32(&full_bar[s]), 1);
+            tc::mbar_init(tc::smem_u32(&empty_bar[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(tc::smem_u32(&tfull_bar[a]), 1);
+            tc::mbar_init(tc::smem_u32(&tempty_bar[a]), 4);
+        }
+        *s_abort = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tmap(&P.tm_a);
+        tc::prefetch_tmap(&P.tm_b);
+        if (P.lora_k16) {
+            tc::prefetch_tmap(&P.tm_a2);
+            tc::prefetch_tmap(&P.tm_b2);
+        }
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total_tiles = s_toff[E] * P.n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = blockIdx.x; t < total_tiles && !*s_abort; t += gridDim.x) {
+                int e, mt, nt;
+                decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
+                const int m0 = s_off[e] + mt * BM;
+                const int nkb = P.num_kb + (P.lora_k16 ? 1 : 0);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    const uint32_t fb = tc::smem_u32(&full_bar[stage]);
+                    if (!tc::mbar_wait(tc::smem_u32(&empty_bar[stage]), phase ^ 1)) {
+                        set_timeout(g, s_abort);
+                        break;
+                    }
+                    const uint32_t sa = tc::smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sb = sa + kABytes;
+                    if (kb < P.num_kb) {
+                        tc::mbar_arrive_expect_tx(fb, kStageBytes);
+                        tc::tma_load_2d(sa, &P.tm_a, fb, kb * BK, m0);
+                        if (B_MN) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                tc::tma_load_3d(sb + j * kBoxMN, &P.tm_b, fb, b_col<PAIRED>(j, nt, g.Ncols), kb * BK, e);
+                        } else {
+                            tc::tma_load_3d(sb, &P.tm_b, fb, kb * BK, nt * BN, e);
+                        }
+                    } else {
+                        tc::mbar_arrive_expect_tx(fb, P.a2_bytes + 4 * P.b2_box_bytes);
+                        tc::tma_load_2d(sa, &P.tm_a2, fb, 0, m0);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            tc::tma_load_3d(sb + j * P.b2_box_bytes, &P.tm_b2, fb, b_col<PAIRED>(j, nt, g.Ncols), 0, e);
+                    }
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_bf16(BM, BN, false, B_MN);
+            const uint32_t idesc2 = tc::idesc_bf16(BM, BN, false, true);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            for (int t = blockIdx.x; t < total_tiles && !*s_abort; t += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!tc::mbar_wait(tc::smem_u32(&tempty_bar[acc]), acc_phase ^ 1)) {
+                    set_timeout(g, s_abort);
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t d = tmem_base + acc * kAccCols;
+                const int nkb = P.num_kb + (P.lora_k16 ? 1 : 0);
+                bool ok = true;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!tc::mbar_wait(tc::smem_u32(&full_bar[stage]), phase)) {
+                        set_timeout(g, s_abort);
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t sa = tc::smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sb = sa + kABytes;
+                    if (kb < P.num_kb) {
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint64_t ad = tc::smem_desc(sa + kk * 32, 16, 1024, tc::kSw128);
+                            const uint64_t bd = B_MN ? tc::smem_desc(sb + kk * 2048, kBoxMN, 1024, tc::kSw128)
+                                                     : tc::smem_desc(sb + kk * 32, 16, 1024, tc::kSw128);
+                            tc::mma_bf16(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    } else {
+                        for (int kk = 0; kk < P.lora_k16; ++kk) {
+                            const uint64_t ad = tc::smem_desc(sa + kk * 32, 16, P.a2_sbo, P.a2_swz);
+                            const uint64_t bd = tc::smem_desc(sb + kk * 2048, P.b2_box_bytes, 1024, tc::kSw128);
+                            tc::mma_bf16(d, ad, bd, idesc2, 1u);
+                        }
+                    }
+                    tc::mma_commit(tc::smem_u32(&empty_bar[stage]));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc::mma_commit(tc::smem_u32(&tfull_bar[acc]));
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        int it = 0;
+        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+            int e, mt, nt;
+            decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
+            const int m0 = s_off[e] + mt * BM;
+            const int row_end = s_off[e + 1];
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            const bool ok = tc::mbar_wait(tc::smem_u32(&tfull_bar[acc]), acc_phase);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) set_timeout(g, s_abort);
+                break;
+            }
+            tc::fence_after_sync();
+            const uint32_t tb = tmem_base + acc * kAccCols + ((uint32_t)(q * 32) << 16);
+            const int p = m0 + row;
+            const bool valid = p < row_end;
+            if constexpr (EPI == EPI_SWIGLU) {
+                const int I = g.Ncols;
+                bf16* GU = (bf16*)g.out0;
+                bf16* Hh = (bf16*)g.out1;
+#pragma unroll 1
+                for (int c = 0; c < BN / 2; c += 16) {
+                    float gv[16], uv[16];
+                    tc::tmem_ld16(tb + c, gv);
+                    tc::tmem_ld16(tb + BN / 2 + c, uv);
+                    tc::tmem_ld_wait();
+                    const int n = nt * (BN / 2) + c;
+                    if (valid && n < I) {
+                        float hv[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) hv[i] = swiglu_f(gv[i], uv[i]);
+                        uint4* dg = reinterpret_cast<uint4*>(GU + (int64_t)p * 2 * I + n);
+                        uint4* du = reinterpret_cast<uint4*>(GU + (int64_t)p * 2 * I + I + n);
+                        uint4* dh = reinterpret_cast<uint4*>(Hh + (int64_t)p * I + n);
+                        dg[0] = pack8_bf16(gv); dg[1] = pack8_bf16(gv + 8);
+                        du[0] = pack8_bf16(uv); du[1] = pack8_bf16(uv + 8);
+                        dh[0] = pack8_bf16(hv); dh[1] = pack8_bf16(hv + 8);
+                    }
+                }
+            } else if constexpr (EPI == EPI_DSWIGLU) {
+                const int I = g.Ncols;
+                const bf16* GU = (const bf16*)g.gu_in;
+                bf16* dGU = (bf16*)g.out0;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 16) {
+                    float dh[16];
+                    tc::tmem_ld16(tb + c, dh);
+                    tc::tmem_ld_wait();
+                    const int n = nt * BN + c;
+                    if (valid && n < I) {
+                        const uint4* sg = reinterpret_cast<const uint4*>(GU + (int64_t)p * 2 * I + n);
+                        const uint4* su = reinterpret_cast<const uint4*>(GU + (int64_t)p * 2 * I + I + n);
+                        float gg[16], uu[16], dg[16], du[16];
+                        unpack8_bf16(sg[0], gg); unpack8_bf16(sg[1], gg + 8);
+                        unpack8_bf16(su[0], uu); unpack8_bf16(su[1], uu + 8);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) dswiglu_f(dh[i], gg[i], uu[i], dg[i], du[i]);
+                        uint4* og = reinterpret_cast<uint4*>(dGU + (int64_t)p * 2 * I + n);
+                        uint4* ou = reinterpret_cast<uint4*>(dGU + (int64_t)p * 2 * I + I + n);
+                        og[0] = pack8_bf16(dg); og[1] = pack8_bf16(dg + 8);
+                        ou[0] = pack8_bf16(du); ou[1] = pack8_bf16(du + 8);
+                    }
+                }
+            } else {
+                float* out = (float*)g.out0;
+                const float w = (EPI == EPI_ROWSCALE_F32 && valid) ? g.w_sorted[p] : 1.0f;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 16) {
+                    float v[16];
+                    tc::tmem_ld16(tb + c, v);
+                    tc::tmem_ld_wait();
+                    const int n = nt * BN + c;
+                    if (valid && n < g.Ncols) {
+                        float4* o = reinterpret_cast<float4*>(out + (int64_t)p * g.ldo + n);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            o[i] = make_float4(w * v[4 * i], w * v[4 * i + 1], w * v[4 * i + 2], w * v[4 * i + 3]);
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&tempty_bar[acc]));
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+CUtensorMapSwizzle swizzle_for_bytes(int inner_bytes) {
+    return inner_bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                              : (inner_bytes >= 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+            const uint32_t* box, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t gd[3], gs[2];
+    cuuint32_t bx[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+    }
+    for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bx, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!cached[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = v > 0 ? v : 1;
+    }
+    return cached[dev];
+}
+
+template <int EPI, bool B_MN>
+cudaError_t launch_tc(const TcParams& P, int grid, size_t smem, cudaStream_t s) {
+    auto k = grouped_gemm_tc_kernel<EPI, B_MN>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kThreads, smem, s>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
+    if (g.N == 0) return cudaSuccess;
+    if (g.K % BK != 0 || g.Ncols % 64 != 0) return cudaErrorInvalidValue;
+    if (g.epi == EPI_SWIGLU && !g.b_mn_major) return cudaErrorInvalidValue;   // gate/up pairing needs MN-major B
+    TcParams P;
+    memset(&P, 0, sizeof(P));
+    P.g = g;
+    P.num_kb = g.K / BK;
+    const bool paired = g.epi == EPI_SWIGLU;
+    P.n_tiles = paired ? (g.Ncols + BN / 2 - 1) / (BN / 2) : (g.Ncols + BN - 1) / BN;
+    // A: [N, K]
+    {
+        const uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)g.N};
+        const uint64_t st[1] = {(uint64_t)g.K * 2};
+        const uint32_t box[2] = {BK, BM};
+        if (!encode(&P.tm_a, g.A, 2, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    }
+    // B: expert stack
+    {
+        const uint64_t rows = (uint64_t)(g.b_expert_stride / g.ldb);
+        const uint64_t dims[3] = {(uint64_t)g.ldb, rows, (uint64_t)g.E};
+        const uint64_t st[2] = {(uint64_t)g.ldb * 2, (uint64_t)g.b_expert_stride * 2};
+        const uint32_t box_mn[3] = {64, BK, 1};
+        const uint32_t box_k[3] = {BK, BN, 1};
+        if (!encode(&P.tm_b, g.B, 3, dims, st, g.b_mn_major ? box_mn : box_k, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    if (g.A2 != nullptr && g.r > 0) {
+        const int rp = g.rp;
+        P.lora_k16 = rp / 16;
+        const uint64_t dims[2] = {(uint64_t)rp, (uint64_t)g.N};
+        const uint64_t st[1] = {(uint64_t)rp * 2};
+        const uint32_t box[2] = {(uint32_t)rp, BM};
+        if (!encode(&P.tm_a2, g.A2, 2, dims, st, box, swizzle_for_bytes(rp * 2))) return cudaErrorInvalidValue;
+        P.a2_bytes = BM * rp * 2;
+        P.a2_sbo = 8 * rp * 2;
+        P.a2_swz = rp >= 64 ? tc::kSw128 : (rp >= 32 ? tc::kSw64 : tc::kSw32);
+        const uint64_t dims2[3] = {(uint64_t)g.ldb2, (uint64_t)g.r, (uint64_t)g.E};
+        const uint64_t st2[2] = {(uint64_t)g.ldb2 * 2, (uint64_t)g.b2_expert_stride * 2};
+        const uint32_t box2[3] = {64, (uint32_t)rp, 1};
+        if (!encode(&P.tm_b2, g.B2, 3, dims2, st2, box2, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        P.b2_box_bytes = 64 * rp * 2;
+    }
+    const int64_t max_tiles = ((g.N + BM - 1) / BM + g.E) * (int64_t)P.n_tiles;
+    const int grid = (int)std::min<int64_t>(sm_count(), max_tiles);
+    const size_t smem = 1024 + (size_t)kStages * kStageBytes + 256 + (size_t)2 * (g.E + 1) * sizeof(int32_t);
+    const bool mn = g.b_mn_major;
+    switch (g.epi) {
+        case EPI_SWIGLU: return mn ? launch_tc<EPI_SWIGLU, true>(P, grid, smem, s) : launch_tc<EPI_SWIGLU, false>(P, grid, smem, s);
+        case EPI_ROWSCALE_F32:
+            return mn ? launch_tc<EPI_ROWSCALE_F32, true>(P, grid, smem, s) : launch_tc<EPI_ROWSCALE_F32, false>(P, grid, smem, s);
+        case EPI_DSWIGLU: return mn ? launch_tc<EPI_DSWIGLU, true>(P, grid, smem, s) : launch_tc<EPI_DSWIGLU, false>(P, grid, smem, s);
+        default: return mn ? launch_tc<EPI_F32, true>(P, grid, smem, s) : launch_tc<EPI_F32, false>(P, grid, smem, s);
+    }
+}
+
+}  // namespace moe
