@@ -42,11 +42,16 @@ GEMM_KERNELS = ("gemm_gate_up_fwd", "gemm_down_fwd", "gemm_down_bwd", "gemm_gate
 
 
 # ----------------------------------------------------------------------------- algorithmic work
-def kernel_work(cfg: mi.MoEConfig) -> dict:
+def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
     """Algorithmic flops and HBM bytes of one launch of each kernel (bf16 = 2 B).
 
     N = T*k routed rows.  GEMM flops count the base and the LoRA product the
-    kernel performs; bytes count each operand once (weights of all experts)."""
+    kernel performs; bytes count each operand once (weights of all experts).
+    A kernel is tensor-bound when its flops per byte reach the ridge point
+    (dense bf16 peak / HBM bandwidth), else HBM-bound."""
+    if ridge is None:
+        pk = load_peaks()
+        ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     T, H, I, E, k, r = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r
     N = T * k
     rp = 16 if r <= 16 else (32 if r <= 32 else 64)
@@ -75,7 +80,7 @@ def kernel_work(cfg: mi.MoEConfig) -> dict:
         "route": dict(flops=0, bytes=N * (8 + 4) * 2 + N * 12 + 8 * (E + 1)),
     }
     for v in w.values():
-        v["bound"] = "tensor" if v["flops"] >= 64 * v["bytes"] else "hbm"
+        v["bound"] = "tensor" if v["flops"] >= ridge * v["bytes"] else "hbm"
     return w
 
 

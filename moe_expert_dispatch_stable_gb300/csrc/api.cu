@@ -131,6 +131,17 @@ BwdWs bwd_ws(const moe_dims* d) {
     return W;
 }
 
+// Rank-r projection P = s * In Wt[e]^T on the tensor cores (tile width RP).
+cudaError_t project(const void* In, int K, const void* Wt, int r, int rp, float scale, const moe_routing* rt,
+                    int E, int64_t N, void* P, int32_t* dev_status, cudaStream_t s) {
+    GroupedGemm g{};
+    g.N = N; g.E = E; g.K = K; g.Ncols = rp;
+    g.A = In; g.B = Wt; g.b_mn_major = false; g.ldb = K; g.b_expert_stride = (int64_t)r * K;
+    g.offsets = rt->offsets; g.tile_offsets = rt->tile_offsets;
+    g.out0 = P; g.scale = scale; g.epi = EPI_PROJ; g.dev_status = dev_status;
+    return launch_grouped_gemm(g, s);
+}
+
 #define MOE_TRY(expr)                                  \
     do {                                               \
         cudaError_t _e = (expr);                       \
@@ -241,7 +252,7 @@ moe_status moe_lora_fwd(const moe_dims* d, const moe_routing* rt, const uint16_t
     const int H = d->H, I = d->I, E = d->E, r = d->r;
 
     MOE_TRY(timed("gather_x", s, [&] { return launch_gather_rows(x, H, rt->perm, nullptr, N, d->k, x_perm, s); }));
-    MOE_TRY(timed("proj_xa", s, [&] { return launch_lora_project(x_perm, H, A_gu, r, L.rp, d->scale, rt->offsets, E, N, XA, s); }));
+    MOE_TRY(timed("proj_xa", s, [&] { return project(x_perm, H, A_gu, r, L.rp, d->scale, rt, E, N, XA, dev_status, s); }));
 
     GroupedGemm g{};
     g.N = N; g.E = E; g.offsets = rt->offsets; g.tile_offsets = rt->tile_offsets; g.dev_status = dev_status;
@@ -252,7 +263,7 @@ moe_status moe_lora_fwd(const moe_dims* d, const moe_routing* rt, const uint16_t
     g.out0 = GU; g.out1 = h; g.epi = EPI_SWIGLU;
     MOE_TRY(timed("gemm_gate_up_fwd", s, [&] { return launch_grouped_gemm(g, s); }));
 
-    MOE_TRY(timed("proj_ha", s, [&] { return launch_lora_project(h, I, A_d, r, L.rp, d->scale, rt->offsets, E, N, HA, s); }));
+    MOE_TRY(timed("proj_ha", s, [&] { return project(h, I, A_d, r, L.rp, d->scale, rt, E, N, HA, dev_status, s); }));
     // down: O = w * (h W_d[e] + HA_s B_d[e])
     GroupedGemm g2{};
     g2.N = N; g2.E = E; g2.offsets = rt->offsets; g2.tile_offsets = rt->tile_offsets; g2.dev_status = dev_status;
@@ -311,7 +322,7 @@ moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt, const uint16_t
     // dO = w * dy[token]
     MOE_TRY(timed("gather_dy", s, [&] { return launch_gather_rows(dy, H, rt->perm, rt->w_sorted, N, d->k, dO, s); }));
     // G_s = s * dO B_d^T
-    MOE_TRY(timed("proj_g", s, [&] { return launch_lora_project(dO, H, B_d, r, L.rp, d->scale, rt->offsets, E, N, G, s); }));
+    MOE_TRY(timed("proj_g", s, [&] { return project(dO, H, B_d, r, L.rp, d->scale, rt, E, N, G, dev_status, s); }));
     // dh = dO W_d[e]^T + G_s A_d[e]  ->  dGU = SwiGLU'(GU) dh
     GroupedGemm g{};
     g.N = N; g.E = E; g.offsets = rt->offsets; g.tile_offsets = rt->tile_offsets; g.dev_status = dev_status;
@@ -321,10 +332,10 @@ moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt, const uint16_t
     g.gu_in = GU; g.out0 = dGU; g.epi = EPI_DSWIGLU;
     MOE_TRY(timed("gemm_down_bwd", s, [&] { return launch_grouped_gemm(g, s); }));
     // dA_d = G_s^T h ; dB_d = HA_s^T dO
-    MOE_TRY(timed("wgrad_dA_d", s, [&] { return launch_lora_wgrad(G, L.rp, r, h, I, rt->offsets, E, N, dA_d, nullptr, 0, s); }));
-    MOE_TRY(timed("wgrad_dB_d", s, [&] { return launch_lora_wgrad(HA, L.rp, r, dO, H, rt->offsets, E, N, dB_d, nullptr, 0, s); }));
+    MOE_TRY(timed("wgrad_dA_d", s, [&] { return launch_lora_wgrad_tc(G, L.rp, r, h, I, rt->offsets, E, N, dA_d, dev_status, s); }));
+    MOE_TRY(timed("wgrad_dB_d", s, [&] { return launch_lora_wgrad_tc(HA, L.rp, r, dO, H, rt->offsets, E, N, dB_d, dev_status, s); }));
     // Gg_s = s * dGU B_gu^T
-    MOE_TRY(timed("proj_gg", s, [&] { return launch_lora_project(dGU, 2 * I, B_gu, r, L.rp, d->scale, rt->offsets, E, N, Gg, s); }));
+    MOE_TRY(timed("proj_gg", s, [&] { return project(dGU, 2 * I, B_gu, r, L.rp, d->scale, rt, E, N, Gg, dev_status, s); }));
     // dX_perm = dGU W_gu[e]^T + Gg_s A_gu[e]
     GroupedGemm g2{};
     g2.N = N; g2.E = E; g2.offsets = rt->offsets; g2.tile_offsets = rt->tile_offsets; g2.dev_status = dev_status;
@@ -335,8 +346,8 @@ moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt, const uint16_t
     MOE_TRY(timed("gemm_gate_up_bwd", s, [&] { return launch_grouped_gemm(g2, s); }));
     MOE_TRY(timed("combine_dx", s, [&] { return launch_combine(dXp, rt->inv_perm, d->T, d->k, H, dx, s); }));
     // dA_gu = Gg_s^T x_perm ; dB_gu = XA_s^T dGU
-    MOE_TRY(timed("wgrad_dA_gu", s, [&] { return launch_lora_wgrad(Gg, L.rp, r, x_perm, H, rt->offsets, E, N, dA_gu, nullptr, 0, s); }));
-    MOE_TRY(timed("wgrad_dB_gu", s, [&] { return launch_lora_wgrad(XA, L.rp, r, dGU, 2 * I, rt->offsets, E, N, dB_gu, nullptr, 0, s); }));
+    MOE_TRY(timed("wgrad_dA_gu", s, [&] { return launch_lora_wgrad_tc(Gg, L.rp, r, x_perm, H, rt->offsets, E, N, dA_gu, dev_status, s); }));
+    MOE_TRY(timed("wgrad_dB_gu", s, [&] { return launch_lora_wgrad_tc(XA, L.rp, r, dGU, 2 * I, rt->offsets, E, N, dB_gu, dev_status, s); }));
     return MOE_OK;
 }
 
@@ -344,7 +355,7 @@ moe_status moe_timing_enable(int32_t on) {
     Timing& t = timing();
     std::lock_guard<std::mutex> g(t.mu);
     t.on = on != 0;
-    t.used = 0;
+    if (t.on) t.used = 0;      // enabling starts a new record; disabling keeps it for moe_timing_read
     return MOE_OK;
 }
 

@@ -9,15 +9,16 @@
 // one more K step of the same accumulator (A2 = s * x A^T rows, B2 = B), so
 // W + BA is never formed.
 //
-// CTA = 6 warps, one CTA per SM, grid = #SMs:
+// CTA = 10 warps, one CTA per SM, grid = #SMs:
 //   warp 0      TMA producer (one lane): A [128 x 64] and B [256 x 64] per stage,
 //               4 stages of 48 KB, 128-byte swizzle; the LoRA step loads A2 / B2
 //   warp 1      TMEM allocator + MMA issuer (one lane): 4 x tcgen05.mma
 //               M=128 N=256 K=16 per stage into one of two 256-column fp32
 //               accumulators (double buffer: the epilogue of tile i overlaps
 //               the MMAs of tile i+1)
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 16 columns, fused SwiGLU /
-//               routing-weight scale / SwiGLU backward, masked stores
+//   warps 2..9  epilogue (two per TMEM lane quarter, each half the columns):
+//               tcgen05.ld 32 lanes x 16 columns, fused SwiGLU / routing-weight
+//               scale / SwiGLU backward, masked stores
 // Every mbarrier wait is bounded; a wait that gives up sets MOE_DEV_TIMEOUT.
 #include "common.cuh"
 #include "epilogue.cuh"
@@ -33,15 +34,23 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int BM = 128, BK = 64;
+constexpr int kEpiWarps = 8;                 // 2 per TMEM lane quarter, each half the columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kABytes = BM * BK * 2;         // 16 KB
-constexpr int kBBytes = BN * BK * 2;         // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kBoxMN = 64 * BK * 2;          // one 64-column MN-major box of B: 8 KB
-constexpr int kAccCols = BN;
-constexpr int kTmemCols = 2 * kAccCols;
+
+// Tile geometry for an output tile width BN (256 for the expert GEMMs; 16/32/64
+// for the rank-r projections).
+template <int BN>
+struct Geo {
+    static constexpr int kBBytes = BN * BK * 2;
+    static constexpr int kStageBytes = kABytes + ((kBBytes + 1023) / 1024) * 1024;
+    static constexpr int kStages = BN >= 256 ? 4 : 8;
+    static constexpr int kAccCols = BN;
+    static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
+};
 
 struct TcParams {
     CUtensorMap tm_a, tm_b, tm_a2, tm_b2;
@@ -85,15 +94,20 @@ __device__ __forceinline__ void unpack8_bf16(const uint4& v, float* f) {
     }
 }
 
-template <bool PAIRED>
+template <bool PAIRED, int BN>
 __device__ __forceinline__ int b_col(int j, int nt, int ncols) {
     if (PAIRED) return (j < 2 ? 0 : ncols) + nt * (BN / 2) + (j & 1) * 64;
     return nt * BN + j * 64;
 }
 
-template <int EPI, bool B_MN>
+template <int EPI, bool B_MN, int BN>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams P) {
     constexpr bool PAIRED = (EPI == EPI_SWIGLU);
+    constexpr int kStages = Geo<BN>::kStages;
+    constexpr int kStageBytes = Geo<BN>::kStageBytes;
+    constexpr int kAccCols = Geo<BN>::kAccCols;
+    constexpr uint32_t kTmemCols = Geo<BN>::kTmemCols;
+    static_assert(BN == 256 || !B_MN, "narrow tiles take a K-major B");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -119,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(tc::smem_u32(&tfull_bar[a]), 1);
-            tc::mbar_init(tc::smem_u32(&tempty_bar[a]), 4);
+            tc::mbar_init(tc::smem_u32(&tempty_bar[a]), kEpiWarps);
         }
         *s_abort = 0;
         tc::fence_mbar_init();
@@ -161,12 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                     const uint32_t sa = tc::smem_u32(smem + stage * kStageBytes);
                     const uint32_t sb = sa + kABytes;
                     if (kb < P.num_kb) {
-                        tc::mbar_arrive_expect_tx(fb, kStageBytes);
+                        tc::mbar_arrive_expect_tx(fb, kABytes + Geo<BN>::kBBytes);
                         tc::tma_load_2d(sa, &P.tm_a, fb, kb * BK, m0);
                         if (B_MN) {
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                tc::tma_load_3d(sb + j * kBoxMN, &P.tm_b, fb, b_col<PAIRED>(j, nt, g.Ncols), kb * BK, e);
+                                tc::tma_load_3d(sb + j * kBoxMN, &P.tm_b, fb, b_col<PAIRED, BN>(j, nt, g.Ncols), kb * BK, e);
                         } else {
                             tc::tma_load_3d(sb, &P.tm_b, fb, kb * BK, nt * BN, e);
                         }
@@ -175,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                         tc::tma_load_2d(sa, &P.tm_a2, fb, 0, m0);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            tc::tma_load_3d(sb + j * P.b2_box_bytes, &P.tm_b2, fb, b_col<PAIRED>(j, nt, g.Ncols), 0, e);
+                            tc::tma_load_3d(sb + j * P.b2_box_bytes, &P.tm_b2, fb, b_col<PAIRED, BN>(j, nt, g.Ncols), 0, e);
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -239,8 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // warp w reads TMEM lanes 32*(w%4)..+31 (one row per thread); the two warps of a
+        // lane quarter split the columns in halves.
         const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row = q * 32 + lane;
+        constexpr int kSpan = PAIRED ? BN / 4 : (BN >= 32 ? BN / 2 : BN);   // columns per warp
+        const int c0 = (BN >= 32 || PAIRED) ? half * kSpan : 0;
+        const bool active = (BN >= 32 || PAIRED) || half == 0;
         int it = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
             int e, mt, nt;
@@ -258,12 +278,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
             const uint32_t tb = tmem_base + acc * kAccCols + ((uint32_t)(q * 32) << 16);
             const int p = m0 + row;
             const bool valid = p < row_end;
-            if constexpr (EPI == EPI_SWIGLU) {
+            if (!active) {
+            } else if constexpr (EPI == EPI_SWIGLU) {
                 const int I = g.Ncols;
                 bf16* GU = (bf16*)g.out0;
                 bf16* Hh = (bf16*)g.out1;
 #pragma unroll 1
-                for (int c = 0; c < BN / 2; c += 16) {
+                for (int c = c0; c < c0 + kSpan; c += 16) {
                     float gv[16], uv[16];
                     tc::tmem_ld16(tb + c, gv);
                     tc::tmem_ld16(tb + BN / 2 + c, uv);
@@ -285,18 +306,36 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                 const int I = g.Ncols;
                 const bf16* GU = (const bf16*)g.gu_in;
                 bf16* dGU = (bf16*)g.out0;
+                const bf16* grow = GU + (int64_t)p * 2 * I;
+                // prefetch the (g, u) pair of the next 16 columns while this chunk computes
+                uint4 pg0 = make_uint4(0, 0, 0, 0), pg1 = pg0, pu0 = pg0, pu1 = pg0;
+                {
+                    const int n = nt * BN + c0;
+                    if (valid && n < I) {
+                        pg0 = __ldg(reinterpret_cast<const uint4*>(grow + n));
+                        pg1 = __ldg(reinterpret_cast<const uint4*>(grow + n) + 1);
+                        pu0 = __ldg(reinterpret_cast<const uint4*>(grow + I + n));
+                        pu1 = __ldg(reinterpret_cast<const uint4*>(grow + I + n) + 1);
+                    }
+                }
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 16) {
+                for (int c = c0; c < c0 + kSpan; c += 16) {
+                    const uint4 g0 = pg0, g1 = pg1, u0 = pu0, u1 = pu1;
+                    const int n = nt * BN + c;
+                    const int nn = n + 16;
+                    if (c + 16 < c0 + kSpan && valid && nn < I) {
+                        pg0 = __ldg(reinterpret_cast<const uint4*>(grow + nn));
+                        pg1 = __ldg(reinterpret_cast<const uint4*>(grow + nn) + 1);
+                        pu0 = __ldg(reinterpret_cast<const uint4*>(grow + I + nn));
+                        pu1 = __ldg(reinterpret_cast<const uint4*>(grow + I + nn) + 1);
+                    }
                     float dh[16];
                     tc::tmem_ld16(tb + c, dh);
                     tc::tmem_ld_wait();
-                    const int n = nt * BN + c;
                     if (valid && n < I) {
-                        const uint4* sg = reinterpret_cast<const uint4*>(GU + (int64_t)p * 2 * I + n);
-                        const uint4* su = reinterpret_cast<const uint4*>(GU + (int64_t)p * 2 * I + I + n);
                         float gg[16], uu[16], dg[16], du[16];
-                        unpack8_bf16(sg[0], gg); unpack8_bf16(sg[1], gg + 8);
-                        unpack8_bf16(su[0], uu); unpack8_bf16(su[1], uu + 8);
+                        unpack8_bf16(g0, gg); unpack8_bf16(g1, gg + 8);
+                        unpack8_bf16(u0, uu); unpack8_bf16(u1, uu + 8);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) dswiglu_f(dh[i], gg[i], uu[i], dg[i], du[i]);
                         uint4* og = reinterpret_cast<uint4*>(dGU + (int64_t)p * 2 * I + n);
@@ -305,11 +344,26 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                         ou[0] = pack8_bf16(du); ou[1] = pack8_bf16(du + 8);
                     }
                 }
+            } else if constexpr (EPI == EPI_PROJ) {
+                bf16* out = (bf16*)g.out0;
+#pragma unroll
+                for (int c = c0; c < c0 + kSpan; c += 16) {
+                    float v[16];
+                    tc::tmem_ld16(tb + c, v);
+                    tc::tmem_ld_wait();
+                    if (valid) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= g.scale;
+                        uint4* o = reinterpret_cast<uint4*>(out + (int64_t)p * BN + c);
+                        o[0] = pack8_bf16(v);
+                        o[1] = pack8_bf16(v + 8);
+                    }
+                }
             } else {
                 float* out = (float*)g.out0;
                 const float w = (EPI == EPI_ROWSCALE_F32 && valid) ? g.w_sorted[p] : 1.0f;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 16) {
+                for (int c = c0; c < c0 + kSpan; c += 16) {
                     float v[16];
                     tc::tmem_ld16(tb + c, v);
                     tc::tmem_ld_wait();
@@ -383,9 +437,9 @@ int sm_count() {
     return cached[dev];
 }
 
-template <int EPI, bool B_MN>
+template <int EPI, bool B_MN, int BN>
 cudaError_t launch_tc(const TcParams& P, int grid, size_t smem, cudaStream_t s) {
-    auto k = grouped_gemm_tc_kernel<EPI, B_MN>;
+    auto k = grouped_gemm_tc_kernel<EPI, B_MN, BN>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     k<<<grid, kThreads, smem, s>>>(P);
@@ -396,14 +450,18 @@ cudaError_t launch_tc(const TcParams& P, int grid, size_t smem, cudaStream_t s) 
 
 cudaError_t launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
     if (g.N == 0) return cudaSuccess;
-    if (g.K % BK != 0 || g.Ncols % 64 != 0) return cudaErrorInvalidValue;
+    if (g.K % BK != 0) return cudaErrorInvalidValue;
+    const bool proj = g.epi == EPI_PROJ;
+    const int BN = proj ? g.Ncols : 256;
+    if (proj && (g.b_mn_major || g.A2 != nullptr || (BN != 16 && BN != 32 && BN != 64))) return cudaErrorInvalidValue;
+    if (!proj && g.Ncols % 64 != 0) return cudaErrorInvalidValue;
     if (g.epi == EPI_SWIGLU && !g.b_mn_major) return cudaErrorInvalidValue;   // gate/up pairing needs MN-major B
     TcParams P;
     memset(&P, 0, sizeof(P));
     P.g = g;
     P.num_kb = g.K / BK;
     const bool paired = g.epi == EPI_SWIGLU;
-    P.n_tiles = paired ? (g.Ncols + BN / 2 - 1) / (BN / 2) : (g.Ncols + BN - 1) / BN;
+    P.n_tiles = proj ? 1 : (paired ? (g.Ncols + 127) / 128 : (g.Ncols + 255) / 256);
     // A: [N, K]
     {
         const uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)g.N};
@@ -417,7 +475,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
         const uint64_t dims[3] = {(uint64_t)g.ldb, rows, (uint64_t)g.E};
         const uint64_t st[2] = {(uint64_t)g.ldb * 2, (uint64_t)g.b_expert_stride * 2};
         const uint32_t box_mn[3] = {64, BK, 1};
-        const uint32_t box_k[3] = {BK, BN, 1};
+        const uint32_t box_k[3] = {BK, (uint32_t)BN, 1};
         if (!encode(&P.tm_b, g.B, 3, dims, st, g.b_mn_major ? box_mn : box_k, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
@@ -439,14 +497,24 @@ cudaError_t launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
     }
     const int64_t max_tiles = ((g.N + BM - 1) / BM + g.E) * (int64_t)P.n_tiles;
     const int grid = (int)std::min<int64_t>(sm_count(), max_tiles);
-    const size_t smem = 1024 + (size_t)kStages * kStageBytes + 256 + (size_t)2 * (g.E + 1) * sizeof(int32_t);
+    const size_t offs_bytes = (size_t)2 * (g.E + 1) * sizeof(int32_t);
     const bool mn = g.b_mn_major;
+    if (proj) {
+        switch (BN) {
+            case 16: return launch_tc<EPI_PROJ, false, 16>(P, grid, Geo<16>::kSmem + offs_bytes, s);
+            case 32: return launch_tc<EPI_PROJ, false, 32>(P, grid, Geo<32>::kSmem + offs_bytes, s);
+            default: return launch_tc<EPI_PROJ, false, 64>(P, grid, Geo<64>::kSmem + offs_bytes, s);
+        }
+    }
+    const size_t smem = Geo<256>::kSmem + offs_bytes;
     switch (g.epi) {
-        case EPI_SWIGLU: return mn ? launch_tc<EPI_SWIGLU, true>(P, grid, smem, s) : launch_tc<EPI_SWIGLU, false>(P, grid, smem, s);
+        case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256>(P, grid, smem, s);
         case EPI_ROWSCALE_F32:
-            return mn ? launch_tc<EPI_ROWSCALE_F32, true>(P, grid, smem, s) : launch_tc<EPI_ROWSCALE_F32, false>(P, grid, smem, s);
-        case EPI_DSWIGLU: return mn ? launch_tc<EPI_DSWIGLU, true>(P, grid, smem, s) : launch_tc<EPI_DSWIGLU, false>(P, grid, smem, s);
-        default: return mn ? launch_tc<EPI_F32, true>(P, grid, smem, s) : launch_tc<EPI_F32, false>(P, grid, smem, s);
+            return mn ? launch_tc<EPI_ROWSCALE_F32, true, 256>(P, grid, smem, s)
+                      : launch_tc<EPI_ROWSCALE_F32, false, 256>(P, grid, smem, s);
+        case EPI_DSWIGLU:
+            return mn ? launch_tc<EPI_DSWIGLU, true, 256>(P, grid, smem, s) : launch_tc<EPI_DSWIGLU, false, 256>(P, grid, smem, s);
+        default: return mn ? launch_tc<EPI_F32, true, 256>(P, grid, smem, s) : launch_tc<EPI_F32, false, 256>(P, grid, smem, s);
     }
 }
 

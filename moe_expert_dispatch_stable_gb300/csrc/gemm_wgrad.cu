@@ -1,0 +1,311 @@
+// Per-expert LoRA weight gradients on the tensor cores (tcgen05 + TMEM + TMA).
+//
+//   D[e, j, m] = sum_{p in rows of expert e} Small[p, j] * Big[p, m]
+//
+// Small = the rank-r activations (already scaled by s), [N, RP]; Big = an
+// activation or gradient in sorted row order, [N, M].  The contraction runs
+// over the expert's ragged row range, so K differs per expert (0 for an expert
+// without rows).  Both operands are MN-major (their contiguous dimension is an
+// output dimension): A tile = Big[64 rows, 128 m] as two 64-column boxes with
+// 128-byte swizzle, B tile = Small[64 rows, RP].  Rows past the expert's end
+// (the next expert's rows, already in the tile) are zeroed in shared memory by
+// the MMA warp before the tile is used, so no foreign row enters the sum.
+//
+// One output tile = (expert, 128 columns of M); each is computed by exactly one
+// CTA in a fixed row order: deterministic, no atomics, no split-K.  Experts
+// without rows write exact zeros.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+
+namespace moe {
+
+namespace {
+
+constexpr int WM = 128, WK = 64;
+constexpr int kWStages = 6;
+constexpr int kWThreads = 192;
+constexpr int kWABytes = WM * WK * 2;   // 16 KB
+
+struct WgradParams {
+    CUtensorMap tm_big, tm_small;
+    const int32_t* offsets;
+    bf16* D;
+    int E, M, r, rp;
+    int m_tiles;
+    int b_bytes;        // WK * rp * 2
+    uint32_t b_sbo, b_swz;
+    int32_t* dev_status;
+};
+
+template <int RP>
+__global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __grid_constant__ WgradParams P) {
+    constexpr int kBBytes = WK * RP * 2;
+    constexpr int kStageBytes = kWABytes + ((kBBytes + 1023) / 1024) * 1024;
+    constexpr int kAcc = RP;
+    constexpr uint32_t kTmemCols = (2 * RP < 32) ? 32 : 2 * RP;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kWStages * kStageBytes);
+    uint64_t* empty_bar = full_bar + kWStages;
+    uint64_t* tfull_bar = empty_bar + kWStages;
+    uint64_t* tempty_bar = tfull_bar + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty_bar + 2);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int32_t* s_off = reinterpret_cast<int32_t*>(tmem_slot + 4);
+    const int E = P.E;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = P.offsets[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            tc::mbar_init(tc::smem_u32(&full_bar[s]), 1);
+            tc::mbar_init(tc::smem_u32(&empty_bar[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(tc::smem_u32(&tfull_bar[a]), 1);
+            tc::mbar_init(tc::smem_u32(&tempty_bar[a]), 4);
+        }
+        *s_abort = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tmap(&P.tm_big);
+        tc::prefetch_tmap(&P.tm_small);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = E * P.m_tiles;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = blockIdx.x; t < total && !*s_abort; t += gridDim.x) {
+                const int e = t / P.m_tiles, mt = t - e * P.m_tiles;
+                const int beg = s_off[e], end = s_off[e + 1];
+                for (int p0 = beg; p0 < end; p0 += WK) {
+                    if (!tc::mbar_wait(tc::smem_u32(&empty_bar[stage]), phase ^ 1)) {
+                        *s_abort = 1;
+                        atomicOr(P.dev_status, MOE_DEV_TIMEOUT);
+                        break;
+                    }
+                    const uint32_t fb = tc::smem_u32(&full_bar[stage]);
+                    const uint32_t sa = tc::smem_u32(smem + stage * kStageBytes);
+                    tc::mbar_arrive_expect_tx(fb, kWABytes + kBBytes);
+                    tc::tma_load_2d(sa, &P.tm_big, fb, mt * WM, p0);
+                    tc::tma_load_2d(sa + kWABytes / 2, &P.tm_big, fb, mt * WM + 64, p0);
+                    tc::tma_load_2d(sa + kWABytes, &P.tm_small, fb, 0, p0);
+                    if (++stage == kWStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        const uint32_t idesc = tc::idesc_bf16(WM, RP, true, true);
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        for (int t = blockIdx.x; t < total && !*s_abort; t += gridDim.x) {
+            const int e = t / P.m_tiles;
+            const int beg = s_off[e], end = s_off[e + 1];
+            if (end == beg) continue;                       // written as zeros by the epilogue
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            ++it;
+            bool ok = tc::mbar_wait(tc::smem_u32(&tempty_bar[acc]), acc_phase ^ 1);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) {
+                    *s_abort = 1;
+                    atomicOr(P.dev_status, MOE_DEV_TIMEOUT);
+                }
+                break;
+            }
+            tc::fence_after_sync();
+            const uint32_t d = tmem_base + acc * kAcc;
+            for (int p0 = beg; p0 < end; p0 += WK) {
+                ok = tc::mbar_wait(tc::smem_u32(&full_bar[stage]), phase);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    if (lane == 0) {
+                        *s_abort = 1;
+                        atomicOr(P.dev_status, MOE_DEV_TIMEOUT);
+                    }
+                    break;
+                }
+                const uint32_t sa = tc::smem_u32(smem + stage * kStageBytes);
+                const uint32_t sb = sa + kWABytes;
+                const int valid = min(WK, end - p0);
+                if (valid < WK) {
+                    // zero the rows of B that belong to the next expert (whole rows: the
+                    // swizzle only permutes 16-byte chunks inside a row)
+                    uint8_t* bt = smem + stage * kStageBytes + kWABytes;
+                    const int nbytes = (WK - valid) * RP * 2;
+                    for (int i = lane * 16; i < nbytes; i += 32 * 16)
+                        *reinterpret_cast<uint4*>(bt + valid * RP * 2 + i) = make_uint4(0, 0, 0, 0);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                __syncwarp();
+                tc::fence_after_sync();
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < WK / 16; ++kk) {
+                        const uint64_t ad = tc::smem_desc(sa + kk * 2048, kWABytes / 2, 1024, tc::kSw128);
+                        const uint64_t bd = tc::smem_desc(sb + kk * 16 * RP * 2, kBBytes, P.b_sbo, P.b_swz);
+                        tc::mma_bf16(d, ad, bd, idesc, (p0 > beg || kk > 0) ? 1u : 0u);
+                    }
+                    tc::mma_commit(tc::smem_u32(&empty_bar[stage]));
+                }
+                __syncwarp();
+                if (++stage == kWStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) tc::mma_commit(tc::smem_u32(&tfull_bar[acc]));
+            __syncwarp();
+        }
+    } else {
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        int it = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const int e = t / P.m_tiles, mt = t - e * P.m_tiles;
+            const int m = mt * WM + row;
+            bf16* De = P.D + (int64_t)e * P.r * P.M;
+            if (s_off[e + 1] == s_off[e]) {
+                if (m < P.M)
+                    for (int j = 0; j < P.r; ++j) De[(int64_t)j * P.M + m] = f2bf(0.f);
+                continue;
+            }
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            ++it;
+            const bool ok = tc::mbar_wait(tc::smem_u32(&tfull_bar[acc]), acc_phase);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) {
+                    *s_abort = 1;
+                    atomicOr(P.dev_status, MOE_DEV_TIMEOUT);
+                }
+                break;
+            }
+            tc::fence_after_sync();
+            const uint32_t tb = tmem_base + acc * kAcc + ((uint32_t)(q * 32) << 16);
+#pragma unroll
+            for (int c = 0; c < RP; c += 16) {
+                float v[16];
+                tc::tmem_ld16(tb + c, v);
+                tc::tmem_ld_wait();
+                if (m < P.M) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (c + i < P.r) De[(int64_t)(c + i) * P.M + m] = f2bf(v[i]);
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&tempty_bar[acc]));
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 wg_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool encode2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_in, uint32_t box_out,
+              CUtensorMapSwizzle sw) {
+    auto fn = wg_encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t gd[2] = {inner, outer};
+    cuuint64_t gs[1] = {inner * 2};
+    cuuint32_t bx[2] = {box_in, box_out};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gd, gs, bx, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int wg_sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!cached[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = v > 0 ? v : 1;
+    }
+    return cached[dev];
+}
+
+template <int RP>
+cudaError_t launch_wg(const WgradParams& P, cudaStream_t s) {
+    constexpr int kBBytes = WK * RP * 2;
+    constexpr int kStageBytes = kWABytes + ((kBBytes + 1023) / 1024) * 1024;
+    const size_t smem = 1024 + (size_t)kWStages * kStageBytes + 256 + (size_t)(P.E + 1) * sizeof(int32_t);
+    auto k = lora_wgrad_tc_kernel<RP>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int total = P.E * P.m_tiles;
+    const int grid = std::min(wg_sm_count(), total);
+    k<<<grid, kWThreads, smem, s>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_lora_wgrad_tc(const void* Small, int rp, int r, const void* Big, int M, const int32_t* offsets,
+                                 int E, int64_t N, void* D, int32_t* dev_status, cudaStream_t s) {
+    if (M % 64 != 0 || (rp != 16 && rp != 32 && rp != 64)) return cudaErrorInvalidValue;
+    WgradParams P;
+    memset(&P, 0, sizeof(P));
+    P.offsets = offsets;
+    P.D = (bf16*)D;
+    P.E = E; P.M = M; P.r = r; P.rp = rp;
+    P.m_tiles = (M + WM - 1) / WM;
+    P.dev_status = dev_status;
+    P.b_sbo = 8 * rp * 2;
+    P.b_swz = rp >= 64 ? tc::kSw128 : (rp >= 32 ? tc::kSw64 : tc::kSw32);
+    const CUtensorMapSwizzle bsw = rp >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                            : (rp >= 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+    const uint64_t rows = N > 0 ? (uint64_t)N : 1;
+    if (!encode2d(&P.tm_big, Big, (uint64_t)M, rows, 64, WK, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    if (!encode2d(&P.tm_small, Small, (uint64_t)rp, rows, (uint32_t)rp, WK, bsw)) return cudaErrorInvalidValue;
+    switch (rp) {
+        case 16: return launch_wg<16>(P, s);
+        case 32: return launch_wg<32>(P, s);
+        default: return launch_wg<64>(P, s);
+    }
+}
+
+}  // namespace moe

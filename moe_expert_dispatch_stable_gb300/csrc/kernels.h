@@ -20,21 +20,20 @@ cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, cons
 // out[t, :] = bf16( sum_{j<k} src[inv_perm[t*k+j], :] )  (fp32 src, fixed j order)
 cudaError_t launch_combine(const float* src, const int32_t* inv_perm, int64_t T, int k, int H,
                            void* out, cudaStream_t s);
-// P[p, j] = s * sum_c In[p, c] * Wt[e(p), j, c] for j < r, 0 for r <= j < RP  (bf16 out)
-cudaError_t launch_lora_project(const void* In, int K, const void* Wt, int r, int rp, float scale,
-                                const int32_t* offsets, int E, int64_t N, void* P, cudaStream_t s);
-// D[e, j, m] = sum_{p in e} Small[p, j] * Big[p, m]  (bf16 out [E, r, M]); fixed row order
-cudaError_t launch_lora_wgrad(const void* Small, int rp, int r, const void* Big, int M,
-                              const int32_t* offsets, int E, int64_t N, void* D, float* partial,
-                              size_t partial_elems, cudaStream_t s);
-size_t lora_wgrad_partial_elems(int64_t N, int E, int M, int rp);
 
-// ---- grouped GEMMs
+// ---- per-expert LoRA weight gradients (gemm_wgrad.cu)
+// D[e, j, m] = sum_{p in rows of e} Small[p, j] * Big[p, m]  (bf16 out [E, r, M]) on the
+// tensor cores, one CTA per (expert, 128 columns), fixed row order, zeros for empty experts.
+cudaError_t launch_lora_wgrad_tc(const void* Small, int rp, int r, const void* Big, int M, const int32_t* offsets,
+                                 int E, int64_t N, void* D, int32_t* dev_status, cudaStream_t s);
+
+// ---- grouped GEMMs (gemm_tc.cu)
 enum GemmEpi : int {
     EPI_SWIGLU = 0,     // paired gate/up accumulators -> GU (bf16, [N,2I]) and h (bf16, [N,I])
     EPI_ROWSCALE_F32 = 1,  // out_f32[p, n] = w_sorted[p] * acc
     EPI_DSWIGLU = 2,    // acc = dh; reads GU, writes dGU (bf16 [N,2I])
-    EPI_F32 = 3         // out_f32[p, n] = acc
+    EPI_F32 = 3,        // out_f32[p, n] = acc
+    EPI_PROJ = 4        // out_bf16[p, 0:Ncols] = scale * acc  (rank-r projection, Ncols = RP)
 };
 
 struct GroupedGemm {
@@ -63,13 +62,13 @@ struct GroupedGemm {
     void* out0;                  // EPI_SWIGLU: GU; EPI_DSWIGLU: dGU; F32 epilogues: float out
     void* out1;                  // EPI_SWIGLU: h
     int ldo;                     // row length of the fp32 output
+    float scale;                 // EPI_PROJ
     int epi;
     int32_t* dev_status;
 };
 
 // Product engine (tcgen05 / TMEM / TMA persistent kernel).
 cudaError_t launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s);
-// CUDA-core engine with the same semantics (numerics reference for tests).
-cudaError_t launch_grouped_gemm_simt(const GroupedGemm& g, cudaStream_t s);
+
 
 }  // namespace moe

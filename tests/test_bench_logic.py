@@ -1,0 +1,51 @@
+"""Host-side logic of bench.py: algorithmic work accounting and the clock parser (no GPU)."""
+import os
+
+import pytest
+
+import bench
+import moe_inputs as mi
+
+
+@pytest.mark.parametrize("name", list(mi.CONFIGS))
+def test_kernel_flops_add_up_to_layer_flops(name):
+    cfg = mi.CONFIGS[name]
+    w = bench.kernel_work(cfg)
+    kernels = [k for k in w if k.startswith(("gemm_", "proj_", "wgrad_"))]
+    assert sum(w[k]["flops"] for k in kernels) == bench.step_flops(cfg)
+    if name in ("gptoss20b", "gptoss120b_skew"):
+        for k in bench.GEMM_KERNELS:
+            assert w[k]["bound"] == "tensor"
+    for k in kernels:
+        if k.startswith(("proj_", "wgrad_")):
+            assert w[k]["bound"] == "hbm"
+
+
+def test_step_flops_matches_closed_form_for_gptoss20b():
+    cfg = mi.CONFIGS["gptoss20b"]
+    N = cfg.T * cfg.k
+    assert bench.step_flops(cfg) == N * (12 * 2880 * 2880 + 12 * 2880 * 16 + 18 * 2880 * 16)
+    assert abs(bench.step_flops(cfg) / 1e12 - 1.6534) < 1e-3
+
+
+def test_clock_sampler_parses_nvidia_smi_csv(tmp_path, monkeypatch):
+    s = bench.ClockSampler(0)
+    p = tmp_path / "c.csv"
+    p.write_text("0, 1980, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Active\n"
+                 "0, 2000, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+                 "0, 1990, 2070, 930.0, 0x0, Not Active, Not Active, Not Active, Not Active\n")
+
+    class FakeProc:
+        def terminate(self): pass
+        def wait(self, timeout=None): return 0
+        def kill(self): pass
+    s.proc, s.path = FakeProc(), str(p)
+    monkeypatch.setattr(bench.time, "sleep", lambda _: None)
+    out = s.stop()
+    assert out["sm_mhz"] == 1990 and out["sm_max_mhz"] == 2070 and out["reasons"] == ["sw_power_cap"]
+    assert not os.path.exists(p)
+
+
+def test_load_peaks_reads_measured_file():
+    pk = bench.load_peaks()
+    assert pk["hbm_gbs"] > 1000 and pk["bf16_tflops"] > 100
