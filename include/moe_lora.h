@@ -120,6 +120,34 @@ MOE_API moe_status moe_route(const void* topk_idx, int32_t idx_bytes, const floa
                      void* workspace, size_t workspace_bytes,
                      int32_t* dev_status, void* stream);
 
+/* Routing for callers that cannot allocate device memory.
+ *
+ * No passage of the pages has a counterpart to this entry point: it exists for
+ * callers of this library that cannot call cudaMalloc -- code running while a
+ * stream is being captured into a CUDA graph (allocation is not allowed there),
+ * hosts whose device memory is entirely owned by another allocator or a fixed
+ * pool, and latency-critical loops where an allocation could synchronise the
+ * device.  Such a caller still passes every input and output, but no workspace.
+ *
+ * It computes exactly what moe_route computes (same kernels, bit-identical
+ * outputs); the routing scratch lives instead in one file-scope device array of
+ * MOE_ROUTE_STATIC_SCRATCH_BYTES that every GPU loading the library holds until
+ * the process exits.  The call needs moe_route_workspace_size(T, k, E) <=
+ * MOE_ROUTE_STATIC_SCRATCH_BYTES, i.e. ceil(T*k / 4096) * E * 4 + 512 bytes at
+ * most (for example T*k <= 258048 slots at E = 1024, or T*k <= 2093056 at
+ * E = 128); larger sizes return MOE_ERR_WORKSPACE and launch nothing.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current): make that first call before any stream
+ * capture.  The call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine) and clears the part of the array that must start at zero on
+ * every call.  All calls share the array, so calls whose kernels overlap on the
+ * GPU (several streams, or several host threads) race: serialise them. */
+#define MOE_ROUTE_STATIC_SCRATCH_BYTES (256u * 1024u)
+MOE_API moe_status moe_route_static(const void* topk_idx, int32_t idx_bytes, const float* topk_w,
+                                    int64_t T, int32_t k, int32_t E, const moe_routing* out,
+                                    int32_t* dev_status, void* stream);
+
 /* ---------------------------------------------------------------- forward
  * Bytes of the `saved` buffer (activations kept for the backward pass) and of
  * the forward workspace. */

@@ -194,6 +194,24 @@ moe_status moe_route(const void* topk_idx, int32_t idx_bytes, const float* topk_
     }, T > 0 ? 3 : 2));
 }
 
+moe_status moe_route_static(const void* topk_idx, int32_t idx_bytes, const float* topk_w, int64_t T, int32_t k,
+                            int32_t E, const moe_routing* out, int32_t* dev_status, void* stream) {
+    size_t need = 0;
+    moe_status st = moe_route_workspace_size(T, k, E, &need);
+    if (st != MOE_OK) return st;
+    if (need > MOE_ROUTE_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+    if (idx_bytes != 4 && idx_bytes != 8) return MOE_ERR_BAD_DIMS;
+    if ((T > 0 && (topk_idx == nullptr || topk_w == nullptr)) || dev_status == nullptr) return MOE_ERR_NULL_ARG;
+    if ((st = check_routing(out, T * (int64_t)k)) != MOE_OK) return st;
+    if (T > 0 && (!aligned16(topk_idx) || !aligned16(topk_w))) return MOE_ERR_MISALIGNED;
+    void* scratch = nullptr;
+    if (route_static_scratch(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(timed("route", (cudaStream_t)stream, [&] {
+        return launch_route(topk_idx, idx_bytes, topk_w, T * (int64_t)k, E, *out, scratch, dev_status,
+                            (cudaStream_t)stream);
+    }, T > 0 ? 3 : 2));
+}
+
 moe_status moe_lora_fwd_sizes(const moe_dims* d, size_t* saved_bytes, size_t* workspace_bytes) {
     moe_status st = check_dims(d);
     if (st != MOE_OK) return st;

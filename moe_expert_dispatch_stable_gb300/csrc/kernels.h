@@ -12,6 +12,8 @@ namespace moe {
 size_t route_workspace_bytes(int64_t N, int E);
 cudaError_t launch_route(const void* idx, int idx_bytes, const float* topk_w, int64_t N, int E,
                          const moe_routing& out, void* ws, int32_t* dev_status, cudaStream_t s);
+// Device address of the fixed MOE_ROUTE_STATIC_SCRATCH_BYTES scratch array (looked up once per device).
+cudaError_t route_static_scratch(void** ptr);
 
 // ---- row kernels (rowops.cu)
 // dst[p, :] = src[perm[p] / k, :]   (optionally scaled by w_sorted[p], rounded to bf16)

@@ -20,6 +20,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <mutex>
+
 namespace moe {
 
 constexpr int kRouteChunk = 4096;
@@ -212,6 +214,33 @@ cudaError_t launch_route(const void* idx, int idx_bytes, const float* topk_w, in
                                                        out.perm, out.inv_perm, out.w_sorted);
     }
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- fixed scratch
+// Scratch of moe_route_static: the per-CTA histograms and the ticket live in this
+// file-scope device array instead of a caller-provided workspace.  Every GPU that
+// loads the library holds it until the process exits; every call shares it.
+static __device__ __align__(256) unsigned char g_route_scratch[MOE_ROUTE_STATIC_SCRATCH_BYTES];
+
+// Device address of g_route_scratch on the current device.  The host-side name of
+// the array is only a stand-in, so the address is looked up once per device (with
+// that device current) and cached.
+cudaError_t route_static_scratch(void** ptr) {
+    static std::mutex mu;
+    static void* cached[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(mu);
+    if (cached[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_route_scratch);
+        if (e != cudaSuccess) return e;
+        cached[dev] = p;
+    }
+    *ptr = cached[dev];
+    return cudaSuccess;
 }
 
 }  // namespace moe
