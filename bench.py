@@ -60,7 +60,7 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
         "gemm_gate_up_fwd": dict(flops=2 * N * H * 2 * I + 2 * N * r * 2 * I,
                                  bytes=b * (N * H + E * H * 2 * I + E * r * 2 * I + N * rp + N * 2 * I + N * I)),
         "gemm_down_fwd": dict(flops=2 * N * I * H + 2 * N * r * H,
-                              bytes=b * (N * I + E * I * H + E * r * H + N * rp) + 4 * N * H),
+                              bytes=b * (N * I + E * I * H + E * r * H + N * rp + N * H)),
         "gemm_down_bwd": dict(flops=2 * N * H * I + 2 * N * r * I,
                               bytes=b * (N * H + E * I * H + E * r * I + N * rp + N * 2 * I + N * 2 * I)),
         "gemm_gate_up_bwd": dict(flops=2 * N * 2 * I * H + 2 * N * r * H,
@@ -71,12 +71,12 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
         "proj_ha": dict(flops=2 * N * I * r, bytes=b * (N * I + E * r * I + N * rp)),
         "proj_g": dict(flops=2 * N * H * r, bytes=b * (N * H + E * r * H + N * rp)),
         "proj_gg": dict(flops=2 * N * 2 * I * r, bytes=b * (N * 2 * I + E * r * 2 * I + N * rp)),
-        "combine_y": dict(flops=N * H, bytes=4 * N * H + b * T * H + 4 * N),
+        "combine_y": dict(flops=N * H, bytes=b * N * H + b * T * H + 4 * N),
         "combine_dx": dict(flops=N * H, bytes=4 * N * H + b * T * H + 4 * N),
-        "wgrad_dA_d": dict(flops=2 * N * r * I, bytes=b * (N * rp + N * I + E * r * I)),
-        "wgrad_dB_d": dict(flops=2 * N * r * H, bytes=b * (N * rp + N * H + E * r * H)),
-        "wgrad_dA_gu": dict(flops=2 * N * r * H, bytes=b * (N * rp + N * H + E * r * H)),
-        "wgrad_dB_gu": dict(flops=2 * N * r * 2 * I, bytes=b * (N * rp + N * 2 * I + E * r * 2 * I)),
+        "wgrad_down": dict(flops=2 * N * r * I + 2 * N * r * H,
+                           bytes=b * (2 * N * rp + N * I + N * H + E * r * I + E * r * H)),
+        "wgrad_gate_up": dict(flops=2 * N * r * H + 2 * N * r * 2 * I,
+                              bytes=b * (2 * N * rp + N * H + N * 2 * I + E * r * H + E * r * 2 * I)),
         "route": dict(flops=0, bytes=N * (8 + 4) * 2 + N * 12 + 8 * (E + 1)),
     }
     for v in w.values():
@@ -116,7 +116,7 @@ class ClockSampler:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-i", str(self.gpu), "-lms", "200", "-f", self.path],
+                                          "-i", str(self.gpu), "-lms", "100", "-f", self.path],
                                          stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -166,10 +166,13 @@ def oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, S: int) -> float:
     return time.perf_counter() - t0
 
 
-def cpu_baseline(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, budget_s: float = 20.0) -> dict:
-    t_small = oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, 2)
-    S = int(max(2, min(cfg.T, 2 * budget_s / max(t_small, 1e-6))))
-    S = min(S, cfg.T)
+def cpu_baseline(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, budget_s: float = 25.0) -> dict:
+    # two-point calibration: a fixed part (routing all tokens, per-expert weight merges)
+    # plus a per-token part
+    t2 = oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, 2)
+    t8 = oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, 8)
+    slope = max((t8 - t2) / 6.0, 1e-6)
+    S = int(max(8, min(cfg.T, 8 + (budget_s - t8) / slope)))
     t = oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, S)
     return {"value": S / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"route of all {cfg.T} tokens + fp64 forward and backward of the first {S} tokens "
@@ -217,8 +220,8 @@ def config_dict(cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="gptoss20b", choices=list(mi.CONFIGS))
     ap.add_argument("--seed", type=int, default=0)
@@ -261,7 +264,7 @@ def main():
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
-        layer.step(t_idx, t_w, ts["x"], ts["dy"])
+        layer.step(t_idx, t_w, ts["x"], ts["dy"], with_topk_grad=False)
     torch.cuda.synchronize()
     assert int(layer.dev_status.item()) == 0, "device status flag set during warm-up"
 
@@ -279,7 +282,7 @@ def main():
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        layer.step(t_idx, t_w, ts["x"], ts["dy"])
+        layer.step(t_idx, t_w, ts["x"], ts["dy"], with_topk_grad=False)
         ends[i].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -287,7 +290,6 @@ def main():
         dist.barrier()
     moe.moe_timing_enable(False)
     launches = moe.moe_launch_count() - launches0
-    clk = clocks.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kt = moe.moe_timing_read()
     total_ms = sum(step_ms)
@@ -309,7 +311,7 @@ def main():
     def e2e_step():
         d_x.copy_(h_x, non_blocking=True); d_dy.copy_(h_dy, non_blocking=True)
         d_idx.copy_(h_idx, non_blocking=True); d_w.copy_(h_w, non_blocking=True)
-        layer.step(d_idx, d_w, d_x, d_dy)
+        layer.step(d_idx, d_w, d_x, d_dy, with_topk_grad=False)
         h_y.copy_(layer.y, non_blocking=True); h_dx.copy_(layer.dx, non_blocking=True)
         for h, g in zip(h_g, layer.grads):
             h.copy_(g, non_blocking=True)
@@ -329,6 +331,7 @@ def main():
         t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
+    clk = clocks.stop()
     e2e_value = cfg.T * args.steps * world / (e2e_ms / 1e3)
     assert int(layer.dev_status.item()) == 0, "device status flag set"
 
@@ -368,6 +371,24 @@ def main():
         "wall_s_timed": wall,
         "kernels_ms_per_step": {n: round(v, 4) for n, v in sorted(kernel_ms_step.items(), key=lambda kv: -kv[1])},
     }
+    # ---- router step in front of the layer (softmax + top-k and its backward), HBM-bound
+    logits = torch.from_numpy(mi.router_logits(cfg, args.seed + rank)).float().to(dev)
+    r_idx, r_w = moe.moe_router_topk(logits, cfg.k)
+    d_tw = torch.randn((cfg.T, cfg.k), device=dev)
+    d_lg = torch.empty_like(logits)
+    moe.moe_router_bwd(logits, r_idx, d_tw, d_logits=d_lg)
+    torch.cuda.synchronize()
+    moe.moe_timing_enable(True)
+    for _ in range(args.steps):
+        moe.moe_router_topk(logits, cfg.k, topk_idx=r_idx, topk_w=r_w)
+        moe.moe_router_bwd(logits, r_idx, d_tw, d_logits=d_lg)
+    torch.cuda.synchronize()
+    moe.moe_timing_enable(False)
+    rt_t = moe.moe_timing_read()
+    te = cfg.T * cfg.E * 4
+    r_bytes = {"router_topk": te + cfg.T * cfg.k * 8, "router_bwd": 2 * te + cfg.T * cfg.k * 8}
+    line["router"] = {n: {"us_per_launch": 1e3 * ms / cnt, "gbs": r_bytes[n] / (ms / cnt / 1e3) / 1e9}
+                      for n, (ms, cnt) in rt_t.items() if n in r_bytes}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         wts = [ts[n].cpu() for n in ("W_gu", "A_gu", "B_gu", "W_d", "A_d", "B_d")]
         line["cpu_baseline"] = cpu_baseline(cfg, idx, w, ts["x"].cpu(), ts["dy"].cpu(), wts)

@@ -154,10 +154,11 @@ MOE_API moe_status moe_route_static(const void* topk_idx, int32_t idx_bytes, con
 MOE_API moe_status moe_lora_fwd_sizes(const moe_dims* d, size_t* saved_bytes, size_t* workspace_bytes);
 
 /* Byte offsets inside `saved` of: x_perm [N,H], GU [N,2I], h [N,I],
- * XA_s [N,RP], HA_s [N,RP] (all bf16, N = T*k rows in sorted order,
+ * XA_s [N,RP], HA_s [N,RP], O [N,H] (all bf16, N = T*k rows in sorted order,
  * RP = r rounded up to 16, 32 or 64, padding columns zero;
- * XA_s = s * x_perm A_gu^T, HA_s = s * h A_d^T).  For inspection and tests. */
-MOE_API moe_status moe_lora_saved_layout(const moe_dims* d, size_t offsets[5], int32_t* rp);
+ * XA_s = s * x_perm A_gu^T, HA_s = s * h A_d^T, O = the unweighted expert
+ * output of each slot).  For inspection and tests. */
+MOE_API moe_status moe_lora_saved_layout(const moe_dims* d, size_t offsets[6], int32_t* rp);
 
 /* Forward of the MoE-LoRA expert layer (Split-LoRA, SwiGLU, weighted combine).
  *  x     [T, H]                  W_gu [E, H, 2I] (gate = cols [0,I), up = [I,2I))
@@ -168,7 +169,8 @@ MOE_API moe_status moe_lora_saved_layout(const moe_dims* d, size_t offsets[5], i
  *   GU = x[t] W_gu[e] + s (x[t] A_gu[e]^T) B_gu[e];  h = silu(GU[:I]) * GU[I:]
  *   o  = h W_d[e] + s (h A_d[e]^T) B_d[e];           y[t] = sum_j w[t,j] o_j
  * with bf16 operands, fp32 accumulation, and the k slots of a token summed in
- * the fixed order j = 0..k-1 (bitwise reproducible). */
+ * the fixed order j = 0..k-1 (bitwise reproducible).  The forward needs no
+ * workspace today (workspace_bytes is 0; `workspace` may be NULL). */
 MOE_API moe_status moe_lora_fwd(const moe_dims* d, const moe_routing* rt,
                         const uint16_t* x,
                         const uint16_t* W_gu, const uint16_t* A_gu, const uint16_t* B_gu,
@@ -185,6 +187,8 @@ MOE_API moe_status moe_lora_bwd_workspace_size(const moe_dims* d, size_t* bytes)
  *  dy [T, H]; saved = the buffer moe_lora_fwd filled (same d, rt, weights).
  *  Outputs (bf16, same layouts as the parameters):
  *   dx [T, H], dA_gu [E, r, H], dB_gu [E, r, 2I], dA_d [E, r, I], dB_d [E, r, H]
+ *  and, when d_topk_w is not NULL, the routing-weight gradient
+ *   d_topk_w [T, k] float32: dL/dw[t,j] = <dy[t], expert_{e(t,j)}(x[t])>
  * Per slot: dO = w dy[t]; dh = dO W_d^T + s (dO B_d^T) A_d;
  *   dGU = SwiGLU'(GU) dh;  dx[t] += dGU W_gu^T + s (dGU B_gu^T) A_gu
  * Per expert (sums over its rows, fixed order, no float atomics):
@@ -197,9 +201,29 @@ MOE_API moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt,
                         const uint16_t* W_d, const uint16_t* A_d, const uint16_t* B_d,
                         const void* saved, size_t saved_bytes,
                         uint16_t* dx, uint16_t* dA_gu, uint16_t* dB_gu,
-                        uint16_t* dA_d, uint16_t* dB_d,
+                        uint16_t* dA_d, uint16_t* dB_d, float* d_topk_w,
                         void* workspace, size_t workspace_bytes,
                         int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------- router
+ * The step in front of moe_route: the workloads route each token by a softmax
+ * over its E router logits followed by the k largest probabilities.
+ *  logits   [T, E] float32 (device)
+ *  topk_idx [T, k] int32 out: experts in descending probability; equal logits go
+ *           to the lower expert index.  Softmax is strictly increasing in each
+ *           logit, so the selection is made on the logits (exact comparisons).
+ *  topk_w   [T, k] float32 out: the selected softmax probabilities (fp32), not
+ *           renormalised.
+ * One kernel, no workspace.  1 <= k <= E <= 1024. */
+MOE_API moe_status moe_router_topk(const float* logits, int64_t T, int32_t E, int32_t k,
+                                   int32_t* topk_idx, float* topk_w, void* stream);
+
+/* Backward of moe_router_topk with the selection held fixed (the softmax VJP):
+ *   d_logits[t,e] = p_e * (g_e - sum_j d_topk_w[t,j] * p_{topk_idx[t,j]}),
+ * p = softmax(logits[t]) recomputed in fp32, g_e = d_topk_w[t,j] where
+ * topk_idx[t,j] = e (0 elsewhere).  d_logits [T, E] float32 out. */
+MOE_API moe_status moe_router_bwd(const float* logits, const int32_t* topk_idx, const float* d_topk_w,
+                                  int64_t T, int32_t E, int32_t k, float* d_logits, void* stream);
 
 /* ---------------------------------------------------------------- diagnostics
  * Per-kernel timing.  moe_timing_enable(1) clears the record and makes every

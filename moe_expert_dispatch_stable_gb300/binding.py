@@ -40,7 +40,9 @@ class moe_routing(ctypes.Structure):
 
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_launch_count", "moe_route_workspace_size", "moe_route",
             "moe_lora_fwd_sizes", "moe_lora_saved_layout", "moe_lora_fwd",
-            "moe_lora_bwd_workspace_size", "moe_lora_bwd", "moe_timing_enable", "moe_timing_read")
+            "moe_lora_bwd_workspace_size", "moe_lora_bwd", "moe_timing_enable", "moe_timing_read",
+            "moe_router_topk", "moe_router_bwd")
+ABI_VERSION = 2
 
 _lib = None
 
@@ -65,13 +67,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_lora_saved_layout.argtypes = [P(moe_dims), P(sz), P(i32)]
     lib.moe_lora_fwd.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 8 + [vp, sz, vp, sz, vp, vp]
     lib.moe_lora_bwd_workspace_size.argtypes = [P(moe_dims), P(sz)]
-    lib.moe_lora_bwd.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 7 + [vp, sz] + [vp] * 5 + [vp, sz, vp, vp]
+    lib.moe_lora_bwd.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 7 + [vp, sz] + [vp] * 6 + [vp, sz, vp, vp]
+    lib.moe_router_topk.argtypes = [vp, i64, i32, i32, vp, vp, vp]
+    lib.moe_router_bwd.argtypes = [vp, vp, vp, i64, i32, i32, vp, vp]
     lib.moe_launch_count.restype = ctypes.c_uint64
     lib.moe_timing_enable.argtypes = [i32]
     lib.moe_timing_read.argtypes = [i32, ctypes.c_char_p, sz, P(ctypes.c_double), P(i32)]
     for name in EXPORTED[3:]:
         getattr(lib, name).restype = i32
-    if lib.moe_abi_version() != 1:
+    if lib.moe_abi_version() != ABI_VERSION:
         raise MoEError("MoE-LoRA library ABI version mismatch")
     _lib = lib
     return lib
@@ -179,7 +183,7 @@ def moe_lora_fwd_sizes(d: Dims):
 
 
 def moe_lora_saved_layout(d: Dims):
-    offs = (ctypes.c_size_t * 5)()
+    offs = (ctypes.c_size_t * 6)()
     rp = ctypes.c_int32()
     _check(load_library().moe_lora_saved_layout(ctypes.byref(d.c_struct()), offs, ctypes.byref(rp)))
     return list(offs), rp.value
@@ -226,8 +230,9 @@ def moe_lora_fwd(d: Dims, rt: Routing, x, W_gu, A_gu, B_gu, W_d, A_d, B_d, y=Non
 
 
 def moe_lora_bwd(d: Dims, rt: Routing, dy, W_gu, A_gu, B_gu, W_d, A_d, B_d, saved, dx=None, grads=None,
-                 workspace=None, dev_status=None, stream=None):
-    """Backward of the layer; returns (dx, dA_gu, dB_gu, dA_d, dB_d)."""
+                 workspace=None, dev_status=None, stream=None, d_topk_w=None):
+    """Backward of the layer; returns (dx, dA_gu, dB_gu, dA_d, dB_d).  When d_topk_w
+    (a [T, k] float32 CUDA tensor) is given it receives dL/d topk_w."""
     lib = load_library()
     _need(dy, "dy", torch.bfloat16, (d.T, d.H))
     _check_weights(d, W_gu, A_gu, B_gu, W_d, A_d, B_d)
@@ -241,12 +246,47 @@ def moe_lora_bwd(d: Dims, rt: Routing, dy, W_gu, A_gu, B_gu, W_d, A_d, B_d, save
     if dev_status is None:
         dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
     dA_gu, dB_gu, dA_d, dB_d = grads
+    if d_topk_w is not None:
+        _need(d_topk_w, "d_topk_w", torch.float32, (d.T, d.k))
     dd, rr = d.c_struct(), rt.c_struct()
     _check(lib.moe_lora_bwd(ctypes.byref(dd), ctypes.byref(rr), _ptr(dy), _ptr(W_gu), _ptr(A_gu), _ptr(B_gu),
                             _ptr(W_d), _ptr(A_d), _ptr(B_d), _ptr(saved), saved.numel(), _ptr(dx),
-                            _ptr(dA_gu), _ptr(dB_gu), _ptr(dA_d), _ptr(dB_d), _ptr(workspace), workspace.numel(),
-                            _ptr(dev_status), _stream(stream)))
+                            _ptr(dA_gu), _ptr(dB_gu), _ptr(dA_d), _ptr(dB_d), _ptr(d_topk_w), _ptr(workspace),
+                            workspace.numel(), _ptr(dev_status), _stream(stream)))
     return dx, dA_gu, dB_gu, dA_d, dB_d
+
+
+def moe_router_topk(logits: torch.Tensor, k: int, topk_idx=None, topk_w=None, stream=None):
+    """Softmax over the E router logits of each token and its k largest
+    probabilities (ties to the lower expert index); returns (topk_idx int32, topk_w)."""
+    _need(logits, "logits", torch.float32)
+    if logits.dim() != 2:
+        raise MoEError("logits must be [T, E]")
+    T, E = logits.shape
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _need(topk_idx, "topk_idx", torch.int32, (T, k))
+    _need(topk_w, "topk_w", torch.float32, (T, k))
+    _check(load_library().moe_router_topk(_ptr(logits), T, E, k, _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+    return topk_idx, topk_w
+
+
+def moe_router_bwd(logits: torch.Tensor, topk_idx: torch.Tensor, d_topk_w: torch.Tensor, d_logits=None,
+                   stream=None) -> torch.Tensor:
+    """Gradient of the router step w.r.t. the logits (selection held fixed)."""
+    _need(logits, "logits", torch.float32)
+    T, E = logits.shape
+    k = topk_idx.shape[1]
+    _need(topk_idx, "topk_idx", torch.int32, (T, k))
+    _need(d_topk_w, "d_topk_w", torch.float32, (T, k))
+    if d_logits is None:
+        d_logits = torch.empty_like(logits)
+    _need(d_logits, "d_logits", torch.float32, (T, E))
+    _check(load_library().moe_router_bwd(_ptr(logits), _ptr(topk_idx), _ptr(d_topk_w), T, E, k, _ptr(d_logits),
+                                         _stream(stream)))
+    return d_logits
 
 
 def moe_launch_count() -> int:
@@ -294,6 +334,7 @@ class MoELoRALayer:
         self.y = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
         self.dx = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
         self.grads = tuple(torch.empty_like(weights[n]) for n in ("A_gu", "B_gu", "A_d", "B_d"))
+        self.d_topk_w = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def _wts(self):
@@ -308,11 +349,12 @@ class MoELoRALayer:
         return moe_lora_fwd(self.d, self.rt, x, *self._wts(), y=self.y, saved=self.saved,
                             workspace=self.fwd_ws, dev_status=self.dev_status, stream=stream)[0]
 
-    def backward(self, dy, stream=None):
+    def backward(self, dy, stream=None, with_topk_grad=True):
         return moe_lora_bwd(self.d, self.rt, dy, *self._wts(), self.saved, dx=self.dx, grads=self.grads,
-                            workspace=self.bwd_ws, dev_status=self.dev_status, stream=stream)
+                            workspace=self.bwd_ws, dev_status=self.dev_status, stream=stream,
+                            d_topk_w=self.d_topk_w if with_topk_grad else None)
 
-    def step(self, topk_idx, topk_w, x, dy, stream=None):
+    def step(self, topk_idx, topk_w, x, dy, stream=None, with_topk_grad=True):
         self.route(topk_idx, topk_w, stream)
         self.forward(x, stream)
-        return self.backward(dy, stream)
+        return self.backward(dy, stream, with_topk_grad)

@@ -83,7 +83,7 @@ moe_status check_routing(const moe_routing* rt, int64_t N) {
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 struct SavedLayout {
-    size_t x_perm, gu, h, xa, ha, total;
+    size_t x_perm, gu, h, xa, ha, o, total;
     int rp;
 };
 
@@ -97,21 +97,17 @@ SavedLayout saved_layout(const moe_dims* d) {
     L.h = o;      o = align_up(o + N * d->I * 2, kAlign);
     L.xa = o;     o = align_up(o + N * L.rp * 2, kAlign);
     L.ha = o;     o = align_up(o + N * L.rp * 2, kAlign);
+    L.o = o;      o = align_up(o + N * d->H * 2, kAlign);
     L.total = o;
     return L;
 }
 
+// The forward needs no workspace (every intermediate is kept in `saved`).
 struct FwdWs {
-    size_t o_perm, total;
+    size_t total;
 };
 
-FwdWs fwd_ws(const moe_dims* d) {
-    const size_t N = (size_t)d->T * d->k;
-    FwdWs W;
-    W.o_perm = 0;
-    W.total = align_up(N * d->H * 4, kAlign);
-    return W;
-}
+FwdWs fwd_ws(const moe_dims*) { return FwdWs{0}; }
 
 struct BwdWs {
     size_t d_o, g_s, dgu, gg_s, dx_perm, total;
@@ -152,7 +148,7 @@ cudaError_t project(const void* In, int K, const void* Wt, int r, int rp, float 
 
 extern "C" {
 
-int32_t moe_abi_version(void) { return 1; }
+int32_t moe_abi_version(void) { return 2; }
 
 const char* moe_status_string(moe_status s) {
     switch (s) {
@@ -221,12 +217,13 @@ moe_status moe_lora_fwd_sizes(const moe_dims* d, size_t* saved_bytes, size_t* wo
     return MOE_OK;
 }
 
-moe_status moe_lora_saved_layout(const moe_dims* d, size_t offsets[5], int32_t* rp) {
+moe_status moe_lora_saved_layout(const moe_dims* d, size_t offsets[6], int32_t* rp) {
     moe_status st = check_dims(d);
     if (st != MOE_OK) return st;
     if (offsets == nullptr || rp == nullptr) return MOE_ERR_NULL_ARG;
     const SavedLayout L = saved_layout(d);
     offsets[0] = L.x_perm; offsets[1] = L.gu; offsets[2] = L.h; offsets[3] = L.xa; offsets[4] = L.ha;
+    offsets[5] = L.o;
     *rp = L.rp;
     return MOE_OK;
 }
@@ -247,9 +244,10 @@ moe_status moe_lora_fwd(const moe_dims* d, const moe_routing* rt, const uint16_t
     if (st != MOE_OK) return st;
     const int64_t Nr = d->T * (int64_t)d->k;
     if ((st = check_routing(rt, Nr)) != MOE_OK) return st;
-    // token-sized buffers may be NULL when T == 0
-    const void* tok[] = {x, y, saved, workspace};
+    // token-sized buffers may be NULL when T == 0; the forward workspace is unused (size 0)
+    const void* tok[] = {x, y, saved};
     const void* always[] = {W_gu, A_gu, B_gu, W_d, A_d, B_d, dev_status};
+    if (!aligned16(workspace)) return MOE_ERR_MISALIGNED;
     for (const void* p : always) if (p == nullptr) return MOE_ERR_NULL_ARG;
     if (Nr > 0) for (const void* p : tok) if (p == nullptr) return MOE_ERR_NULL_ARG;
     for (const void* p : always) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
@@ -266,10 +264,10 @@ moe_status moe_lora_fwd(const moe_dims* d, const moe_routing* rt, const uint16_t
     void* h = sv + L.h;
     void* XA = sv + L.xa;
     void* HA = sv + L.ha;
-    float* O = (float*)((char*)workspace + W.o_perm);
+    void* O = sv + L.o;
     const int H = d->H, I = d->I, E = d->E, r = d->r;
 
-    MOE_TRY(timed("gather_x", s, [&] { return launch_gather_rows(x, H, rt->perm, nullptr, N, d->k, x_perm, s); }));
+    MOE_TRY(timed("gather_x", s, [&] { return launch_gather_rows(x, H, rt->perm, nullptr, N, d->k, x_perm, nullptr, nullptr, s); }));
     MOE_TRY(timed("proj_xa", s, [&] { return project(x_perm, H, A_gu, r, L.rp, d->scale, rt, E, N, XA, dev_status, s); }));
 
     GroupedGemm g{};
@@ -282,24 +280,24 @@ moe_status moe_lora_fwd(const moe_dims* d, const moe_routing* rt, const uint16_t
     MOE_TRY(timed("gemm_gate_up_fwd", s, [&] { return launch_grouped_gemm(g, s); }));
 
     MOE_TRY(timed("proj_ha", s, [&] { return project(h, I, A_d, r, L.rp, d->scale, rt, E, N, HA, dev_status, s); }));
-    // down: O = w * (h W_d[e] + HA_s B_d[e])
+    // down: O = h W_d[e] + HA_s B_d[e]  (unweighted, kept for the routing-weight gradient)
     GroupedGemm g2{};
     g2.N = N; g2.E = E; g2.offsets = rt->offsets; g2.tile_offsets = rt->tile_offsets; g2.dev_status = dev_status;
     g2.K = I; g2.Ncols = H; g2.A = h;
     g2.B = W_d; g2.b_mn_major = true; g2.ldb = H; g2.b_expert_stride = (int64_t)I * H;
     g2.A2 = HA; g2.rp = L.rp; g2.r = r; g2.B2 = B_d; g2.ldb2 = H; g2.b2_expert_stride = (int64_t)r * H;
-    g2.w_sorted = rt->w_sorted; g2.out0 = O; g2.ldo = H; g2.epi = EPI_ROWSCALE_F32;
+    g2.out0 = O; g2.ldo = H; g2.epi = EPI_BF16;
     MOE_TRY(timed("gemm_down_fwd", s, [&] { return launch_grouped_gemm(g2, s); }));
 
-    MOE_TRY(timed("combine_y", s, [&] { return launch_combine(O, rt->inv_perm, d->T, d->k, H, y, s); }));
+    MOE_TRY(timed("combine_y", s, [&] { return launch_combine(O, false, rt->w_sorted, rt->inv_perm, d->T, d->k, H, y, s); }));
     return MOE_OK;
 }
 
 moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt, const uint16_t* dy, const uint16_t* W_gu,
                         const uint16_t* A_gu, const uint16_t* B_gu, const uint16_t* W_d, const uint16_t* A_d,
                         const uint16_t* B_d, const void* saved, size_t saved_bytes, uint16_t* dx,
-                        uint16_t* dA_gu, uint16_t* dB_gu, uint16_t* dA_d, uint16_t* dB_d, void* workspace,
-                        size_t workspace_bytes, int32_t* dev_status, void* stream) {
+                        uint16_t* dA_gu, uint16_t* dB_gu, uint16_t* dA_d, uint16_t* dB_d, float* d_topk_w,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
     moe_status st = check_dims(d);
     if (st != MOE_OK) return st;
     const int64_t Nr = d->T * (int64_t)d->k;
@@ -311,6 +309,7 @@ moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt, const uint16_t
     if (Nr > 0) for (const void* p : tok) if (p == nullptr) return MOE_ERR_NULL_ARG;
     for (const void* p : always) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
     for (const void* p : tok) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    if (!aligned16(d_topk_w)) return MOE_ERR_MISALIGNED;
     const SavedLayout L = saved_layout(d);
     const BwdWs W = bwd_ws(d);
     if (saved_bytes < L.total || workspace_bytes < W.total) return MOE_ERR_WORKSPACE;
@@ -330,15 +329,16 @@ moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt, const uint16_t
     const void* h = sv + L.h;
     const void* XA = sv + L.xa;
     const void* HA = sv + L.ha;
+    const void* Os = sv + L.o;
     char* ws = (char*)workspace;
     void* dO = ws + W.d_o;
     void* G = ws + W.g_s;
     void* dGU = ws + W.dgu;
     void* Gg = ws + W.gg_s;
-    float* dXp = (float*)(ws + W.dx_perm);
+    void* dXp = ws + W.dx_perm;
 
-    // dO = w * dy[token]
-    MOE_TRY(timed("gather_dy", s, [&] { return launch_gather_rows(dy, H, rt->perm, rt->w_sorted, N, d->k, dO, s); }));
+    // dO = w * dy[token]  (and d_topk_w[slot] = <dy[token], O[p]> when requested)
+    MOE_TRY(timed("gather_dy", s, [&] { return launch_gather_rows(dy, H, rt->perm, rt->w_sorted, N, d->k, dO, Os, d_topk_w, s); }));
     // G_s = s * dO B_d^T
     MOE_TRY(timed("proj_g", s, [&] { return project(dO, H, B_d, r, L.rp, d->scale, rt, E, N, G, dev_status, s); }));
     // dh = dO W_d[e]^T + G_s A_d[e]  ->  dGU = SwiGLU'(GU) dh
@@ -350,8 +350,10 @@ moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt, const uint16_t
     g.gu_in = GU; g.out0 = dGU; g.epi = EPI_DSWIGLU;
     MOE_TRY(timed("gemm_down_bwd", s, [&] { return launch_grouped_gemm(g, s); }));
     // dA_d = G_s^T h ; dB_d = HA_s^T dO
-    MOE_TRY(timed("wgrad_dA_d", s, [&] { return launch_lora_wgrad_tc(G, L.rp, r, h, I, rt->offsets, E, N, dA_d, dev_status, s); }));
-    MOE_TRY(timed("wgrad_dB_d", s, [&] { return launch_lora_wgrad_tc(HA, L.rp, r, dO, H, rt->offsets, E, N, dB_d, dev_status, s); }));
+    {
+        const WgradProblem wp[2] = {{G, h, I, dA_d}, {HA, dO, H, dB_d}};
+        MOE_TRY(timed("wgrad_down", s, [&] { return launch_lora_wgrad_tc(wp, 2, L.rp, r, rt->offsets, E, N, dev_status, s); }));
+    }
     // Gg_s = s * dGU B_gu^T
     MOE_TRY(timed("proj_gg", s, [&] { return project(dGU, 2 * I, B_gu, r, L.rp, d->scale, rt, E, N, Gg, dev_status, s); }));
     // dX_perm = dGU W_gu[e]^T + Gg_s A_gu[e]
@@ -360,13 +362,37 @@ moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt, const uint16_t
     g2.K = 2 * I; g2.Ncols = H; g2.A = dGU;
     g2.B = W_gu; g2.b_mn_major = false; g2.ldb = 2 * I; g2.b_expert_stride = (int64_t)H * 2 * I;
     g2.A2 = Gg; g2.rp = L.rp; g2.r = r; g2.B2 = A_gu; g2.ldb2 = H; g2.b2_expert_stride = (int64_t)r * H;
-    g2.out0 = dXp; g2.ldo = H; g2.epi = EPI_F32;
+    g2.out0 = dXp; g2.ldo = H; g2.epi = EPI_PLAIN_F32;
     MOE_TRY(timed("gemm_gate_up_bwd", s, [&] { return launch_grouped_gemm(g2, s); }));
-    MOE_TRY(timed("combine_dx", s, [&] { return launch_combine(dXp, rt->inv_perm, d->T, d->k, H, dx, s); }));
+    MOE_TRY(timed("combine_dx", s, [&] { return launch_combine(dXp, true, nullptr, rt->inv_perm, d->T, d->k, H, dx, s); }));
     // dA_gu = Gg_s^T x_perm ; dB_gu = XA_s^T dGU
-    MOE_TRY(timed("wgrad_dA_gu", s, [&] { return launch_lora_wgrad_tc(Gg, L.rp, r, x_perm, H, rt->offsets, E, N, dA_gu, dev_status, s); }));
-    MOE_TRY(timed("wgrad_dB_gu", s, [&] { return launch_lora_wgrad_tc(XA, L.rp, r, dGU, 2 * I, rt->offsets, E, N, dB_gu, dev_status, s); }));
+    {
+        const WgradProblem wp[2] = {{Gg, x_perm, H, dA_gu}, {XA, dGU, 2 * I, dB_gu}};
+        MOE_TRY(timed("wgrad_gate_up", s, [&] { return launch_lora_wgrad_tc(wp, 2, L.rp, r, rt->offsets, E, N, dev_status, s); }));
+    }
     return MOE_OK;
+}
+
+moe_status moe_router_topk(const float* logits, int64_t T, int32_t E, int32_t k, int32_t* topk_idx, float* topk_w,
+                           void* stream) {
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || T * (int64_t)k >= (int64_t(1) << 31)) return MOE_ERR_BAD_DIMS;
+    if (T > 0 && (logits == nullptr || topk_idx == nullptr || topk_w == nullptr)) return MOE_ERR_NULL_ARG;
+    if (!aligned16(logits) || !aligned16(topk_idx) || !aligned16(topk_w)) return MOE_ERR_MISALIGNED;
+    return cuda_status(timed("router_topk", (cudaStream_t)stream, [&] {
+        return launch_router_topk(logits, T, E, k, topk_idx, topk_w, (cudaStream_t)stream);
+    }, T > 0 ? 1 : 0));
+}
+
+moe_status moe_router_bwd(const float* logits, const int32_t* topk_idx, const float* d_topk_w, int64_t T, int32_t E,
+                          int32_t k, float* d_logits, void* stream) {
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || T * (int64_t)k >= (int64_t(1) << 31)) return MOE_ERR_BAD_DIMS;
+    if (T > 0 && (logits == nullptr || topk_idx == nullptr || d_topk_w == nullptr || d_logits == nullptr))
+        return MOE_ERR_NULL_ARG;
+    if (!aligned16(logits) || !aligned16(topk_idx) || !aligned16(d_topk_w) || !aligned16(d_logits))
+        return MOE_ERR_MISALIGNED;
+    return cuda_status(timed("router_bwd", (cudaStream_t)stream, [&] {
+        return launch_router_bwd(logits, topk_idx, d_topk_w, T, E, k, d_logits, (cudaStream_t)stream);
+    }, T > 0 ? 1 : 0));
 }
 
 moe_status moe_timing_enable(int32_t on) {

@@ -41,12 +41,13 @@ constexpr int kABytes = BM * BK * 2;         // 16 KB
 constexpr int kBoxMN = 64 * BK * 2;          // one 64-column MN-major box of B: 8 KB
 
 // Tile geometry for an output tile width BN (256 for the expert GEMMs; 16/32/64
-// for the rank-r projections).
-template <int BN>
+// for the rank-r projections).  PAIR: a 2-CTA cluster shares one 256 x 256 tile,
+// each CTA holding 128 rows of A and 128 columns of B per stage.
+template <int BN, bool PAIR = false>
 struct Geo {
-    static constexpr int kBBytes = BN * BK * 2;
+    static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK * 2;
     static constexpr int kStageBytes = kABytes + ((kBBytes + 1023) / 1024) * 1024;
-    static constexpr int kStages = BN >= 256 ? 4 : 8;
+    static constexpr int kStages = PAIR ? 6 : (BN >= 256 ? 4 : 8);
     static constexpr int kAccCols = BN;
     static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
@@ -100,14 +101,17 @@ __device__ __forceinline__ int b_col(int j, int nt, int ncols) {
     return nt * BN + j * 64;
 }
 
-template <int EPI, bool B_MN, int BN>
+template <int EPI, bool B_MN, int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams P) {
     constexpr bool PAIRED = (EPI == EPI_SWIGLU);
-    constexpr int kStages = Geo<BN>::kStages;
-    constexpr int kStageBytes = Geo<BN>::kStageBytes;
-    constexpr int kAccCols = Geo<BN>::kAccCols;
-    constexpr uint32_t kTmemCols = Geo<BN>::kTmemCols;
+    using G = Geo<BN, PAIR>;
+    constexpr int kStages = G::kStages;
+    constexpr int kStageBytes = G::kStageBytes;
+    constexpr int kAccCols = G::kAccCols;
+    constexpr uint32_t kTmemCols = G::kTmemCols;
+    constexpr int TM = PAIR ? 2 * BM : BM;          // rows per tile
     static_assert(BN == 256 || !B_MN, "narrow tiles take a K-major B");
+    static_assert(!PAIR || BN == 256, "SM pairs run the 256-wide expert GEMMs only");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -122,9 +126,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
     int32_t* s_toff = s_off + (E + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? tc::cluster_rank() : 0u;     // 0 = leader of the pair
+    const int tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int tile_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+
     for (int i = threadIdx.x; i <= E; i += blockDim.x) {
         s_off[i] = g.offsets[i];
-        s_toff[i] = g.tile_offsets[i];
+        if (!PAIR) s_toff[i] = g.tile_offsets[i];
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -133,10 +141,30 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(tc::smem_u32(&tfull_bar[a]), 1);
-            tc::mbar_init(tc::smem_u32(&tempty_bar[a]), kEpiWarps);
+            tc::mbar_init(tc::smem_u32(&tempty_bar[a]), PAIR ? 2 * kEpiWarps : kEpiWarps);
         }
         *s_abort = 0;
         tc::fence_mbar_init();
+    }
+    if constexpr (PAIR) {
+        // 256-row tile offsets: prefix sum of ceil(count / 256) (warp 0, 32 experts per step)
+        __syncthreads();
+        if (warp == 0) {
+            int run = 0;
+            for (int b = 0; b < E; b += 32) {
+                const int e = b + lane;
+                const int v = e < E ? (s_off[e + 1] - s_off[e] + TM - 1) / TM : 0;
+                int incl = v;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int n = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (lane >= d) incl += n;
+                }
+                if (e < E) s_toff[e] = run + incl - v;
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) s_toff[E] = run;
+        }
     }
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&P.tm_a);
@@ -147,11 +175,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
         }
     }
     if (warp == 1) {
-        tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
-        tc::tmem_relinquish();
+        if constexpr (PAIR) {
+            tc::tmem_alloc_pair(tc::smem_u32(tmem_slot), kTmemCols);
+            tc::tmem_relinquish_pair();
+        } else {
+            tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
+            tc::tmem_relinquish();
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) tc::cluster_sync();    // the peer's barriers exist before anyone signals them
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     const int total_tiles = s_toff[E] * P.n_tiles;
@@ -161,35 +195,62 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            for (int t = blockIdx.x; t < total_tiles && !*s_abort; t += gridDim.x) {
+            for (int t = tile0; t < total_tiles && !*s_abort; t += tile_step) {
                 int e, mt, nt;
                 decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
-                const int m0 = s_off[e] + mt * BM;
+                const int m0 = s_off[e] + mt * TM + (int)rank * BM;      // this CTA's 128 rows
                 const int nkb = P.num_kb + (P.lora_k16 ? 1 : 0);
                 for (int kb = 0; kb < nkb; ++kb) {
-                    const uint32_t fb = tc::smem_u32(&full_bar[stage]);
                     if (!tc::mbar_wait(tc::smem_u32(&empty_bar[stage]), phase ^ 1)) {
                         set_timeout(g, s_abort);
                         break;
                     }
+                    const uint32_t fb_local = tc::smem_u32(&full_bar[stage]);
                     const uint32_t sa = tc::smem_u32(smem + stage * kStageBytes);
                     const uint32_t sb = sa + kABytes;
-                    if (kb < P.num_kb) {
-                        tc::mbar_arrive_expect_tx(fb, kABytes + Geo<BN>::kBBytes);
-                        tc::tma_load_2d(sa, &P.tm_a, fb, kb * BK, m0);
-                        if (B_MN) {
+                    if constexpr (PAIR) {
+                        // both CTAs' loads complete on the leader's full barrier
+                        const uint32_t fb = tc::mapa(fb_local, 0);
+                        if (kb < P.num_kb) {
+                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * (kABytes + G::kBBytes));
+                            tc::tma_load_2d_pair(sa, &P.tm_a, fb, kb * BK, m0);
+                            if (B_MN) {
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                tc::tma_load_3d(sb + j * kBoxMN, &P.tm_b, fb, b_col<PAIRED, BN>(j, nt, g.Ncols), kb * BK, e);
+                                for (int jj = 0; jj < 2; ++jj)
+                                    tc::tma_load_3d_pair(sb + jj * kBoxMN, &P.tm_b, fb,
+                                                         b_col<PAIRED, BN>(2 * (int)rank + jj, nt, g.Ncols), kb * BK, e);
+                            } else {
+                                tc::tma_load_3d_pair(sb, &P.tm_b, fb, kb * BK, nt * BN + (int)rank * (BN / 2), e);
+                            }
                         } else {
-                            tc::tma_load_3d(sb, &P.tm_b, fb, kb * BK, nt * BN, e);
+                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * (P.a2_bytes + 2 * P.b2_box_bytes));
+                            tc::tma_load_2d_pair(sa, &P.tm_a2, fb, 0, m0);
+#pragma unroll
+                            for (int jj = 0; jj < 2; ++jj)
+                                tc::tma_load_3d_pair(sb + jj * P.b2_box_bytes, &P.tm_b2, fb,
+                                                     b_col<PAIRED, BN>(2 * (int)rank + jj, nt, g.Ncols), 0, e);
                         }
                     } else {
-                        tc::mbar_arrive_expect_tx(fb, P.a2_bytes + 4 * P.b2_box_bytes);
-                        tc::tma_load_2d(sa, &P.tm_a2, fb, 0, m0);
+                        const uint32_t fb = fb_local;
+                        if (kb < P.num_kb) {
+                            tc::mbar_arrive_expect_tx(fb, kABytes + G::kBBytes);
+                            tc::tma_load_2d(sa, &P.tm_a, fb, kb * BK, m0);
+                            if (B_MN) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            tc::tma_load_3d(sb + j * P.b2_box_bytes, &P.tm_b2, fb, b_col<PAIRED, BN>(j, nt, g.Ncols), 0, e);
+                                for (int j = 0; j < 4; ++j)
+                                    tc::tma_load_3d(sb + j * kBoxMN, &P.tm_b, fb, b_col<PAIRED, BN>(j, nt, g.Ncols),
+                                                    kb * BK, e);
+                            } else {
+                                tc::tma_load_3d(sb, &P.tm_b, fb, kb * BK, nt * BN, e);
+                            }
+                        } else {
+                            tc::mbar_arrive_expect_tx(fb, P.a2_bytes + 4 * P.b2_box_bytes);
+                            tc::tma_load_2d(sa, &P.tm_a2, fb, 0, m0);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                tc::tma_load_3d(sb + j * P.b2_box_bytes, &P.tm_b2, fb, b_col<PAIRED, BN>(j, nt, g.Ncols),
+                                                0, e);
+                        }
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -199,14 +260,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = tc::idesc_bf16(BM, BN, false, B_MN);
-            const uint32_t idesc2 = tc::idesc_bf16(BM, BN, false, true);
+        // ------------------------------------------------------------ MMA issuer (leader only for pairs)
+        if (lane == 0 && rank == 0) {
+            const uint32_t idesc = tc::idesc_bf16(TM, BN, false, B_MN);
+            const uint32_t idesc2 = tc::idesc_bf16(TM, BN, false, true);
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
-            for (int t = blockIdx.x; t < total_tiles && !*s_abort; t += gridDim.x, ++it) {
+            for (int t = tile0; t < total_tiles && !*s_abort; t += tile_step, ++it) {
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!tc::mbar_wait(tc::smem_u32(&tempty_bar[acc]), acc_phase ^ 1)) {
@@ -232,23 +293,27 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                             const uint64_t ad = tc::smem_desc(sa + kk * 32, 16, 1024, tc::kSw128);
                             const uint64_t bd = B_MN ? tc::smem_desc(sb + kk * 2048, kBoxMN, 1024, tc::kSw128)
                                                      : tc::smem_desc(sb + kk * 32, 16, 1024, tc::kSw128);
-                            tc::mma_bf16(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                            if constexpr (PAIR) tc::mma_bf16_pair(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                            else tc::mma_bf16(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
                         }
                     } else {
                         for (int kk = 0; kk < P.lora_k16; ++kk) {
                             const uint64_t ad = tc::smem_desc(sa + kk * 32, 16, P.a2_sbo, P.a2_swz);
                             const uint64_t bd = tc::smem_desc(sb + kk * 2048, P.b2_box_bytes, 1024, tc::kSw128);
-                            tc::mma_bf16(d, ad, bd, idesc2, 1u);
+                            if constexpr (PAIR) tc::mma_bf16_pair(d, ad, bd, idesc2, 1u);
+                            else tc::mma_bf16(d, ad, bd, idesc2, 1u);
                         }
                     }
-                    tc::mma_commit(tc::smem_u32(&empty_bar[stage]));
+                    if constexpr (PAIR) tc::mma_commit_pair(tc::smem_u32(&empty_bar[stage]), 0x3);
+                    else tc::mma_commit(tc::smem_u32(&empty_bar[stage]));
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                tc::mma_commit(tc::smem_u32(&tfull_bar[acc]));
+                if constexpr (PAIR) tc::mma_commit_pair(tc::smem_u32(&tfull_bar[acc]), 0x3);
+                else tc::mma_commit(tc::smem_u32(&tfull_bar[acc]));
             }
         }
     } else {
@@ -262,10 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
         const int c0 = (BN >= 32 || PAIRED) ? half * kSpan : 0;
         const bool active = (BN >= 32 || PAIRED) || half == 0;
         int it = 0;
-        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+        const uint32_t tempty_leader0 = PAIR ? tc::mapa(tc::smem_u32(&tempty_bar[0]), 0) : 0u;
+        for (int t = tile0; t < total_tiles; t += tile_step, ++it) {
             int e, mt, nt;
             decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
-            const int m0 = s_off[e] + mt * BM;
+            const int m0 = s_off[e] + mt * TM + (int)rank * BM;
             const int row_end = s_off[e + 1];
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
@@ -297,8 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                         uint4* dg = reinterpret_cast<uint4*>(GU + (int64_t)p * 2 * I + n);
                         uint4* du = reinterpret_cast<uint4*>(GU + (int64_t)p * 2 * I + I + n);
                         uint4* dh = reinterpret_cast<uint4*>(Hh + (int64_t)p * I + n);
-                        dg[0] = pack8_bf16(gv); dg[1] = pack8_bf16(gv + 8);
-                        du[0] = pack8_bf16(uv); du[1] = pack8_bf16(uv + 8);
+                        // GU is only read again by the backward: stream it past L2 (evict-first)
+                        __stcs(dg, pack8_bf16(gv)); __stcs(dg + 1, pack8_bf16(gv + 8));
+                        __stcs(du, pack8_bf16(uv)); __stcs(du + 1, pack8_bf16(uv + 8));
                         dh[0] = pack8_bf16(hv); dh[1] = pack8_bf16(hv + 8);
                     }
                 }
@@ -359,9 +426,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                         o[1] = pack8_bf16(v + 8);
                     }
                 }
+            } else if constexpr (EPI == EPI_BF16) {
+                bf16* out = (bf16*)g.out0;
+#pragma unroll 1
+                for (int c = c0; c < c0 + kSpan; c += 16) {
+                    float v[16];
+                    tc::tmem_ld16(tb + c, v);
+                    tc::tmem_ld_wait();
+                    const int n = nt * BN + c;
+                    if (valid && n < g.Ncols) {
+                        uint4* o = reinterpret_cast<uint4*>(out + (int64_t)p * g.ldo + n);
+                        // read once by the combine and once by the backward: evict-first
+                        __stcs(o, pack8_bf16(v));
+                        __stcs(o + 1, pack8_bf16(v + 8));
+                    }
+                }
             } else {
                 float* out = (float*)g.out0;
-                const float w = (EPI == EPI_ROWSCALE_F32 && valid) ? g.w_sorted[p] : 1.0f;
 #pragma unroll 1
                 for (int c = c0; c < c0 + kSpan; c += 16) {
                     float v[16];
@@ -371,21 +452,26 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                     if (valid && n < g.Ncols) {
                         float4* o = reinterpret_cast<float4*>(out + (int64_t)p * g.ldo + n);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            o[i] = make_float4(w * v[4 * i], w * v[4 * i + 1], w * v[4 * i + 2], w * v[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i)   // read once by the combine: evict-first
+                            __stcs(o + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
                     }
                 }
             }
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&tempty_bar[acc]));
+            if (lane == 0) {
+                if constexpr (PAIR) tc::mbar_arrive_cluster(tempty_leader0 + acc * (uint32_t)sizeof(uint64_t));
+                else tc::mbar_arrive(tc::smem_u32(&tempty_bar[acc]));
+            }
         }
     }
     tc::fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) tc::cluster_sync();    // the leader's MMAs into the peer's TMEM are done
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem_base, kTmemCols);
+        if constexpr (PAIR) tc::tmem_dealloc_pair(tmem_base, kTmemCols);
+        else tc::tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -437,19 +523,52 @@ int sm_count() {
     return cached[dev];
 }
 
-template <int EPI, bool B_MN, int BN>
-cudaError_t launch_tc(const TcParams& P, int grid, size_t smem, cudaStream_t s) {
-    auto k = grouped_gemm_tc_kernel<EPI, B_MN, BN>;
+// One CTA per SM (grid = min(#SMs, tiles)); SM pairs: as many 2-CTA clusters as can be
+// resident at once (so that no pair waits for another to finish), at most one per tile.
+template <int EPI, bool B_MN, int BN, bool PAIR>
+cudaError_t launch_tc(const TcParams& P, int64_t max_tiles, size_t smem, cudaStream_t s) {
+    auto k = grouped_gemm_tc_kernel<EPI, B_MN, BN, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, smem, s>>>(P);
-    return cudaGetLastError();
+    if constexpr (!PAIR) {
+        const int grid = (int)std::min<int64_t>(sm_count(), max_tiles);
+        k<<<grid, kThreads, smem, s>>>(P);
+        return cudaGetLastError();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3((unsigned)(sm_count() & ~1), 1, 1);
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, k, &cfg);
+        if (e != cudaSuccess) return e;
+        if (clusters < 1) return cudaErrorNotSupported;     // caller falls back to single-CTA tiles
+        const int64_t pairs = std::min<int64_t>(clusters, max_tiles);
+        cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+        return cudaLaunchKernelEx(&cfg, k, P);
+    }
 }
+
+// SM pairs halve the B bytes each SM pulls through L2 per flop but pad every expert
+// to 256-row tiles; they pay off when experts average at least MOE_PAIR_MIN_ROWS rows.
+#ifndef MOE_PAIR_MIN_ROWS
+#define MOE_PAIR_MIN_ROWS 384
+#endif
+bool use_sm_pairs(const GroupedGemm& g) { return g.N >= (int64_t)MOE_PAIR_MIN_ROWS * g.E; }
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
-    if (g.N == 0) return cudaSuccess;
+namespace {
+
+cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) {
     if (g.K % BK != 0) return cudaErrorInvalidValue;
     const bool proj = g.epi == EPI_PROJ;
     const int BN = proj ? g.Ncols : 256;
@@ -461,6 +580,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
     P.g = g;
     P.num_kb = g.K / BK;
     const bool paired = g.epi == EPI_SWIGLU;
+    const bool pair = allow_pairs && !proj && use_sm_pairs(g);
     P.n_tiles = proj ? 1 : (paired ? (g.Ncols + 127) / 128 : (g.Ncols + 255) / 256);
     // A: [N, K]
     {
@@ -475,7 +595,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
         const uint64_t dims[3] = {(uint64_t)g.ldb, rows, (uint64_t)g.E};
         const uint64_t st[2] = {(uint64_t)g.ldb * 2, (uint64_t)g.b_expert_stride * 2};
         const uint32_t box_mn[3] = {64, BK, 1};
-        const uint32_t box_k[3] = {BK, (uint32_t)BN, 1};
+        const uint32_t box_k[3] = {BK, (uint32_t)(pair ? BN / 2 : BN), 1};
         if (!encode(&P.tm_b, g.B, 3, dims, st, g.b_mn_major ? box_mn : box_k, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
@@ -495,27 +615,59 @@ cudaError_t launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
         if (!encode(&P.tm_b2, g.B2, 3, dims2, st2, box2, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
         P.b2_box_bytes = 64 * rp * 2;
     }
-    const int64_t max_tiles = ((g.N + BM - 1) / BM + g.E) * (int64_t)P.n_tiles;
-    const int grid = (int)std::min<int64_t>(sm_count(), max_tiles);
+    const int64_t tm = pair ? 2 * BM : BM;
+    const int64_t max_tiles = ((g.N + tm - 1) / tm + g.E) * (int64_t)P.n_tiles;
     const size_t offs_bytes = (size_t)2 * (g.E + 1) * sizeof(int32_t);
     const bool mn = g.b_mn_major;
     if (proj) {
         switch (BN) {
-            case 16: return launch_tc<EPI_PROJ, false, 16>(P, grid, Geo<16>::kSmem + offs_bytes, s);
-            case 32: return launch_tc<EPI_PROJ, false, 32>(P, grid, Geo<32>::kSmem + offs_bytes, s);
-            default: return launch_tc<EPI_PROJ, false, 64>(P, grid, Geo<64>::kSmem + offs_bytes, s);
+            case 16: return launch_tc<EPI_PROJ, false, 16, false>(P, max_tiles, Geo<16>::kSmem + offs_bytes, s);
+            case 32: return launch_tc<EPI_PROJ, false, 32, false>(P, max_tiles, Geo<32>::kSmem + offs_bytes, s);
+            default: return launch_tc<EPI_PROJ, false, 64, false>(P, max_tiles, Geo<64>::kSmem + offs_bytes, s);
         }
+    }
+    if (pair) {
+        const size_t smem = Geo<256, true>::kSmem + offs_bytes;
+        cudaError_t e;
+        switch (g.epi) {
+            case EPI_SWIGLU: e = launch_tc<EPI_SWIGLU, true, 256, true>(P, max_tiles, smem, s); break;
+            case EPI_BF16:
+                e = mn ? launch_tc<EPI_BF16, true, 256, true>(P, max_tiles, smem, s)
+                       : launch_tc<EPI_BF16, false, 256, true>(P, max_tiles, smem, s);
+                break;
+            case EPI_DSWIGLU:
+                e = mn ? launch_tc<EPI_DSWIGLU, true, 256, true>(P, max_tiles, smem, s)
+                       : launch_tc<EPI_DSWIGLU, false, 256, true>(P, max_tiles, smem, s);
+                break;
+            default:
+                e = mn ? launch_tc<EPI_PLAIN_F32, true, 256, true>(P, max_tiles, smem, s)
+                       : launch_tc<EPI_PLAIN_F32, false, 256, true>(P, max_tiles, smem, s);
+        }
+        return e;
     }
     const size_t smem = Geo<256>::kSmem + offs_bytes;
     switch (g.epi) {
-        case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256>(P, grid, smem, s);
-        case EPI_ROWSCALE_F32:
-            return mn ? launch_tc<EPI_ROWSCALE_F32, true, 256>(P, grid, smem, s)
-                      : launch_tc<EPI_ROWSCALE_F32, false, 256>(P, grid, smem, s);
+        case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256, false>(P, max_tiles, smem, s);
+        case EPI_BF16:
+            return mn ? launch_tc<EPI_BF16, true, 256, false>(P, max_tiles, smem, s)
+                      : launch_tc<EPI_BF16, false, 256, false>(P, max_tiles, smem, s);
         case EPI_DSWIGLU:
-            return mn ? launch_tc<EPI_DSWIGLU, true, 256>(P, grid, smem, s) : launch_tc<EPI_DSWIGLU, false, 256>(P, grid, smem, s);
-        default: return mn ? launch_tc<EPI_F32, true, 256>(P, grid, smem, s) : launch_tc<EPI_F32, false, 256>(P, grid, smem, s);
+            return mn ? launch_tc<EPI_DSWIGLU, true, 256, false>(P, max_tiles, smem, s)
+                      : launch_tc<EPI_DSWIGLU, false, 256, false>(P, max_tiles, smem, s);
+        default:
+            return mn ? launch_tc<EPI_PLAIN_F32, true, 256, false>(P, max_tiles, smem, s)
+                      : launch_tc<EPI_PLAIN_F32, false, 256, false>(P, max_tiles, smem, s);
     }
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(const GroupedGemm& g, cudaStream_t s) {
+    if (g.N == 0) return cudaSuccess;
+    const cudaError_t e = launch_impl(g, true, s);
+    // no resident 2-CTA cluster fits on this device: single-CTA tiles
+    if (e == cudaErrorNotSupported) return launch_impl(g, false, s);
+    return e;
 }
 
 }  // namespace moe

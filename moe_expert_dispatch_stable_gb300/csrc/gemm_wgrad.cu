@@ -32,16 +32,27 @@ constexpr int kWStages = 6;
 constexpr int kWThreads = 192;
 constexpr int kWABytes = WM * WK * 2;   // 16 KB
 
+// Up to two problems with the same expert partition and rank share one launch.
 struct WgradParams {
-    CUtensorMap tm_big, tm_small;
+    CUtensorMap tm_big[2], tm_small[2];
     const int32_t* offsets;
-    bf16* D;
-    int E, M, r, rp;
-    int m_tiles;
-    int b_bytes;        // WK * rp * 2
+    bf16* D[2];
+    int M[2];
+    int m_tiles[2];
+    int nprob;
+    int E, r, rp;
     uint32_t b_sbo, b_swz;
     int32_t* dev_status;
 };
+
+// tile t -> (problem, expert, 128-column tile)
+__device__ __forceinline__ void wg_decode(const WgradParams& P, int t, int& prob, int& e, int& mt) {
+    const int t0 = P.E * P.m_tiles[0];
+    prob = t < t0 ? 0 : 1;
+    const int u = prob == 0 ? t : t - t0;
+    e = u / P.m_tiles[prob];
+    mt = u - e * P.m_tiles[prob];
+}
 
 template <int RP>
 __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __grid_constant__ WgradParams P) {
@@ -75,8 +86,10 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
         tc::fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        tc::prefetch_tmap(&P.tm_big);
-        tc::prefetch_tmap(&P.tm_small);
+        for (int i = 0; i < P.nprob; ++i) {
+            tc::prefetch_tmap(&P.tm_big[i]);
+            tc::prefetch_tmap(&P.tm_small[i]);
+        }
     }
     if (warp == 1) {
         tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
@@ -86,14 +99,15 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = E * P.m_tiles;
+    const int total = E * (P.m_tiles[0] + (P.nprob > 1 ? P.m_tiles[1] : 0));
 
     if (warp == 0) {
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             for (int t = blockIdx.x; t < total && !*s_abort; t += gridDim.x) {
-                const int e = t / P.m_tiles, mt = t - e * P.m_tiles;
+                int prob, e, mt;
+                wg_decode(P, t, prob, e, mt);
                 const int beg = s_off[e], end = s_off[e + 1];
                 for (int p0 = beg; p0 < end; p0 += WK) {
                     if (!tc::mbar_wait(tc::smem_u32(&empty_bar[stage]), phase ^ 1)) {
@@ -104,9 +118,9 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
                     const uint32_t fb = tc::smem_u32(&full_bar[stage]);
                     const uint32_t sa = tc::smem_u32(smem + stage * kStageBytes);
                     tc::mbar_arrive_expect_tx(fb, kWABytes + kBBytes);
-                    tc::tma_load_2d(sa, &P.tm_big, fb, mt * WM, p0);
-                    tc::tma_load_2d(sa + kWABytes / 2, &P.tm_big, fb, mt * WM + 64, p0);
-                    tc::tma_load_2d(sa + kWABytes, &P.tm_small, fb, 0, p0);
+                    tc::tma_load_2d(sa, &P.tm_big[prob], fb, mt * WM, p0);
+                    tc::tma_load_2d(sa + kWABytes / 2, &P.tm_big[prob], fb, mt * WM + 64, p0);
+                    tc::tma_load_2d(sa + kWABytes, &P.tm_small[prob], fb, 0, p0);
                     if (++stage == kWStages) {
                         stage = 0;
                         phase ^= 1;
@@ -120,7 +134,8 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
         uint32_t phase = 0;
         int it = 0;
         for (int t = blockIdx.x; t < total && !*s_abort; t += gridDim.x) {
-            const int e = t / P.m_tiles;
+            int prob, e, mt;
+            wg_decode(P, t, prob, e, mt);
             const int beg = s_off[e], end = s_off[e + 1];
             if (end == beg) continue;                       // written as zeros by the epilogue
             const int acc = it & 1;
@@ -184,12 +199,14 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
         const int row = q * 32 + lane;
         int it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const int e = t / P.m_tiles, mt = t - e * P.m_tiles;
+            int prob, e, mt;
+            wg_decode(P, t, prob, e, mt);
+            const int M = P.M[prob];
             const int m = mt * WM + row;
-            bf16* De = P.D + (int64_t)e * P.r * P.M;
+            bf16* De = P.D[prob] + (int64_t)e * P.r * M;
             if (s_off[e + 1] == s_off[e]) {
-                if (m < P.M)
-                    for (int j = 0; j < P.r; ++j) De[(int64_t)j * P.M + m] = f2bf(0.f);
+                if (m < M)
+                    for (int j = 0; j < P.r; ++j) De[(int64_t)j * M + m] = f2bf(0.f);
                 continue;
             }
             const int acc = it & 1;
@@ -210,10 +227,10 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
                 float v[16];
                 tc::tmem_ld16(tb + c, v);
                 tc::tmem_ld_wait();
-                if (m < P.M) {
+                if (m < M) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        if (c + i < P.r) De[(int64_t)(c + i) * P.M + m] = f2bf(v[i]);
+                        if (c + i < P.r) De[(int64_t)(c + i) * M + m] = f2bf(v[i]);
                 }
             }
             tc::fence_before_sync();
@@ -276,7 +293,7 @@ cudaError_t launch_wg(const WgradParams& P, cudaStream_t s) {
     auto k = lora_wgrad_tc_kernel<RP>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int total = P.E * P.m_tiles;
+    const int total = P.E * (P.m_tiles[0] + (P.nprob > 1 ? P.m_tiles[1] : 0));
     const int grid = std::min(wg_sm_count(), total);
     k<<<grid, kWThreads, smem, s>>>(P);
     return cudaGetLastError();
@@ -284,23 +301,30 @@ cudaError_t launch_wg(const WgradParams& P, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_lora_wgrad_tc(const void* Small, int rp, int r, const void* Big, int M, const int32_t* offsets,
-                                 int E, int64_t N, void* D, int32_t* dev_status, cudaStream_t s) {
-    if (M % 64 != 0 || (rp != 16 && rp != 32 && rp != 64)) return cudaErrorInvalidValue;
+cudaError_t launch_lora_wgrad_tc(const WgradProblem* probs, int nprob, int rp, int r, const int32_t* offsets, int E,
+                                 int64_t N, int32_t* dev_status, cudaStream_t s) {
+    if (nprob < 1 || nprob > 2 || (rp != 16 && rp != 32 && rp != 64)) return cudaErrorInvalidValue;
     WgradParams P;
     memset(&P, 0, sizeof(P));
     P.offsets = offsets;
-    P.D = (bf16*)D;
-    P.E = E; P.M = M; P.r = r; P.rp = rp;
-    P.m_tiles = (M + WM - 1) / WM;
+    P.nprob = nprob;
+    P.E = E; P.r = r; P.rp = rp;
     P.dev_status = dev_status;
     P.b_sbo = 8 * rp * 2;
     P.b_swz = rp >= 64 ? tc::kSw128 : (rp >= 32 ? tc::kSw64 : tc::kSw32);
     const CUtensorMapSwizzle bsw = rp >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B
                                             : (rp >= 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
     const uint64_t rows = N > 0 ? (uint64_t)N : 1;
-    if (!encode2d(&P.tm_big, Big, (uint64_t)M, rows, 64, WK, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-    if (!encode2d(&P.tm_small, Small, (uint64_t)rp, rows, (uint32_t)rp, WK, bsw)) return cudaErrorInvalidValue;
+    for (int i = 0; i < nprob; ++i) {
+        const WgradProblem& q = probs[i];
+        if (q.M % 64 != 0) return cudaErrorInvalidValue;
+        P.D[i] = (bf16*)q.D;
+        P.M[i] = q.M;
+        P.m_tiles[i] = (q.M + WM - 1) / WM;
+        if (!encode2d(&P.tm_big[i], q.Big, (uint64_t)q.M, rows, 64, WK, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        if (!encode2d(&P.tm_small[i], q.Small, (uint64_t)rp, rows, (uint32_t)rp, WK, bsw)) return cudaErrorInvalidValue;
+    }
     switch (rp) {
         case 16: return launch_wg<16>(P, s);
         case 32: return launch_wg<32>(P, s);

@@ -16,25 +16,40 @@ cudaError_t launch_route(const void* idx, int idx_bytes, const float* topk_w, in
 cudaError_t route_static_scratch(void** ptr);
 
 // ---- row kernels (rowops.cu)
-// dst[p, :] = src[perm[p] / k, :]   (optionally scaled by w_sorted[p], rounded to bf16)
+// dst[p, :] = src[perm[p] / k, :]   (optionally scaled by w_sorted[p], rounded to bf16).
+// With O and d_w given: d_w[perm[p]] = <src[perm[p] / k, :], O[p, :]> (fp32), in the same pass.
 cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, const float* w_sorted,
-                               int64_t N, int k, void* dst, cudaStream_t s);
-// out[t, :] = bf16( sum_{j<k} src[inv_perm[t*k+j], :] )  (fp32 src, fixed j order)
-cudaError_t launch_combine(const float* src, const int32_t* inv_perm, int64_t T, int k, int H,
-                           void* out, cudaStream_t s);
+                               int64_t N, int k, void* dst, const void* O, float* d_w, cudaStream_t s);
+// out[t, :] = bf16( sum_{j<k} w * src[inv_perm[t*k+j], :] ), w = w_sorted[inv_perm[t*k+j]] (or 1 when
+// w_sorted is null); bf16 or fp32 src, fp32 sum in the fixed order j = 0..k-1
+cudaError_t launch_combine(const void* src, bool src_f32, const float* w_sorted, const int32_t* inv_perm, int64_t T,
+                           int k, int H, void* out, cudaStream_t s);
+
+// ---- router (router.cu)
+cudaError_t launch_router_topk(const float* logits, int64_t T, int E, int k, int32_t* topk_idx, float* topk_w,
+                               cudaStream_t s);
+cudaError_t launch_router_bwd(const float* logits, const int32_t* topk_idx, const float* d_topk_w, int64_t T, int E,
+                              int k, float* d_logits, cudaStream_t s);
 
 // ---- per-expert LoRA weight gradients (gemm_wgrad.cu)
 // D[e, j, m] = sum_{p in rows of e} Small[p, j] * Big[p, m]  (bf16 out [E, r, M]) on the
-// tensor cores, one CTA per (expert, 128 columns), fixed row order, zeros for empty experts.
-cudaError_t launch_lora_wgrad_tc(const void* Small, int rp, int r, const void* Big, int M, const int32_t* offsets,
-                                 int E, int64_t N, void* D, int32_t* dev_status, cudaStream_t s);
+// tensor cores, one CTA per (problem, expert, 128 columns), fixed row order, zeros for
+// empty experts.  One or two problems (same experts, same rank) per launch.
+struct WgradProblem {
+    const void* Small;   // [N, RP] bf16
+    const void* Big;     // [N, M] bf16
+    int M;
+    void* D;             // [E, r, M] bf16
+};
+cudaError_t launch_lora_wgrad_tc(const WgradProblem* probs, int nprob, int rp, int r, const int32_t* offsets, int E,
+                                 int64_t N, int32_t* dev_status, cudaStream_t s);
 
 // ---- grouped GEMMs (gemm_tc.cu)
 enum GemmEpi : int {
     EPI_SWIGLU = 0,     // paired gate/up accumulators -> GU (bf16, [N,2I]) and h (bf16, [N,I])
-    EPI_ROWSCALE_F32 = 1,  // out_f32[p, n] = w_sorted[p] * acc
+    EPI_BF16 = 1,       // out_bf16[p, n] = acc
     EPI_DSWIGLU = 2,    // acc = dh; reads GU, writes dGU (bf16 [N,2I])
-    EPI_F32 = 3,        // out_f32[p, n] = acc
+    EPI_PLAIN_F32 = 3,  // out_f32[p, n] = acc
     EPI_PROJ = 4        // out_bf16[p, 0:Ncols] = scale * acc  (rank-r projection, Ncols = RP)
 };
 
@@ -59,11 +74,10 @@ struct GroupedGemm {
     int64_t b2_expert_stride;
     const int32_t* offsets;      // [E+1]
     const int32_t* tile_offsets; // [E+1], 128-row tiles
-    const float* w_sorted;       // EPI_ROWSCALE_F32
     const void* gu_in;           // EPI_DSWIGLU: GU [N, 2*Ncols]
-    void* out0;                  // EPI_SWIGLU: GU; EPI_DSWIGLU: dGU; F32 epilogues: float out
+    void* out0;                  // EPI_SWIGLU: GU; EPI_DSWIGLU: dGU; BF16: bf16 out; PLAIN_F32: fp32 out
     void* out1;                  // EPI_SWIGLU: h
-    int ldo;                     // row length of the fp32 output
+    int ldo;                     // row length of the BF16 / PLAIN_F32 output
     float scale;                 // EPI_PROJ
     int epi;
     int32_t* dev_status;

@@ -33,6 +33,11 @@ against the pages:
 * backward -- the GPU MODE lecture's principle "start from the exact math":
   the gradient of each step is derived by hand (here: chain rule through the
   merged matrices, below), not by autograd.
+* router -- the step in front of the routing in every workload: softmax over
+  the E router logits of a token, then the k largest probabilities (no
+  renormalisation, ties to the lower expert index); its backward is the
+  softmax VJP with the selection held fixed, fed by dL/dw[t,j] = <dy[t],
+  unweighted expert output> (y is linear in the routing weights).
 
 Layouts follow the C ABI: x [T,H]; W_gu [E,H,2I]; W_d [E,I,H]; A_gu [E,r,H]
 (= A^T, PEFT lora_A layout); B_gu [E,r,2I]; A_d [E,r,I]; B_d [E,r,H].
@@ -40,7 +45,9 @@ In math form A_math = A_stored^T (in x r) and B_math = B_stored (r x out).
 
 Parity pins: see tests/test_oracle.py (invariants, library sort, brute force,
 split == merged, B = 0, E = 1 dense MLP, finite differences, a hand-worked
-golden case).  No numeric example of the layer is printed on the pages.
+golden case) and tests/test_oracle_router.py (library top-k, torch autograd
+of the softmax, exact directional derivative in w, finite differences of the
+composed router + layer).  No numeric example is printed on the pages.
 """
 from __future__ import annotations
 
@@ -223,3 +230,58 @@ def lora_bwd(dy, x, topk_idx, topk_w, W_gu, A_gu, B_gu, W_d, A_d, B_d, scale,
             dA_d[e] = scale * (Bd @ dM_d.T)
             dB_d[e] = scale * (Ad @ dM_d)
     return dx, dA_gu, dB_gu, dA_d, dB_d
+
+
+# --------------------------------------------------------------------------
+# router (the step in front of the routing, and its gradient)
+# --------------------------------------------------------------------------
+def router_topk(logits, k: int):
+    """Softmax over all E logits, then the k largest probabilities, descending,
+    ties to the lower expert index, no renormalisation (the router recipe of
+    the workloads).  Softmax is strictly increasing in each logit, so the
+    selection is made on the logits themselves and is exact.
+
+    Returns topk_idx [T,k] int64, topk_w [T,k] and the probabilities p [T,E]."""
+    z = _f64(logits)
+    order = np.argsort(-z, axis=1, kind="stable")[:, :k]
+    zc = z - z.max(axis=1, keepdims=True)
+    p = np.exp(zc)
+    p /= p.sum(axis=1, keepdims=True)
+    return order.astype(np.int64), np.take_along_axis(p, order, axis=1), p
+
+
+def router_bwd(logits, topk_idx, d_topk_w):
+    """VJP of topk_w[t,j] = softmax(z[t])[topk_idx[t,j]] with the selection held
+    fixed: d p_i / d z_e = p_i (delta_ie - p_e), hence
+      dz[t,e] = p_e * (g_e - sum_j d_topk_w[t,j] * topk_w[t,j]),
+    with g_e = d_topk_w[t,j] if e = topk_idx[t,j] (else 0)."""
+    z = _f64(logits)
+    idx = _i64(topk_idx)
+    dw = _f64(d_topk_w)
+    zc = z - z.max(axis=1, keepdims=True)
+    p = np.exp(zc)
+    p /= p.sum(axis=1, keepdims=True)
+    w = np.take_along_axis(p, idx, axis=1)
+    g = np.zeros_like(p)
+    np.put_along_axis(g, idx, dw, axis=1)
+    return p * (g - (dw * w).sum(axis=1, keepdims=True))
+
+
+def lora_dtopk_w(dy, x, topk_idx, W_gu, A_gu, B_gu, W_d, A_d, B_d, scale, token_subset=None):
+    """Gradient of L = <dy, y> w.r.t. the routing weights: y is linear in them,
+    so dL/dw[t,j] = <dy[t], f_e(x[t])> with f_e the unweighted expert output
+    (merged weights, fp64).  Slots of tokens outside token_subset stay 0."""
+    x = _f64(x); idx = _i64(topk_idx); dy = _f64(dy)
+    T = x.shape[0]
+    E = W_gu.shape[0]
+    I = W_d.shape[1]
+    dw = np.zeros(idx.shape)
+    for e in range(E):
+        t_idx, j_idx = _expert_rows(idx, e, token_subset)
+        if t_idx.size == 0:
+            continue
+        M_gu = merged(_f64(W_gu[e]), _f64(A_gu[e]), _f64(B_gu[e]), scale)
+        M_d = merged(_f64(W_d[e]), _f64(A_d[e]), _f64(B_d[e]), scale)
+        O = swiglu(x[t_idx] @ M_gu, I) @ M_d
+        dw[t_idx, j_idx] = (dy[t_idx] * O).sum(axis=1)
+    return dw

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.moe_abi_version() == 1
+    assert lib.moe_abi_version() == 2
     for code in range(0, 7):
         assert lib.moe_status_string(code)
 
@@ -55,7 +55,8 @@ def test_size_queries_and_dim_checks(lib):
     saved, ws = b.moe_lora_fwd_sizes(ok)
     N = 4096 * 4
     assert saved >= N * 2880 * 2 + N * 5760 * 2 + N * 2880 * 2 + 2 * N * 16 * 2
-    assert ws >= N * 2880 * 4
+    assert ws == 0                                          # the forward keeps everything in `saved`
+    assert saved >= N * (2880 * 2 + 5760 * 2 + 2880 * 2 + 2 * 16 * 2 + 2880 * 2)
     assert b.moe_lora_bwd_workspace_size(ok) >= N * (2880 * 2 + 5760 * 2 + 2880 * 4)
     offs, rp = b.moe_lora_saved_layout(ok)
     assert rp == 16 and offs[0] == 0 and all(o % 256 == 0 for o in offs) and offs == sorted(offs)
@@ -93,8 +94,19 @@ def test_null_and_misaligned_arguments_rejected_before_launch(lib):
     assert lib.moe_lora_fwd(ctypes.byref(d), ctypes.byref(rt), *p, ctypes.c_void_p(16), 1,
                             ctypes.c_void_p(16), 1 << 30, ctypes.c_void_p(16), None) == 4
     assert lib.moe_lora_bwd(ctypes.byref(d), ctypes.byref(rt), *p[:7], ctypes.c_void_p(16), 1 << 30,
-                            ctypes.c_void_p(24), *p[:4], ctypes.c_void_p(16), 1 << 30, ctypes.c_void_p(16),
+                            ctypes.c_void_p(24), *p[:4], None, ctypes.c_void_p(16), 1 << 30, ctypes.c_void_p(16),
                             None) == 3
+    # misaligned d_topk_w
+    assert lib.moe_lora_bwd(ctypes.byref(d), ctypes.byref(rt), *p[:7], ctypes.c_void_p(16), 1 << 30,
+                            ctypes.c_void_p(16), *p[:4], ctypes.c_void_p(20), ctypes.c_void_p(16), 1 << 30,
+                            ctypes.c_void_p(16), None) == 3
+    # router: bad sizes, NULL outputs, misaligned logits
+    assert lib.moe_router_topk(ctypes.c_void_p(16), 8, 4, 5, ctypes.c_void_p(16), ctypes.c_void_p(16), None) == 2
+    assert lib.moe_router_topk(ctypes.c_void_p(16), 8, 2048, 2, ctypes.c_void_p(16), ctypes.c_void_p(16), None) == 2
+    assert lib.moe_router_topk(ctypes.c_void_p(16), 8, 4, 2, None, ctypes.c_void_p(16), None) == 1
+    assert lib.moe_router_topk(ctypes.c_void_p(20), 8, 4, 2, ctypes.c_void_p(16), ctypes.c_void_p(16), None) == 3
+    assert lib.moe_router_bwd(ctypes.c_void_p(16), ctypes.c_void_p(16), None, 8, 4, 2, ctypes.c_void_p(16),
+                              None) == 1
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
