@@ -84,6 +84,13 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
     return w
 
 
+# DRAM bytes (read + write) per launch from ncu captures of the current kernels
+# (profiles/), keyed by (workload, kernel); None where no capture of the current code exists.
+MEASURED_TRAFFIC = {
+    ("gptoss20b", "gemm_gate_up_fwd"): 1.434e9 + 0.263e9,
+}
+
+
 def step_flops(cfg: mi.MoEConfig) -> int:
     """Algorithmic fwd+bwd flops of the layer: N (12 H I + 12 H r + 18 I r)."""
     N = cfg.T * cfg.k
@@ -98,6 +105,25 @@ def load_peaks():
         return dict(hbm_gbs=p["hbm_gbs"], bf16_tflops=p["bf16_tflops"],
                     bf16_tflops_sustained=p.get("bf16_tflops_sustained", p["bf16_tflops"]), source="measured")
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest `value` over all ranks (identity without torch.distributed): the job's
+    time is its slowest replica's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_replica_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job tokens/s of `world` independent replicas (weak scaling): all replicas'
+    tokens over the slowest replica's time."""
+    return tokens_per_replica_step * steps * world / (max_ms / 1e3)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -216,6 +242,56 @@ def config_dict(cfg):
             "l2": "flushed between steps (256 MiB write); inputs+weights also exceed L2"}
 
 
+# ----------------------------------------------------------------------------- offload
+def offload_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, L: int, reps: int) -> dict:
+    """Backward of an L-layer stack (shared weights) with the saved activations in
+    pinned host memory, reloaded with two device buffers or one, against the same
+    stack with every layer's activations resident."""
+    import torch
+    from moe_expert_dispatch_stable_gb300.offload import OffloadedMoEStack
+    weights = [layer.w] * L
+    routing = [(t_idx, t_w)] * L
+    out = {"layers": L, "saved_bytes_per_layer": None}
+    resident = [moe.MoELoRALayer(layer.d, layer.w, dev) for _ in range(L)]
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        total = 0.0
+        for _ in range(reps):
+            s.record()
+            fn()
+            e.record()
+            torch.cuda.synchronize()
+            total += s.elapsed_time(e)
+        return total / reps
+
+    def res_fwd():
+        x = ts["x"]
+        for l in range(L):
+            resident[l].route(*routing[l])
+            x = resident[l].forward(x)
+
+    def res_bwd():
+        g = ts["dy"]
+        for l in range(L - 1, -1, -1):
+            g = resident[l].backward(g, with_topk_grad=False)[0]
+    res_fwd()
+    out["bwd_ms_resident"] = timed(res_bwd)
+    del resident
+    for nb in (2, 1):
+        stack = OffloadedMoEStack(layer.d, weights, dev, buffers=nb)
+        out["saved_bytes_per_layer"] = stack.saved_bytes
+        stack.forward(ts["x"], routing)
+        torch.cuda.synchronize()
+        out[f"bwd_ms_{'double' if nb == 2 else 'single'}"] = timed(lambda: stack.backward(ts["dy"]))
+        del stack
+    torch.cuda.empty_cache()
+    out["h2d_gb_per_bwd"] = L * out["saved_bytes_per_layer"] / 1e9
+    return out
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -227,6 +303,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--breakdown", action="store_true", help="print per-kernel times to stderr")
+    ap.add_argument("--no-offload", action="store_true", help="skip the offloaded-stack measurement")
+    ap.add_argument("--offload-layers", type=int, default=4)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = mi.CONFIGS[args.config]
@@ -292,12 +370,8 @@ def main():
     launches = moe.moe_launch_count() - launches0
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kt = moe.moe_timing_read()
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = cfg.T * args.steps * world / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(step_ms), dev)
+    value = job_throughput(cfg.T, args.steps, world, total_ms)
 
     # ---- end to end through host buffers
     h_x = ts["x"].cpu().pin_memory(); h_dy = ts["dy"].cpu().pin_memory()
@@ -326,13 +400,9 @@ def main():
         e2e_step()
         e_e[i].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e))
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)), dev)
     clk = clocks.stop()
-    e2e_value = cfg.T * args.steps * world / (e2e_ms / 1e3)
+    e2e_value = job_throughput(cfg.T, args.steps, world, e2e_ms)
     assert int(layer.dev_status.item()) == 0, "device status flag set"
 
     # ---- roofline of the dominant kernel and the GEMM aggregate
@@ -345,13 +415,15 @@ def main():
     if wk["bound"] == "tensor":
         ach = wk["flops"] / (ms_launch / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"], "traffic": None,
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"],
+                "traffic": MEASURED_TRAFFIC.get((cfg.name, dom)),
                 "algorithmic_flops_per_launch": wk["flops"], "ms_per_launch": ms_launch,
                 "peak_source": f"{peaks['source']} bf16 sustained"}
     else:
         ach = wk["bytes"] / (ms_launch / 1e3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": wk["bytes"],
+                "frac": ach / peaks["hbm_gbs"], "traffic": MEASURED_TRAFFIC.get((cfg.name, dom)),
+                "algorithmic_bytes_per_launch": wk["bytes"],
                 "ms_per_launch": ms_launch, "peak_source": f"{peaks['source']} hbm copy"}
     g_ms = sum(kt[n][0] for n in GEMM_KERNELS if n in kt) / args.steps
     g_fl = sum(work[n]["flops"] for n in GEMM_KERNELS)
@@ -389,6 +461,11 @@ def main():
     r_bytes = {"router_topk": te + cfg.T * cfg.k * 8, "router_bwd": 2 * te + cfg.T * cfg.k * 8}
     line["router"] = {n: {"us_per_launch": 1e3 * ms / cnt, "gbs": r_bytes[n] / (ms / cnt / 1e3) / 1e9}
                       for n, (ms, cnt) in rt_t.items() if n in r_bytes}
+    # ---- stack of layers with saved activations offloaded to pinned host memory:
+    # backward time with double-buffered reload vs single buffer vs resident
+    if not args.no_offload:
+        line["offload"] = offload_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, args.offload_layers,
+                                              max(3, args.steps // 20))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         wts = [ts[n].cpu() for n in ("W_gu", "A_gu", "B_gu", "W_d", "A_d", "B_d")]
         line["cpu_baseline"] = cpu_baseline(cfg, idx, w, ts["x"].cpu(), ts["dy"].cpu(), wts)

@@ -45,9 +45,12 @@ constexpr int kBoxMN = 64 * BK * 2;          // one 64-column MN-major box of B:
 // each CTA holding 128 rows of A and 128 columns of B per stage.
 template <int BN, bool PAIR = false>
 struct Geo {
-    static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK * 2;
-    static constexpr int kStageBytes = kABytes + ((kBBytes + 1023) / 1024) * 1024;
-    static constexpr int kStages = PAIR ? 6 : (BN >= 256 ? 4 : 8);
+    // narrow tiles (the HBM-bound projections) load KW 64-column boxes of A per stage so
+    // that every row is fetched in 256-512 byte runs
+    static constexpr int KW = BN >= 256 ? 1 : (BN <= 16 ? 4 : 2);
+    static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK * 2 * KW;
+    static constexpr int kStageBytes = kABytes * KW + ((kBBytes + 1023) / 1024) * 1024;
+    static constexpr int kStages = PAIR ? 6 : (BN >= 256 ? 4 : (216 * 1024) / kStageBytes);
     static constexpr int kAccCols = BN;
     static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
@@ -199,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                 int e, mt, nt;
                 decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
                 const int m0 = s_off[e] + mt * TM + (int)rank * BM;      // this CTA's 128 rows
-                const int nkb = P.num_kb + (P.lora_k16 ? 1 : 0);
+                const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : P.num_kb + (P.lora_k16 ? 1 : 0);
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!tc::mbar_wait(tc::smem_u32(&empty_bar[stage]), phase ^ 1)) {
                         set_timeout(g, s_abort);
@@ -229,6 +232,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                             for (int jj = 0; jj < 2; ++jj)
                                 tc::tma_load_3d_pair(sb + jj * P.b2_box_bytes, &P.tm_b2, fb,
                                                      b_col<PAIRED, BN>(2 * (int)rank + jj, nt, g.Ncols), 0, e);
+                        }
+                    } else if constexpr (G::KW > 1) {
+                        // narrow tile: KW consecutive 64-column boxes of A and of B per stage
+                        const uint32_t fb = fb_local;
+                        const int nbox = min(G::KW, P.num_kb - kb * G::KW);
+                        tc::mbar_arrive_expect_tx(fb, nbox * (kABytes + BN * BK * 2));
+                        for (int j = 0; j < nbox; ++j) {
+                            const int kx = (kb * G::KW + j) * BK;
+                            tc::tma_load_2d(sa + j * kABytes, &P.tm_a, fb, kx, m0);
+                            tc::tma_load_3d(sa + G::KW * kABytes + j * (BN * BK * 2), &P.tm_b, fb, kx, nt * BN, e);
                         }
                     } else {
                         const uint32_t fb = fb_local;
@@ -276,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                 }
                 tc::fence_after_sync();
                 const uint32_t d = tmem_base + acc * kAccCols;
-                const int nkb = P.num_kb + (P.lora_k16 ? 1 : 0);
+                const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : P.num_kb + (P.lora_k16 ? 1 : 0);
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!tc::mbar_wait(tc::smem_u32(&full_bar[stage]), phase)) {
@@ -287,7 +300,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                     tc::fence_after_sync();
                     const uint32_t sa = tc::smem_u32(smem + stage * kStageBytes);
                     const uint32_t sb = sa + kABytes;
-                    if (kb < P.num_kb) {
+                    if constexpr (G::KW > 1) {
+                        const int nbox = min(G::KW, P.num_kb - kb * G::KW);
+                        for (int j = 0; j < nbox; ++j) {
+#pragma unroll
+                            for (int kk = 0; kk < BK / 16; ++kk) {
+                                const uint64_t ad = tc::smem_desc(sa + j * kABytes + kk * 32, 16, 1024, tc::kSw128);
+                                const uint64_t bd = tc::smem_desc(sa + G::KW * kABytes + j * (BN * BK * 2) + kk * 32, 16,
+                                                                  1024, tc::kSw128);
+                                tc::mma_bf16(d, ad, bd, idesc, (kb > 0 || j > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                    } else if (kb < P.num_kb) {
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk) {
                             const uint64_t ad = tc::smem_desc(sa + kk * 32, 16, 1024, tc::kSw128);
