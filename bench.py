@@ -242,6 +242,36 @@ def config_dict(cfg):
             "l2": "flushed between steps (256 MiB write); inputs+weights also exceed L2"}
 
 
+# ----------------------------------------------------------------------------- fp8 base weights
+def fp8_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, steps: int, flush) -> dict:
+    """route + fwd + bwd with the expert base weights in FP8 (e4m3 codes + power-of-two
+    column scales), timed like the main loop."""
+    import torch
+    wq = moe.quantize_expert_weights(layer.w)
+    q8 = moe.MoELoRALayer(layer.d, wq, dev)
+    for _ in range(3):
+        q8.step(t_idx, t_w, ts["x"], ts["dy"], with_topk_grad=False)
+    torch.cuda.synchronize()
+    moe.moe_timing_enable(True)
+    ms = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        q8.step(t_idx, t_w, ts["x"], ts["dy"], with_topk_grad=False)
+        e.record()
+        torch.cuda.synchronize()
+        ms += s.elapsed_time(e)
+    moe.moe_timing_enable(False)
+    kt = moe.moe_timing_read()
+    assert int(q8.dev_status.item()) == 0
+    gemm_ms = sum(kt[n][0] for n in GEMM_KERNELS if n in kt) / steps
+    wbytes = sum(t.numel() * t.element_size() for n, t in wq.items() if n.startswith(("Wq", "s_")))
+    del q8, wq
+    return {"ms_per_step": ms / steps, "tokens_per_s": cfg.T * steps / (ms / 1e3), "gemm_ms_per_step": gemm_ms,
+            "base_weight_bytes": wbytes, "steps": steps}
+
+
 # ----------------------------------------------------------------------------- offload
 def offload_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, L: int, reps: int) -> dict:
     """Backward of an L-layer stack (shared weights) with the saved activations in
@@ -304,6 +334,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--breakdown", action="store_true", help="print per-kernel times to stderr")
     ap.add_argument("--no-offload", action="store_true", help="skip the offloaded-stack measurement")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-base-weight measurement")
     ap.add_argument("--offload-layers", type=int, default=4)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -461,6 +492,9 @@ def main():
     r_bytes = {"router_topk": te + cfg.T * cfg.k * 8, "router_bwd": 2 * te + cfg.T * cfg.k * 8}
     line["router"] = {n: {"us_per_launch": 1e3 * ms / cnt, "gbs": r_bytes[n] / (ms / cnt / 1e3) / 1e9}
                       for n, (ms, cnt) in rt_t.items() if n in r_bytes}
+    # ---- the same step with FP8 (e4m3) base weights, dequantised inside the GEMMs
+    if not args.no_fp8:
+        line["fp8_base"] = fp8_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, max(10, args.steps // 4), flush)
     # ---- stack of layers with saved activations offloaded to pinned host memory:
     # backward time with double-buffered reload vs single buffer vs resident
     if not args.no_offload:

@@ -205,6 +205,42 @@ MOE_API moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt,
                         void* workspace, size_t workspace_bytes,
                         int32_t* dev_status, void* stream);
 
+/* ---------------------------------------------------------------- FP8 expert base weights
+ * A quantised frozen base (the pages' QLoRA variant of the expert layer, in the
+ * FP8 e4m3 format): per matrix m and column c of W [n_mat, rows, cols] (bf16),
+ *   scales[m, c] = 2^ceil(log2(max_r |W[m, r, c]| / 448))   (1 for an all-zero column)
+ *   Wq[m, r, c]  = e4m3 code of W[m, r, c] / scales[m, c], round to nearest even.
+ * With power-of-two scales the division is exact and every dequantised value
+ * e4m3(Wq) * scale is exactly a bf16 number.  Wq uint8 [n_mat, rows, cols],
+ * scales float32 [n_mat, cols].  One kernel; weight preparation, not the hot path. */
+MOE_API moe_status moe_quantize_fp8(const uint16_t* W, int64_t n_mat, int64_t rows, int32_t cols,
+                                    uint8_t* Wq, float* scales, void* stream);
+
+/* moe_lora_fwd / moe_lora_bwd with FP8 base weights: Wq_gu [E, H, 2I] and Wq_d [E, I, H]
+ * hold e4m3 codes with column scales s_gu [E, 2I] and s_d [E, H] (moe_quantize_fp8).
+ * The GEMMs stream the codes (half the bytes of bf16) and dequantise them to bf16 in
+ * shared memory before the tensor cores read them, so the results are bit-identical to
+ * moe_lora_fwd / moe_lora_bwd called with the dequantised bf16 weights.  The LoRA
+ * factors and activations stay bf16.  Same saved / workspace sizes. */
+MOE_API moe_status moe_lora_fwd_fp8(const moe_dims* d, const moe_routing* rt, const uint16_t* x,
+                                    const uint8_t* Wq_gu, const float* s_gu,
+                                    const uint16_t* A_gu, const uint16_t* B_gu,
+                                    const uint8_t* Wq_d, const float* s_d,
+                                    const uint16_t* A_d, const uint16_t* B_d, uint16_t* y,
+                                    void* saved, size_t saved_bytes,
+                                    void* workspace, size_t workspace_bytes,
+                                    int32_t* dev_status, void* stream);
+MOE_API moe_status moe_lora_bwd_fp8(const moe_dims* d, const moe_routing* rt, const uint16_t* dy,
+                                    const uint8_t* Wq_gu, const float* s_gu,
+                                    const uint16_t* A_gu, const uint16_t* B_gu,
+                                    const uint8_t* Wq_d, const float* s_d,
+                                    const uint16_t* A_d, const uint16_t* B_d,
+                                    const void* saved, size_t saved_bytes,
+                                    uint16_t* dx, uint16_t* dA_gu, uint16_t* dB_gu,
+                                    uint16_t* dA_d, uint16_t* dB_d, float* d_topk_w,
+                                    void* workspace, size_t workspace_bytes,
+                                    int32_t* dev_status, void* stream);
+
 /* ---------------------------------------------------------------- router
  * The step in front of moe_route: the workloads route each token by a softmax
  * over its E router logits followed by the k largest probabilities.

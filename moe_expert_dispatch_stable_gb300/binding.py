@@ -41,7 +41,7 @@ class moe_routing(ctypes.Structure):
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_launch_count", "moe_route_workspace_size", "moe_route",
             "moe_lora_fwd_sizes", "moe_lora_saved_layout", "moe_lora_fwd",
             "moe_lora_bwd_workspace_size", "moe_lora_bwd", "moe_timing_enable", "moe_timing_read",
-            "moe_router_topk", "moe_router_bwd")
+            "moe_router_topk", "moe_router_bwd", "moe_quantize_fp8", "moe_lora_fwd_fp8", "moe_lora_bwd_fp8")
 ABI_VERSION = 2
 
 _lib = None
@@ -69,6 +69,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_lora_bwd_workspace_size.argtypes = [P(moe_dims), P(sz)]
     lib.moe_lora_bwd.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 7 + [vp, sz] + [vp] * 6 + [vp, sz, vp, vp]
     lib.moe_router_topk.argtypes = [vp, i64, i32, i32, vp, vp, vp]
+    lib.moe_quantize_fp8.argtypes = [vp, i64, i64, i32, vp, vp, vp]
+    lib.moe_lora_fwd_fp8.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 10 + [vp, sz, vp, sz, vp, vp]
+    lib.moe_lora_bwd_fp8.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 10 + [sz] + [vp] * 6 + [vp, sz, vp, vp]
     lib.moe_router_bwd.argtypes = [vp, vp, vp, i64, i32, i32, vp, vp]
     lib.moe_launch_count.restype = ctypes.c_uint64
     lib.moe_timing_enable.argtypes = [i32]
@@ -289,6 +292,62 @@ def moe_router_bwd(logits: torch.Tensor, topk_idx: torch.Tensor, d_topk_w: torch
     return d_logits
 
 
+def moe_quantize_fp8(W: torch.Tensor, stream=None):
+    """FP8 (e4m3) codes and per-column power-of-two scales of a bf16 weight stack
+    [..., rows, cols]; returns (Wq uint8, scales float32 [..., cols])."""
+    _need(W, "W", torch.bfloat16)
+    rows, cols = W.shape[-2], W.shape[-1]
+    n_mat = W.numel() // max(rows * cols, 1)
+    Wq = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
+    sc = torch.empty(W.shape[:-2] + (cols,), dtype=torch.float32, device=W.device)
+    _check(load_library().moe_quantize_fp8(_ptr(W), n_mat, rows, cols, _ptr(Wq), _ptr(sc), _stream(stream)))
+    return Wq, sc
+
+
+def quantize_expert_weights(weights: dict, stream=None) -> dict:
+    """Expert weights with the two base stacks replaced by FP8 codes + scales."""
+    out = {k: v for k, v in weights.items() if k not in ("W_gu", "W_d")}
+    out["Wq_gu"], out["s_gu"] = moe_quantize_fp8(weights["W_gu"], stream)
+    out["Wq_d"], out["s_d"] = moe_quantize_fp8(weights["W_d"], stream)
+    return out
+
+
+def _fp8_args(d: Dims, w: dict):
+    _need(w["Wq_gu"], "Wq_gu", torch.uint8, (d.E, d.H, 2 * d.I))
+    _need(w["s_gu"], "s_gu", torch.float32, (d.E, 2 * d.I))
+    _need(w["Wq_d"], "Wq_d", torch.uint8, (d.E, d.I, d.H))
+    _need(w["s_d"], "s_d", torch.float32, (d.E, d.H))
+    bf = torch.bfloat16
+    _need(w["A_gu"], "A_gu", bf, (d.E, d.r, d.H))
+    _need(w["B_gu"], "B_gu", bf, (d.E, d.r, 2 * d.I))
+    _need(w["A_d"], "A_d", bf, (d.E, d.r, d.I))
+    _need(w["B_d"], "B_d", bf, (d.E, d.r, d.H))
+    return [_ptr(w[n]) for n in ("Wq_gu", "s_gu", "A_gu", "B_gu", "Wq_d", "s_d", "A_d", "B_d")]
+
+
+def moe_lora_fwd_fp8(d: Dims, rt: Routing, x, w: dict, y, saved, workspace, dev_status, stream=None):
+    """Forward with FP8 base weights (`w` from quantize_expert_weights)."""
+    _need(x, "x", torch.bfloat16, (d.T, d.H))
+    dd, rr = d.c_struct(), rt.c_struct()
+    _check(load_library().moe_lora_fwd_fp8(ctypes.byref(dd), ctypes.byref(rr), _ptr(x), *_fp8_args(d, w), _ptr(y),
+                                           _ptr(saved), saved.numel(), _ptr(workspace), workspace.numel(),
+                                           _ptr(dev_status), _stream(stream)))
+    return y
+
+
+def moe_lora_bwd_fp8(d: Dims, rt: Routing, dy, w: dict, saved, dx, grads, workspace, dev_status, stream=None,
+                     d_topk_w=None):
+    """Backward with FP8 base weights; returns (dx, dA_gu, dB_gu, dA_d, dB_d)."""
+    _need(dy, "dy", torch.bfloat16, (d.T, d.H))
+    dA_gu, dB_gu, dA_d, dB_d = grads
+    dd, rr = d.c_struct(), rt.c_struct()
+    _check(load_library().moe_lora_bwd_fp8(ctypes.byref(dd), ctypes.byref(rr), _ptr(dy), *_fp8_args(d, w),
+                                           _ptr(saved), saved.numel(), _ptr(dx), _ptr(dA_gu), _ptr(dB_gu),
+                                           _ptr(dA_d), _ptr(dB_d), _ptr(d_topk_w), _ptr(workspace),
+                                           workspace.numel(), _ptr(dev_status), _stream(stream)))
+    return dx, dA_gu, dB_gu, dA_d, dB_d
+
+
 def moe_launch_count() -> int:
     """Launch operations the library has issued so far (host-side count)."""
     return int(load_library().moe_launch_count())
@@ -324,6 +383,7 @@ class MoELoRALayer:
     def __init__(self, d: Dims, weights: dict, device="cuda"):
         self.d = d
         self.w = weights
+        self.fp8 = "Wq_gu" in weights          # FP8 base weights (quantize_expert_weights)
         dev = torch.device(device)
         self.rt = Routing.empty(d.T, d.k, d.E, dev)
         self.route_ws = torch.empty(moe_route_workspace_size(d.T, d.k, d.E), dtype=torch.uint8, device=dev)
@@ -346,13 +406,19 @@ class MoELoRALayer:
                          dev_status=self.dev_status, stream=stream)
 
     def forward(self, x, stream=None):
+        if self.fp8:
+            return moe_lora_fwd_fp8(self.d, self.rt, x, self.w, self.y, self.saved, self.fwd_ws, self.dev_status,
+                                    stream)
         return moe_lora_fwd(self.d, self.rt, x, *self._wts(), y=self.y, saved=self.saved,
                             workspace=self.fwd_ws, dev_status=self.dev_status, stream=stream)[0]
 
     def backward(self, dy, stream=None, with_topk_grad=True):
+        dtw = self.d_topk_w if with_topk_grad else None
+        if self.fp8:
+            return moe_lora_bwd_fp8(self.d, self.rt, dy, self.w, self.saved, self.dx, self.grads, self.bwd_ws,
+                                    self.dev_status, stream, d_topk_w=dtw)
         return moe_lora_bwd(self.d, self.rt, dy, *self._wts(), self.saved, dx=self.dx, grads=self.grads,
-                            workspace=self.bwd_ws, dev_status=self.dev_status, stream=stream,
-                            d_topk_w=self.d_topk_w if with_topk_grad else None)
+                            workspace=self.bwd_ws, dev_status=self.dev_status, stream=stream, d_topk_w=dtw)
 
     def step(self, topk_idx, topk_w, x, dy, stream=None, with_topk_grad=True):
         self.route(topk_idx, topk_w, stream)

@@ -25,6 +25,7 @@
 #include "kernels.h"
 #include "tc_ptx.cuh"
 
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -36,21 +37,25 @@ namespace {
 
 constexpr int BM = 128, BK = 64;
 constexpr int kEpiWarps = 8;                 // 2 per TMEM lane quarter, each half the columns
+constexpr int kConvWarps = 8;                 // FP8 weights: dequantising warps (2 per scheduler)
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+__host__ __device__ constexpr int threads_of(bool q8) { return kThreads + (q8 ? 32 * kConvWarps : 0); }
 constexpr int kABytes = BM * BK * 2;         // 16 KB
 constexpr int kBoxMN = 64 * BK * 2;          // one 64-column MN-major box of B: 8 KB
 
 // Tile geometry for an output tile width BN (256 for the expert GEMMs; 16/32/64
 // for the rank-r projections).  PAIR: a 2-CTA cluster shares one 256 x 256 tile,
 // each CTA holding 128 rows of A and 128 columns of B per stage.
-template <int BN, bool PAIR = false>
+template <int BN, bool PAIR = false, bool Q8 = false>
 struct Geo {
     // narrow tiles (the HBM-bound projections) load KW 64-column boxes of A per stage so
     // that every row is fetched in 256-512 byte runs
     static constexpr int KW = BN >= 256 ? 1 : (BN <= 16 ? 4 : 2);
     static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK * 2 * KW;
-    static constexpr int kStageBytes = kABytes * KW + ((kBBytes + 1023) / 1024) * 1024;
-    static constexpr int kStages = PAIR ? 6 : (BN >= 256 ? 4 : (216 * 1024) / kStageBytes);
+    // FP8 weights: the TMA lands the e4m3 codes in a staging slot (half of B's bytes)
+    static constexpr int kQBytes = Q8 ? kBBytes / 2 : 0;
+    static constexpr int kStageBytes = kABytes * KW + ((kBBytes + 1023) / 1024) * 1024 + kQBytes;
+    static constexpr int kStages = Q8 ? (PAIR ? 5 : 3) : (PAIR ? 6 : (BN >= 256 ? 4 : (216 * 1024) / kStageBytes));
     static constexpr int kAccCols = BN;
     static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
@@ -104,10 +109,11 @@ __device__ __forceinline__ int b_col(int j, int nt, int ncols) {
     return nt * BN + j * 64;
 }
 
-template <int EPI, bool B_MN, int BN, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams P) {
+template <int EPI, bool B_MN, int BN, bool PAIR, bool Q8>
+__global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams P) {
     constexpr bool PAIRED = (EPI == EPI_SWIGLU);
-    using G = Geo<BN, PAIR>;
+    using G = Geo<BN, PAIR, Q8>;
+    static_assert(!Q8 || BN == 256, "FP8 weights are for the expert GEMMs");
     constexpr int kStages = G::kStages;
     constexpr int kStageBytes = G::kStageBytes;
     constexpr int kAccCols = G::kAccCols;
@@ -121,7 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
     uint64_t* empty_bar = full_bar + kStages;
     uint64_t* tfull_bar = empty_bar + kStages;
     uint64_t* tempty_bar = tfull_bar + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty_bar + 2);
+    uint64_t* staged_bar = tempty_bar + 2;          // FP8 codes landed in the staging slot
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(staged_bar + kStages);
     volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int32_t* s_off = reinterpret_cast<int32_t*>(tmem_slot + 4);
     const GroupedGemm& g = P.g;
@@ -139,8 +146,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            tc::mbar_init(tc::smem_u32(&full_bar[s]), 1);
+            // with FP8 weights the B half of a stage is complete when the converter warps
+            // (of both CTAs of a pair) have arrived
+            tc::mbar_init(tc::smem_u32(&full_bar[s]), Q8 ? 1 + kConvWarps * (PAIR ? 2 : 1) : 1);
             tc::mbar_init(tc::smem_u32(&empty_bar[s]), 1);
+            tc::mbar_init(tc::smem_u32(&staged_bar[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(tc::smem_u32(&tfull_bar[a]), 1);
@@ -214,7 +224,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                     if constexpr (PAIR) {
                         // both CTAs' loads complete on the leader's full barrier
                         const uint32_t fb = tc::mapa(fb_local, 0);
-                        if (kb < P.num_kb) {
+                        if (kb < P.num_kb && Q8) {
+                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * kABytes);
+                            tc::tma_load_2d_pair(sa, &P.tm_a, fb, kb * BK, m0);
+                            const uint32_t sq = sb + G::kBBytes;
+                            const uint32_t qb = tc::smem_u32(&staged_bar[stage]);
+                            tc::mbar_arrive_expect_tx(qb, G::kQBytes);
+                            if (B_MN) {
+#pragma unroll
+                                for (int jj = 0; jj < 2; ++jj)
+                                    tc::tma_load_3d(sq + jj * (kBoxMN / 2), &P.tm_b, qb,
+                                                    b_col<PAIRED, BN>(2 * (int)rank + jj, nt, g.Ncols), kb * BK, e);
+                            } else {
+                                tc::tma_load_3d(sq, &P.tm_b, qb, kb * BK, nt * BN + (int)rank * (BN / 2), e);
+                            }
+                        } else if (kb < P.num_kb) {
                             if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * (kABytes + G::kBBytes));
                             tc::tma_load_2d_pair(sa, &P.tm_a, fb, kb * BK, m0);
                             if (B_MN) {
@@ -245,7 +269,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                         }
                     } else {
                         const uint32_t fb = fb_local;
-                        if (kb < P.num_kb) {
+                        if (kb < P.num_kb && Q8) {
+                            tc::mbar_arrive_expect_tx(fb, kABytes);
+                            tc::tma_load_2d(sa, &P.tm_a, fb, kb * BK, m0);
+                            const uint32_t sq = sb + G::kBBytes;
+                            const uint32_t qb = tc::smem_u32(&staged_bar[stage]);
+                            tc::mbar_arrive_expect_tx(qb, G::kQBytes);
+                            if (B_MN) {
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    tc::tma_load_3d(sq + j * (kBoxMN / 2), &P.tm_b, qb, b_col<PAIRED, BN>(j, nt, g.Ncols),
+                                                    kb * BK, e);
+                            } else {
+                                tc::tma_load_3d(sq, &P.tm_b, qb, kb * BK, nt * BN, e);
+                            }
+                        } else if (kb < P.num_kb) {
                             tc::mbar_arrive_expect_tx(fb, kABytes + G::kBBytes);
                             tc::tma_load_2d(sa, &P.tm_a, fb, kb * BK, m0);
                             if (B_MN) {
@@ -338,6 +376,94 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
                 if (!ok) break;
                 if constexpr (PAIR) tc::mma_commit_pair(tc::smem_u32(&tfull_bar[acc]), 0x3);
                 else tc::mma_commit(tc::smem_u32(&tfull_bar[acc]));
+            }
+        }
+    } else if (Q8 && warp >= 2 + kEpiWarps) {
+        // ------------------------------------------------------------ FP8 dequantisers
+        // e4m3 codes (staging slot, plain row-major boxes of 64 bytes per row) -> bf16 in
+        // the 128-byte-swizzled layout TMA would have written: row r, 16-byte chunk cc of
+        // 8 elements at r * 128 + ((cc ^ (r & 7)) << 4); each value times its column's
+        // power-of-two scale (exact).
+        if constexpr (Q8) {
+            constexpr int kCT = 32 * kConvWarps;                // converter threads
+            constexpr int kUnits = G::kQBytes / 8;              // 8 codes per unit
+            constexpr int kIters = kUnits / kCT;
+            constexpr int kBoxes = B_MN ? (PAIR ? 2 : 4) : 1;
+            static_assert(kUnits % kCT == 0 && 512 % kCT == 0, "units per stage must split evenly");
+            const int ct = threadIdx.x - 32 * (2 + kEpiWarps);
+            const int cc = ct & 7;                              // the thread's 16-byte chunk of a row
+            const uint32_t full_leader0 = PAIR ? tc::mapa(tc::smem_u32(&full_bar[0]), 0) : 0u;
+            int stage = 0;
+            uint32_t sbits = 0;                                 // per-stage parity of staged_bar
+            bool ok = true;
+            float sv[kBoxes][8];                                // column scales of this thread's chunks
+            for (int t = tile0; t < total_tiles && ok && !*s_abort; t += tile_step) {
+                int e, mt, nt;
+                decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
+                const float* se = g.b_scale + (int64_t)e * g.ldb;
+                if constexpr (B_MN) {
+                    // MN-major: a chunk's scales depend on its columns only, fixed for the tile
+#pragma unroll
+                    for (int j = 0; j < kBoxes; ++j) {
+                        const int col = b_col<PAIRED, BN>((PAIR ? 2 * (int)rank : 0) + j, nt, g.Ncols) + cc * 8;
+                        const bool in = col < g.ldb;
+                        const float4 a = in ? __ldg(reinterpret_cast<const float4*>(se + col)) : make_float4(0, 0, 0, 0);
+                        const float4 b = in ? __ldg(reinterpret_cast<const float4*>(se + col) + 1) : make_float4(0, 0, 0, 0);
+                        sv[j][0] = a.x; sv[j][1] = a.y; sv[j][2] = a.z; sv[j][3] = a.w;
+                        sv[j][4] = b.x; sv[j][5] = b.y; sv[j][6] = b.z; sv[j][7] = b.w;
+                    }
+                }
+                const int nkb = P.num_kb + (P.lora_k16 ? 1 : 0);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (kb < P.num_kb) {
+                        if constexpr (!B_MN) {
+                            // K-major: the scales follow k, fixed for the stage
+                            const float4 a = __ldg(reinterpret_cast<const float4*>(se + kb * BK + cc * 8));
+                            const float4 b = __ldg(reinterpret_cast<const float4*>(se + kb * BK + cc * 8) + 1);
+                            sv[0][0] = a.x; sv[0][1] = a.y; sv[0][2] = a.z; sv[0][3] = a.w;
+                            sv[0][4] = b.x; sv[0][5] = b.y; sv[0][6] = b.z; sv[0][7] = b.w;
+                        }
+                        const bool got = tc::mbar_wait(tc::smem_u32(&staged_bar[stage]), (sbits >> stage) & 1u);
+                        if (!__all_sync(0xffffffffu, got)) {
+                            if (lane == 0) set_timeout(g, s_abort);
+                            ok = false;
+                            break;
+                        }
+                        sbits ^= 1u << stage;
+                        uint8_t* bt = smem + stage * kStageBytes + kABytes;
+                        const uint8_t* qt = bt + G::kBBytes;
+#pragma unroll
+                        for (int i = 0; i < kIters; ++i) {
+                            const int u = ct + kCT * i;
+                            // 64-column box (MN-major); ct < kCT and kCT divides 512, so it is (i * kCT) / 512
+                            const int j = B_MN ? (i * kCT) / 512 : 0;
+                            const int r = B_MN ? ((u >> 3) & 63) : (u >> 3);
+                            const uint32_t src = j * (kBoxMN / 2) + r * 64 + cc * 8;
+                            const uint32_t dst = j * kBoxMN + r * 128 + ((cc ^ (r & 7)) << 4);
+                            const uint2 q = *reinterpret_cast<const uint2*>(qt + src);
+                            const uint32_t w[2] = {q.x, q.y};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const uint16_t pr = (uint16_t)(w[h >> 1] >> ((h & 1) * 16));
+                                uint32_t f16x2;
+                                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pr));
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&f16x2));
+                                const __nv_bfloat162 bv =
+                                    __floats2bfloat162_rn(f.x * sv[j][2 * h], f.y * sv[j][2 * h + 1]);
+                                o[h] = *reinterpret_cast<const uint32_t*>(&bv);
+                            }
+                            *reinterpret_cast<uint4*>(bt + dst) = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (PAIR) tc::mbar_arrive_cluster(full_leader0 + stage * (uint32_t)sizeof(uint64_t));
+                        else tc::mbar_arrive(tc::smem_u32(&full_bar[stage]));
+                    }
+                    if (++stage == kStages) stage = 0;
+                }
             }
         }
     } else {
@@ -519,7 +645,8 @@ CUtensorMapSwizzle swizzle_for_bytes(int inner_bytes) {
 }
 
 bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-            const uint32_t* box, CUtensorMapSwizzle sw) {
+            const uint32_t* box, CUtensorMapSwizzle sw,
+            CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     cuuint64_t gd[3], gs[2];
@@ -529,7 +656,7 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, co
         bx[i] = box[i];
     }
     for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bx, es,
+    return fn(m, dt, rank, const_cast<void*>(base), gd, gs, bx, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -549,14 +676,15 @@ int sm_count() {
 
 // One CTA per SM (grid = min(#SMs, tiles)); SM pairs: as many 2-CTA clusters as can be
 // resident at once (so that no pair waits for another to finish), at most one per tile.
-template <int EPI, bool B_MN, int BN, bool PAIR>
+template <int EPI, bool B_MN, int BN, bool PAIR, bool Q8 = false>
 cudaError_t launch_tc(const TcParams& P, int64_t max_tiles, size_t smem, cudaStream_t s) {
-    auto k = grouped_gemm_tc_kernel<EPI, B_MN, BN, PAIR>;
+    auto k = grouped_gemm_tc_kernel<EPI, B_MN, BN, PAIR, Q8>;
+    constexpr int kThr = threads_of(Q8);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if constexpr (!PAIR) {
         const int grid = (int)std::min<int64_t>(sm_count(), max_tiles);
-        k<<<grid, kThreads, smem, s>>>(P);
+        k<<<grid, kThr, smem, s>>>(P);
         return cudaGetLastError();
     } else {
         cudaLaunchConfig_t cfg = {};
@@ -565,7 +693,7 @@ cudaError_t launch_tc(const TcParams& P, int64_t max_tiles, size_t smem, cudaStr
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(kThr, 1, 1);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = s;
         cfg.attrs = attr;
@@ -604,7 +732,12 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
     P.g = g;
     P.num_kb = g.K / BK;
     const bool paired = g.epi == EPI_SWIGLU;
-    const bool pair = allow_pairs && !proj && use_sm_pairs(g);
+    const bool q8 = g.b_scale != nullptr;
+    // FP8 weights always run on SM pairs: each CTA dequantises half of the B tile
+    const bool pair = allow_pairs && !proj && (q8 || use_sm_pairs(g));
+    if (q8 && (proj || g.ldb % 64 != 0)) return cudaErrorInvalidValue;
+    // FP8 kernels exist for the layer's four GEMMs: MN-major B forward, K-major B backward
+    if (q8 && g.b_mn_major != (g.epi == EPI_SWIGLU || g.epi == EPI_BF16)) return cudaErrorInvalidValue;
     P.n_tiles = proj ? 1 : (paired ? (g.Ncols + 127) / 128 : (g.Ncols + 255) / 256);
     // A: [N, K]
     {
@@ -620,8 +753,15 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
         const uint64_t st[2] = {(uint64_t)g.ldb * 2, (uint64_t)g.b_expert_stride * 2};
         const uint32_t box_mn[3] = {64, BK, 1};
         const uint32_t box_k[3] = {BK, (uint32_t)(pair ? BN / 2 : BN), 1};
-        if (!encode(&P.tm_b, g.B, 3, dims, st, g.b_mn_major ? box_mn : box_k, CU_TENSOR_MAP_SWIZZLE_128B))
+        if (q8) {
+            // e4m3 codes, one byte each, landed unswizzled in the staging slot
+            const uint64_t st8[2] = {(uint64_t)g.ldb, (uint64_t)g.b_expert_stride};
+            if (!encode(&P.tm_b, g.B, 3, dims, st8, g.b_mn_major ? box_mn : box_k, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_DATA_TYPE_UINT8))
+                return cudaErrorInvalidValue;
+        } else if (!encode(&P.tm_b, g.B, 3, dims, st, g.b_mn_major ? box_mn : box_k, CU_TENSOR_MAP_SWIZZLE_128B)) {
             return cudaErrorInvalidValue;
+        }
     }
     if (g.A2 != nullptr && g.r > 0) {
         const int rp = g.rp;
@@ -648,6 +788,27 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
             case 16: return launch_tc<EPI_PROJ, false, 16, false>(P, max_tiles, Geo<16>::kSmem + offs_bytes, s);
             case 32: return launch_tc<EPI_PROJ, false, 32, false>(P, max_tiles, Geo<32>::kSmem + offs_bytes, s);
             default: return launch_tc<EPI_PROJ, false, 64, false>(P, max_tiles, Geo<64>::kSmem + offs_bytes, s);
+        }
+    }
+    if (q8) {
+        // FP8 weights: the forward GEMMs take an MN-major B, the backward ones a K-major B
+        cudaError_t e;
+        if (pair) {
+            const size_t smem = Geo<256, true, true>::kSmem + offs_bytes;
+            switch (g.epi) {
+                case EPI_SWIGLU: e = launch_tc<EPI_SWIGLU, true, 256, true, true>(P, max_tiles, smem, s); break;
+                case EPI_BF16: e = launch_tc<EPI_BF16, true, 256, true, true>(P, max_tiles, smem, s); break;
+                case EPI_DSWIGLU: e = launch_tc<EPI_DSWIGLU, false, 256, true, true>(P, max_tiles, smem, s); break;
+                default: e = launch_tc<EPI_PLAIN_F32, false, 256, true, true>(P, max_tiles, smem, s);
+            }
+            return e;
+        }
+        const size_t smem = Geo<256, false, true>::kSmem + offs_bytes;
+        switch (g.epi) {
+            case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256, false, true>(P, max_tiles, smem, s);
+            case EPI_BF16: return launch_tc<EPI_BF16, true, 256, false, true>(P, max_tiles, smem, s);
+            case EPI_DSWIGLU: return launch_tc<EPI_DSWIGLU, false, 256, false, true>(P, max_tiles, smem, s);
+            default: return launch_tc<EPI_PLAIN_F32, false, 256, false, true>(P, max_tiles, smem, s);
         }
     }
     if (pair) {

@@ -25,6 +25,11 @@ cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, cons
 cudaError_t launch_combine(const void* src, bool src_f32, const float* w_sorted, const int32_t* inv_perm, int64_t T,
                            int k, int H, void* out, cudaStream_t s);
 
+// ---- FP8 expert weights (quant.cu)
+// scale[m, c] = 2^ceil(log2(amax_r |W[m, r, c]| / 448)), Wq[m, r, c] = e4m3_rn(W[m, r, c] / scale[m, c])
+cudaError_t launch_quantize_fp8(const void* W, int64_t n_mat, int64_t rows, int cols, void* Wq, float* scale,
+                                cudaStream_t s);
+
 // ---- router (router.cu)
 cudaError_t launch_router_topk(const float* logits, int64_t T, int E, int k, int32_t* topk_idx, float* topk_w,
                                cudaStream_t s);
@@ -64,6 +69,7 @@ struct GroupedGemm {
     const void* A;        // [N, K] bf16, K contiguous
     const void* B;        // bf16 expert stack
     bool b_mn_major;      // true: B_e(c, n) = B[e][c][n] (row length ldb); false: B[e][n][c]
+    const float* b_scale; // non-null: B holds e4m3 codes, value = code * b_scale[e * ldb + column of B[e]]
     int ldb;              // elements per row of B[e]
     int64_t b_expert_stride;  // elements between experts
     const void* A2;       // [N, RP] bf16 (LoRA rank activations, pre-scaled by s), or null

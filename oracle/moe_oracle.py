@@ -285,3 +285,34 @@ def lora_dtopk_w(dy, x, topk_idx, W_gu, A_gu, B_gu, W_d, A_d, B_d, scale, token_
         O = swiglu(x[t_idx] @ M_gu, I) @ M_d
         dw[t_idx, j_idx] = (dy[t_idx] * O).sum(axis=1)
     return dw
+
+
+# --------------------------------------------------------------------------
+# FP8 (e4m3) expert base weights
+# --------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def quantize_fp8(W):
+    """Per matrix and column: scale = 2^ceil(log2(amax / 448)) (1 for an all-zero
+    column), codes = e4m3 round-to-nearest-even of W / scale.  W: [..., rows, cols].
+    Returns (codes uint8 in the e4m3 bit layout, scales float32 [..., cols]).
+
+    With power-of-two scales, W / scale is exact and every dequantised value
+    code * scale is exactly representable in bf16, so the quantised base weights
+    are a set of bf16 weights."""
+    import torch
+    w = _f64(W)
+    amax = np.abs(w).max(axis=-2)
+    with np.errstate(divide="ignore"):
+        e = np.ceil(np.log2(amax / E4M3_MAX))
+    scale = np.where(amax > 0, np.exp2(e), 1.0)
+    q = torch.tensor(w / scale[..., None, :], dtype=torch.float64).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).numpy(), scale.astype(np.float32)
+
+
+def dequantize_fp8(codes, scales):
+    """Dequantised weights (float64): e4m3 value of each code times its column scale."""
+    import torch
+    c = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return c * np.asarray(scales, np.float64)[..., None, :]

@@ -118,3 +118,27 @@ def test_binding_fails_loudly_without_library(tmp_path):
             b.load_library(str(tmp_path / "missing.so"))
     finally:
         b._lib = saved
+
+
+def _header_arity():
+    """Number of parameters of every MOE_API function in include/ (void -> 0)."""
+    out = {}
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(([^)]*)\)\s*;", text):
+            params = [p for p in m.group(2).split(",") if p.strip()]
+            out[m.group(1)] = 0 if params == ["void"] or [p.strip() for p in params] == ["void"] else len(params)
+    return out
+
+
+def test_binding_argtypes_match_header_arity(lib):
+    from moe_expert_dispatch_stable_gb300 import binding as b
+    arity = _header_arity()
+    assert len(arity) >= 18
+    for name in b.EXPORTED:                     # every function the binding wraps
+        argtypes = getattr(lib, name).argtypes
+        n = arity[name]
+        if argtypes is None:
+            assert n == 0, f"{name}: no argtypes set but the header declares {n} parameters"
+        else:
+            assert len(argtypes) == n, f"{name}: binding declares {len(argtypes)} arguments, header {n}"

@@ -1,0 +1,100 @@
+"""FP8 (e4m3) expert base weights: the device quantiser against the oracle's (bit
+for bit), and the FP8 layer against the bf16 layer run on the dequantised
+weights (bit for bit: the tensor cores see the same bf16 values), plus the fp64
+oracle on the dequantised weights (tolerance)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from oracle import moe_oracle as orc
+from tests.gpu_common import WEIGHT_NAMES, assert_close, make_case, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def test_quantizer_bit_exact_against_oracle():
+    import moe_expert_dispatch_stable_gb300 as moe
+    for name in ("tiny", "gptoss20b"):
+        cfg = mi.CONFIGS[name]
+        W = mi.make_tensor(cfg, "W_d", 0, "cuda" if name != "tiny" else "cpu").cuda()
+        W[0, :, 3] = 0                                  # an all-zero column
+        W[-1, 5, 7] = 300.0                             # a large outlier
+        Wq, sc = moe.moe_quantize_fp8(W)
+        torch.cuda.synchronize()
+        for e in (0, W.shape[0] - 1):
+            codes, scales = orc.quantize_fp8(W[e].cpu())
+            assert np.array_equal(Wq[e].cpu().numpy(), codes)
+            assert np.array_equal(sc[e].cpu().numpy(), scales)
+
+
+CASES = {
+    "ragged_single": mi.MoEConfig("ragged", T=700, H=256, E=6, k=2, I=320, r=16, alpha=32),
+    "pairs_ragged": mi.MoEConfig("pairs", T=1000, H=256, E=4, k=2, I=320, r=16, alpha=32),
+    "tiny_r8": mi.CONFIGS["tiny"],
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fp8_layer_is_bit_identical_to_bf16_on_dequantized_weights(name):
+    import moe_expert_dispatch_stable_gb300 as moe
+    cfg = CASES[name]
+    idx, w, ts = make_case(cfg, seed=2)
+    wq = moe.quantize_expert_weights(ts)
+    # the oracle's quantiser on the same bf16 weights gives the same codes and scales, and
+    # its dequantised weights are the bf16 reference the FP8 layer must reproduce
+    deq = {}
+    for name_w, qn, sn in (("W_gu", "Wq_gu", "s_gu"), ("W_d", "Wq_d", "s_d")):
+        codes, scales = orc.quantize_fp8(ts[name_w].cpu())
+        assert np.array_equal(wq[qn].cpu().numpy(), codes) and np.array_equal(wq[sn].cpu().numpy(), scales)
+        deq[name_w] = torch.tensor(orc.dequantize_fp8(codes, scales)).to(torch.bfloat16).cuda()
+    bf_w = {**ts, **deq}
+    d = moe.Dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r, cfg.scale)
+    ti, tw = torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()
+    ref = moe.MoELoRALayer(d, bf_w)
+    q8 = moe.MoELoRALayer(d, wq)
+    g_ref = ref.step(ti, tw, ts["x"], ts["dy"])
+    g_q8 = q8.step(ti, tw, ts["x"], ts["dy"])
+    torch.cuda.synchronize()
+    assert int(q8.dev_status.item()) == 0
+    assert torch.equal(q8.y, ref.y)
+    for a, b in zip(g_q8, g_ref):
+        assert torch.equal(a, b)
+    assert torch.equal(q8.d_topk_w, ref.d_topk_w)
+    # and against the fp64 oracle with the dequantised weights
+    c = {k: v.cpu() for k, v in {**ts, **deq}.items()}
+    wts = [c[n] for n in WEIGHT_NAMES]
+    assert_close("y", to64(q8.y), orc.lora_fwd(c["x"], idx, w, *wts, cfg.scale))
+
+
+def test_fp8_full_size_deepseek_shape_bit_identical():
+    """The HBM-bound workload FP8 weights are for: 256 experts, H = 7168, 128 rows per expert."""
+    import moe_expert_dispatch_stable_gb300 as moe
+    cfg = mi.CONFIGS["dsv3"]
+    idx, w, ts = make_case(cfg, seed=0)
+    wq = moe.quantize_expert_weights(ts)
+    torch.cuda.synchronize()
+    d = moe.Dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r, cfg.scale)
+    ti, tw = torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()
+    q8 = moe.MoELoRALayer(d, wq)
+    g_q8 = [g.clone() for g in q8.step(ti, tw, ts["x"], ts["dy"])]
+    y_q8 = q8.y.clone()
+    del q8
+    # dequantise on the device with torch (codes -> e4m3 -> float * scale -> bf16, exact)
+    bf = dict(ts)
+    for name, qn, sn in (("W_gu", "Wq_gu", "s_gu"), ("W_d", "Wq_d", "s_d")):
+        bf[name] = (wq[qn].view(torch.float8_e4m3fn).float() * wq[sn][:, None, :]).to(torch.bfloat16)
+    del wq
+    ref = moe.MoELoRALayer(d, bf)
+    g_ref = ref.step(ti, tw, ts["x"], ts["dy"])
+    torch.cuda.synchronize()
+    assert torch.equal(y_q8, ref.y)
+    for a, b in zip(g_q8, g_ref):
+        assert torch.equal(a, b)
