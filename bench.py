@@ -266,10 +266,11 @@ def fp8_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, steps: int, flush) -> 
     kt = moe.moe_timing_read()
     assert int(q8.dev_status.item()) == 0
     gemm_ms = sum(kt[n][0] for n in GEMM_KERNELS if n in kt) / steps
+    kernels = {n: round(v[0] / steps, 4) for n, v in kt.items() if n in GEMM_KERNELS}
     wbytes = sum(t.numel() * t.element_size() for n, t in wq.items() if n.startswith(("Wq", "s_")))
     del q8, wq
     return {"ms_per_step": ms / steps, "tokens_per_s": cfg.T * steps / (ms / 1e3), "gemm_ms_per_step": gemm_ms,
-            "base_weight_bytes": wbytes, "steps": steps}
+            "gemm_kernels_ms_per_step": kernels, "base_weight_bytes": wbytes, "steps": steps}
 
 
 # ----------------------------------------------------------------------------- offload

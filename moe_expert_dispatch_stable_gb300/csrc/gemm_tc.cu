@@ -38,6 +38,13 @@ namespace {
 constexpr int BM = 128, BK = 64;
 constexpr int kEpiWarps = 8;                 // 2 per TMEM lane quarter, each half the columns
 constexpr int kConvWarps = 8;                 // FP8 weights: dequantising warps (2 per scheduler)
+// the converter warps form groups; group g owns the stages s with s % kConvGroups == g,
+// so that several stages are dequantised at once and one group's proxy fence overlaps
+// another's work.  Owning whole stages keeps every mbarrier phase wait of a group within
+// one phase of the barrier (a stage cannot move on before its owner has arrived).
+constexpr int kConvGroups = 2;
+constexpr int kSignalBytes = 4;                // FP8 pairs: the peer's "B half converted" store
+static_assert(kConvWarps % kConvGroups == 0 && (kConvGroups & (kConvGroups - 1)) == 0, "converter groups");
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 __host__ __device__ constexpr int threads_of(bool q8) { return kThreads + (q8 ? 32 * kConvWarps : 0); }
 constexpr int kABytes = BM * BK * 2;         // 16 KB
@@ -52,10 +59,11 @@ struct Geo {
     // that every row is fetched in 256-512 byte runs
     static constexpr int KW = BN >= 256 ? 1 : (BN <= 16 ? 4 : 2);
     static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK * 2 * KW;
-    // FP8 weights: the TMA lands the e4m3 codes in a staging slot (half of B's bytes)
+    // FP8 weights: the TMA lands the e4m3 codes in the upper half of the B slot and the
+    // converter warps expand them in place, so a stage is as large as with bf16 weights
     static constexpr int kQBytes = Q8 ? kBBytes / 2 : 0;
-    static constexpr int kStageBytes = kABytes * KW + ((kBBytes + 1023) / 1024) * 1024 + kQBytes;
-    static constexpr int kStages = Q8 ? (PAIR ? 5 : 3) : (PAIR ? 6 : (BN >= 256 ? 4 : (216 * 1024) / kStageBytes));
+    static constexpr int kStageBytes = kABytes * KW + ((kBBytes + 1023) / 1024) * 1024;
+    static constexpr int kStages = PAIR ? 6 : (BN >= 256 ? 4 : (216 * 1024) / kStageBytes);
     static constexpr int kAccCols = BN;
     static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
@@ -130,6 +138,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
     uint64_t* staged_bar = tempty_bar + 2;          // FP8 codes landed in the staging slot
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(staged_bar + kStages);
     volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint32_t* sig_slot = tmem_slot + 2;             // FP8 pairs: target of the peer's stage signals
     int32_t* s_off = reinterpret_cast<int32_t*>(tmem_slot + 4);
     const GroupedGemm& g = P.g;
     const int E = g.E;
@@ -146,9 +155,10 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            // with FP8 weights the B half of a stage is complete when the converter warps
-            // (of both CTAs of a pair) have arrived
-            tc::mbar_init(tc::smem_u32(&full_bar[s]), Q8 ? 1 + kConvWarps * (PAIR ? 2 : 1) : 1);
+            // with FP8 weights the B half of a stage is complete when the converter group
+            // that owns the stage has arrived (and, in a pair, the peer's group has completed
+            // kSignalBytes transaction bytes on it)
+            tc::mbar_init(tc::smem_u32(&full_bar[s]), Q8 ? 2 : 1);
             tc::mbar_init(tc::smem_u32(&empty_bar[s]), 1);
             tc::mbar_init(tc::smem_u32(&staged_bar[s]), 1);
         }
@@ -225,9 +235,9 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                         // both CTAs' loads complete on the leader's full barrier
                         const uint32_t fb = tc::mapa(fb_local, 0);
                         if (kb < P.num_kb && Q8) {
-                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * kABytes);
+                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * kABytes + kSignalBytes);
                             tc::tma_load_2d_pair(sa, &P.tm_a, fb, kb * BK, m0);
-                            const uint32_t sq = sb + G::kBBytes;
+                            const uint32_t sq = sb + G::kQBytes;
                             const uint32_t qb = tc::smem_u32(&staged_bar[stage]);
                             tc::mbar_arrive_expect_tx(qb, G::kQBytes);
                             if (B_MN) {
@@ -272,7 +282,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                         if (kb < P.num_kb && Q8) {
                             tc::mbar_arrive_expect_tx(fb, kABytes);
                             tc::tma_load_2d(sa, &P.tm_a, fb, kb * BK, m0);
-                            const uint32_t sq = sb + G::kBBytes;
+                            const uint32_t sq = sb + G::kQBytes;
                             const uint32_t qb = tc::smem_u32(&staged_bar[stage]);
                             tc::mbar_arrive_expect_tx(qb, G::kQBytes);
                             if (B_MN) {
@@ -330,7 +340,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : P.num_kb + (P.lora_k16 ? 1 : 0);
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!tc::mbar_wait(tc::smem_u32(&full_bar[stage]), phase)) {
+                    // FP8 pairs: the peer's converted half is published by a cluster-scope release
+                    if (!tc::mbar_wait<Q8 && PAIR>(tc::smem_u32(&full_bar[stage]), phase)) {
                         set_timeout(g, s_abort);
                         ok = false;
                         break;
@@ -385,19 +396,25 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
         // 8 elements at r * 128 + ((cc ^ (r & 7)) << 4); each value times its column's
         // power-of-two scale (exact).
         if constexpr (Q8) {
-            constexpr int kCT = 32 * kConvWarps;                // converter threads
-            constexpr int kUnits = G::kQBytes / 8;              // 8 codes per unit
-            constexpr int kIters = kUnits / kCT;
+            constexpr int kGT = 32 * (kConvWarps / kConvGroups);    // threads of one group
+            constexpr int kUnits = G::kQBytes / 8;                  // 8 codes per unit
+            constexpr int kIters = kUnits / kGT;
             constexpr int kBoxes = B_MN ? (PAIR ? 2 : 4) : 1;
-            static_assert(kUnits % kCT == 0 && 512 % kCT == 0, "units per stage must split evenly");
+            static_assert(kUnits % kGT == 0 && 512 % kGT == 0, "units per stage must split evenly");
+            static_assert(kStages % kConvGroups == 0, "every group owns whole stages");
             const int ct = threadIdx.x - 32 * (2 + kEpiWarps);
-            const int cc = ct & 7;                              // the thread's 16-byte chunk of a row
+            const int grp = ct / kGT;
+            const int gt = ct % kGT;
+            const int cc = gt & 7;                                  // the thread's 16-byte chunk of a row
             const uint32_t full_leader0 = PAIR ? tc::mapa(tc::smem_u32(&full_bar[0]), 0) : 0u;
+            const uint32_t sig_leader = PAIR ? tc::mapa(tc::smem_u32(sig_slot), 0) : 0u;
             int stage = 0;
-            uint32_t sbits = 0;                                 // per-stage parity of staged_bar
+            uint32_t sbits = 0;                                     // per-stage parity of staged_bar
             bool ok = true;
-            float sv[kBoxes][8];                                // column scales of this thread's chunks
-            for (int t = tile0; t < total_tiles && ok && !*s_abort; t += tile_step) {
+            float sv[kBoxes][8];                                    // column scales of this thread's chunks
+            // the warps of a group leave together: every exit decision is a group-wide vote
+            // (an abort elsewhere stops the producer, and the next staged wait then runs out)
+            for (int t = tile0; t < total_tiles && ok; t += tile_step) {
                 int e, mt, nt;
                 decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
                 const float* se = g.b_scale + (int64_t)e * g.ldb;
@@ -415,7 +432,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 }
                 const int nkb = P.num_kb + (P.lora_k16 ? 1 : 0);
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (kb < P.num_kb) {
+                    const bool mine = (stage % kConvGroups) == grp;
+                    if (mine && kb < P.num_kb) {
                         if constexpr (!B_MN) {
                             // K-major: the scales follow k, fixed for the stage
                             const float4 a = __ldg(reinterpret_cast<const float4*>(se + kb * BK + cc * 8));
@@ -424,24 +442,30 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                             sv[0][4] = b.x; sv[0][5] = b.y; sv[0][6] = b.z; sv[0][7] = b.w;
                         }
                         const bool got = tc::mbar_wait(tc::smem_u32(&staged_bar[stage]), (sbits >> stage) & 1u);
-                        if (!__all_sync(0xffffffffu, got)) {
-                            if (lane == 0) set_timeout(g, s_abort);
+                        if (!tc::named_bar_and(1 + grp, kGT, got && !*s_abort)) {
+                            if (gt == 0) set_timeout(g, s_abort);
                             ok = false;
                             break;
                         }
                         sbits ^= 1u << stage;
                         uint8_t* bt = smem + stage * kStageBytes + kABytes;
-                        const uint8_t* qt = bt + G::kBBytes;
+                        const uint8_t* qt = bt + G::kQBytes;
+                        // all of the group's codes are read before any bf16 value overwrites them
+                        uint2 q[kIters];
 #pragma unroll
                         for (int i = 0; i < kIters; ++i) {
-                            const int u = ct + kCT * i;
-                            // 64-column box (MN-major); ct < kCT and kCT divides 512, so it is (i * kCT) / 512
-                            const int j = B_MN ? (i * kCT) / 512 : 0;
+                            const int u = gt + kGT * i;
+                            const int j = B_MN ? (i * kGT) / 512 : 0;   // gt < kGT and kGT divides 512
                             const int r = B_MN ? ((u >> 3) & 63) : (u >> 3);
-                            const uint32_t src = j * (kBoxMN / 2) + r * 64 + cc * 8;
-                            const uint32_t dst = j * kBoxMN + r * 128 + ((cc ^ (r & 7)) << 4);
-                            const uint2 q = *reinterpret_cast<const uint2*>(qt + src);
-                            const uint32_t w[2] = {q.x, q.y};
+                            q[i] = *reinterpret_cast<const uint2*>(qt + j * (kBoxMN / 2) + r * 64 + cc * 8);
+                        }
+                        tc::named_bar_sync(1 + grp, kGT);
+#pragma unroll
+                        for (int i = 0; i < kIters; ++i) {
+                            const int u = gt + kGT * i;
+                            const int j = B_MN ? (i * kGT) / 512 : 0;
+                            const int r = B_MN ? ((u >> 3) & 63) : (u >> 3);
+                            const uint32_t w[2] = {q[i].x, q[i].y};
                             uint32_t o[4];
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {
@@ -453,14 +477,22 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                                     __floats2bfloat162_rn(f.x * sv[j][2 * h], f.y * sv[j][2 * h + 1]);
                                 o[h] = *reinterpret_cast<const uint32_t*>(&bv);
                             }
-                            *reinterpret_cast<uint4*>(bt + dst) = make_uint4(o[0], o[1], o[2], o[3]);
+                            *reinterpret_cast<uint4*>(bt + j * kBoxMN + r * 128 + ((cc ^ (r & 7)) << 4)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
                         }
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     }
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (PAIR) tc::mbar_arrive_cluster(full_leader0 + stage * (uint32_t)sizeof(uint64_t));
-                        else tc::mbar_arrive(tc::smem_u32(&full_bar[stage]));
+                    if (mine) {
+                        // one signal per group and stage, after every thread's writes and proxy fence:
+                        // a CTA-scope arrive on this CTA's full barrier, or from the peer of a pair an
+                        // asynchronous store that completes transaction bytes on the leader's (a
+                        // cluster-scope arrive would hold the thread for a microsecond)
+                        tc::named_bar_sync(1 + grp, kGT);
+                        if (gt == 0) {
+                            if (!PAIR || rank == 0) tc::mbar_arrive(tc::smem_u32(&full_bar[stage]));
+                            else if (kb < P.num_kb)
+                                tc::st_async_signal(sig_leader, 1u, full_leader0 + stage * (uint32_t)sizeof(uint64_t));
+                        }
                     }
                     if (++stage == kStages) stage = 0;
                 }
@@ -615,6 +647,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             }
         }
     }
+    // after an abort, a peer's last stage signal may still be in flight towards the leader
+    if (Q8 && PAIR && *s_abort) __nanosleep(20000);
     tc::fence_before_sync();
     __syncthreads();
     if constexpr (PAIR) tc::cluster_sync();    // the leader's MMAs into the peer's TMEM are done

@@ -52,15 +52,47 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// the same with acquire semantics at cluster scope (a phase completed from the peer CTA)
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete; false on timeout.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (poll()) return true;
     const uint64_t t0 = globaltimer();
     uint32_t n = 0;
-    while (!mbar_try_wait(bar, parity)) {
+    while (!poll()) {
         if ((++n & 255u) == 0 && globaltimer() - t0 > kWaitTimeoutNs) return false;
     }
     return true;
+}
+
+// named barrier `id` (1..15) over `n` threads (a multiple of 32)
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// named barrier that also returns the AND of `v` over the `n` participating threads
+__device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
 }
 
 // ---------------------------------------------------------------- TMA
@@ -162,6 +194,15 @@ __device__ __forceinline__ void cluster_sync() {
 // Arrive on an mbarrier given by its shared::cluster address (possibly the peer CTA's).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// 4-byte store into the peer CTA's shared memory that completes 4 transaction bytes on
+// an mbarrier there (release at cluster scope); the issuing thread does not wait for it,
+// unlike a cluster-scope arrive
+__device__ __forceinline__ void st_async_signal(uint32_t cluster_addr, uint32_t value, uint32_t cluster_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cluster_addr),
+                 "r"(value), "r"(cluster_bar)
+                 : "memory");
 }
 
 // TMA load into this CTA's shared memory that signals an mbarrier in either CTA of the pair.
