@@ -25,7 +25,6 @@
 #include "kernels.h"
 #include "tc_ptx.cuh"
 
-#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -42,7 +41,10 @@ constexpr int kConvWarps = 8;                 // FP8 weights: dequantising warps
 // so that several stages are dequantised at once and one group's proxy fence overlaps
 // another's work.  Owning whole stages keeps every mbarrier phase wait of a group within
 // one phase of the barrier (a stage cannot move on before its owner has arrived).
-constexpr int kConvGroups = 2;
+#ifndef MOE_CONV_GROUPS
+#define MOE_CONV_GROUPS 2
+#endif
+constexpr int kConvGroups = MOE_CONV_GROUPS;
 constexpr int kSignalBytes = 4;                // FP8 pairs: the peer's "B half converted" store
 static_assert(kConvWarps % kConvGroups == 0 && (kConvGroups & (kConvGroups - 1)) == 0, "converter groups");
 constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -115,6 +117,78 @@ template <bool PAIRED, int BN>
 __device__ __forceinline__ int b_col(int j, int nt, int ncols) {
     if (PAIRED) return (j < 2 ? 0 : ncols) + nt * (BN / 2) + (j & 1) * 64;
     return nt * BN + j * 64;
+}
+
+// ---- e4m3 -> bf16 by bit placement.  A code c = s|eeee|mmm placed as the bf16 bit
+// pattern s|0000eeee|mmm0000 has the value c * 2^-120 (for e = 0 too: the pattern is then
+// a bf16 subnormal with the same mantissa), so one exact bf16 multiply by 2^120 * scale
+// (a power of two) gives the dequantised weight.  When 2^120 * scale is beyond bf16's
+// range (scale > 2^7) the multiply is split into 2^120 and scale.
+constexpr uint32_t kBf16x2Pow120 = 0x7B807B80u;    // (2^120, 2^120)
+
+// biased binary exponent of a power of two (fp32 subnormals included); -1000 for zero
+__device__ __forceinline__ int pow2_biased_exp(float s) {
+    const uint32_t b = __float_as_uint(s);
+    const int e = (int)((b >> 23) & 0xffu);
+    return e ? e : (b ? ilogbf(s) + 127 : -1000);
+}
+
+// bf16 bit pattern of the power of two with biased exponent e (subnormal below 1; 0 for none)
+__device__ __forceinline__ uint32_t bf16_pow2_bits(int e) {
+    return e >= 1 ? (uint32_t)e << 7 : (e >= -6 ? 1u << (e + 6) : 0u);
+}
+
+// multipliers for 8 consecutive columns (bf16x2 pairs) from their scales; sets `big` when
+// 2^120 * scale overflows bf16 for one of them, and then holds the scales themselves
+__device__ __forceinline__ void fp8_multipliers(const float* sc, uint32_t* m, bool& big) {
+    // common case, all eight scales normal powers of two <= 2^7: the bf16 pattern of a
+    // power of two is the upper half of its fp32 pattern, and 120 << 7 adds 120 to the
+    // exponent field
+    uint32_t b[8];
+    bool fast = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        b[i] = __float_as_uint(sc[i]);
+        fast &= b[i] - 0x00800000u <= 0x43000000u - 0x00800000u;
+    }
+    if (fast) {
+        big = false;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m[i] = __byte_perm(b[2 * i], b[2 * i + 1], 0x7632) + 0x3C003C00u;
+        return;
+    }
+    int e[8];
+    big = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        e[i] = pow2_biased_exp(sc[i]);
+        big |= e[i] + 120 > 254;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int a = e[2 * i] + (big ? 0 : 120), b = e[2 * i + 1] + (big ? 0 : 120);
+        m[i] = bf16_pow2_bits(a) | (bf16_pow2_bits(b) << 16);
+    }
+}
+
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+    __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// 8 e4m3 codes (two words, first code in the low byte) -> 8 bf16 values (four words)
+__device__ __forceinline__ uint4 fp8x8_to_bf16(uint2 q, const uint32_t* m, bool big) {
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t w = h ? q.y : q.x;
+        const uint32_t v = __byte_perm(w, 0, 0x3120);      // lanes (c0 | c2 << 8, c1 | c3 << 8)
+        o[2 * h] = ((v & 0x007f007fu) << 4) | ((v << 8) & 0x80008000u);     // (c0, c1)
+        o[2 * h + 1] = ((v & 0x7f007f00u) >> 4) | (v & 0x80008000u);       // (c2, c3)
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = hmul2_bits(big ? hmul2_bits(o[i], kBf16x2Pow120) : o[i], m[i]);
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 template <int EPI, bool B_MN, int BN, bool PAIR, bool Q8>
@@ -394,7 +468,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
         // e4m3 codes (staging slot, plain row-major boxes of 64 bytes per row) -> bf16 in
         // the 128-byte-swizzled layout TMA would have written: row r, 16-byte chunk cc of
         // 8 elements at r * 128 + ((cc ^ (r & 7)) << 4); each value times its column's
-        // power-of-two scale (exact).
+        // power-of-two scale (exact, fp8x8_to_bf16).
         if constexpr (Q8) {
             constexpr int kGT = 32 * (kConvWarps / kConvGroups);    // threads of one group
             constexpr int kUnits = G::kQBytes / 8;                  // 8 codes per unit
@@ -411,7 +485,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             int stage = 0;
             uint32_t sbits = 0;                                     // per-stage parity of staged_bar
             bool ok = true;
-            float sv[kBoxes][8];                                    // column scales of this thread's chunks
+            uint32_t fm[kBoxes][4];                                 // multipliers of this thread's chunks
+            bool big[kBoxes];
             // the warps of a group leave together: every exit decision is a group-wide vote
             // (an abort elsewhere stops the producer, and the next staged wait then runs out)
             for (int t = tile0; t < total_tiles && ok; t += tile_step) {
@@ -426,20 +501,19 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                         const bool in = col < g.ldb;
                         const float4 a = in ? __ldg(reinterpret_cast<const float4*>(se + col)) : make_float4(0, 0, 0, 0);
                         const float4 b = in ? __ldg(reinterpret_cast<const float4*>(se + col) + 1) : make_float4(0, 0, 0, 0);
-                        sv[j][0] = a.x; sv[j][1] = a.y; sv[j][2] = a.z; sv[j][3] = a.w;
-                        sv[j][4] = b.x; sv[j][5] = b.y; sv[j][6] = b.z; sv[j][7] = b.w;
+                        const float sc[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                        fp8_multipliers(sc, fm[j], big[j]);
                     }
                 }
                 const int nkb = P.num_kb + (P.lora_k16 ? 1 : 0);
                 for (int kb = 0; kb < nkb; ++kb) {
                     const bool mine = (stage % kConvGroups) == grp;
                     if (mine && kb < P.num_kb) {
+                        // K-major: the scales follow k; loaded before the wait, used after it
+                        float4 ka, kb4;
                         if constexpr (!B_MN) {
-                            // K-major: the scales follow k, fixed for the stage
-                            const float4 a = __ldg(reinterpret_cast<const float4*>(se + kb * BK + cc * 8));
-                            const float4 b = __ldg(reinterpret_cast<const float4*>(se + kb * BK + cc * 8) + 1);
-                            sv[0][0] = a.x; sv[0][1] = a.y; sv[0][2] = a.z; sv[0][3] = a.w;
-                            sv[0][4] = b.x; sv[0][5] = b.y; sv[0][6] = b.z; sv[0][7] = b.w;
+                            ka = __ldg(reinterpret_cast<const float4*>(se + kb * BK + cc * 8));
+                            kb4 = __ldg(reinterpret_cast<const float4*>(se + kb * BK + cc * 8) + 1);
                         }
                         const bool got = tc::mbar_wait(tc::smem_u32(&staged_bar[stage]), (sbits >> stage) & 1u);
                         if (!tc::named_bar_and(1 + grp, kGT, got && !*s_abort)) {
@@ -448,6 +522,10 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                             break;
                         }
                         sbits ^= 1u << stage;
+                        if constexpr (!B_MN) {
+                            const float sc[8] = {ka.x, ka.y, ka.z, ka.w, kb4.x, kb4.y, kb4.z, kb4.w};
+                            fp8_multipliers(sc, fm[0], big[0]);
+                        }
                         uint8_t* bt = smem + stage * kStageBytes + kABytes;
                         const uint8_t* qt = bt + G::kQBytes;
                         // all of the group's codes are read before any bf16 value overwrites them
@@ -465,20 +543,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                             const int u = gt + kGT * i;
                             const int j = B_MN ? (i * kGT) / 512 : 0;
                             const int r = B_MN ? ((u >> 3) & 63) : (u >> 3);
-                            const uint32_t w[2] = {q[i].x, q[i].y};
-                            uint32_t o[4];
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const uint16_t pr = (uint16_t)(w[h >> 1] >> ((h & 1) * 16));
-                                uint32_t f16x2;
-                                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pr));
-                                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&f16x2));
-                                const __nv_bfloat162 bv =
-                                    __floats2bfloat162_rn(f.x * sv[j][2 * h], f.y * sv[j][2 * h + 1]);
-                                o[h] = *reinterpret_cast<const uint32_t*>(&bv);
-                            }
                             *reinterpret_cast<uint4*>(bt + j * kBoxMN + r * 128 + ((cc ^ (r & 7)) << 4)) =
-                                make_uint4(o[0], o[1], o[2], o[3]);
+                                fp8x8_to_bf16(q[i], fm[j], big[j]);
                         }
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     }

@@ -298,9 +298,9 @@ def quantize_fp8(W):
     column), codes = e4m3 round-to-nearest-even of W / scale.  W: [..., rows, cols].
     Returns (codes uint8 in the e4m3 bit layout, scales float32 [..., cols]).
 
-    With power-of-two scales, W / scale is exact and every dequantised value
-    code * scale is exactly representable in bf16, so the quantised base weights
-    are a set of bf16 weights."""
+    With power-of-two scales, W / scale is exact, and code * scale rounded to bf16
+    (exact unless the scale is so small that the product falls below bf16's normal
+    range) gives a set of bf16 base weights."""
     import torch
     w = _f64(W)
     amax = np.abs(w).max(axis=-2)

@@ -74,6 +74,45 @@ def test_fp8_layer_is_bit_identical_to_bf16_on_dequantized_weights(name):
     assert_close("y", to64(q8.y), orc.lora_fwd(c["x"], idx, w, *wts, cfg.scale))
 
 
+
+@pytest.mark.parametrize("name", ["ragged_single", "pairs_ragged"])
+def test_fp8_extreme_column_scales_bit_identical(name):
+    """Columns whose power-of-two scale is far from 1: above 2^7 (the dequantising
+    multiply is split in two), below fp32's normal range (a subnormal scale), and tiny
+    enough that code * scale rounds in bf16 -- the FP8 layer still matches the bf16 layer
+    on the dequantised weights bit for bit."""
+    import moe_expert_dispatch_stable_gb300 as moe
+    cfg = CASES[name]
+    idx, w, ts = make_case(cfg, seed=5)
+    ts = dict(ts)
+    W_gu, W_d = ts["W_gu"].clone(), ts["W_d"].clone()
+    W_gu[:, :, 0:8] *= 2.0 ** 26                         # gate columns: scale > 2^7
+    W_gu[:, :, cfg.I + 8:cfg.I + 16] *= 2.0 ** -120      # up columns: scale below 2^-126
+    W_d[:, :, 3] *= 2.0 ** 26
+    W_d[:, :, 5:7] *= 2.0 ** -125
+    ts["W_gu"], ts["W_d"] = W_gu, W_d
+    wq = moe.quantize_expert_weights(ts)
+    torch.cuda.synchronize()
+    assert float(wq["s_gu"][:, 0:8].min()) > 2.0 ** 7
+    assert float(wq["s_gu"][:, cfg.I + 8:cfg.I + 16].max()) < 2.0 ** -126
+    bf = dict(ts)
+    for name_w, qn, sn in (("W_gu", "Wq_gu", "s_gu"), ("W_d", "Wq_d", "s_d")):
+        codes, scales = orc.quantize_fp8(ts[name_w].cpu())
+        assert np.array_equal(wq[qn].cpu().numpy(), codes) and np.array_equal(wq[sn].cpu().numpy(), scales)
+        bf[name_w] = (wq[qn].view(torch.float8_e4m3fn).float() * wq[sn][:, None, :]).to(torch.bfloat16)
+    d = moe.Dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r, cfg.scale)
+    ti, tw = torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda()
+    ref = moe.MoELoRALayer(d, bf)
+    q8 = moe.MoELoRALayer(d, wq)
+    g_ref = ref.step(ti, tw, ts["x"], ts["dy"])
+    g_q8 = q8.step(ti, tw, ts["x"], ts["dy"])
+    torch.cuda.synchronize()
+    assert int(q8.dev_status.item()) == 0
+    assert bool(torch.isfinite(ref.y.float()).all())
+    assert torch.equal(q8.y, ref.y)
+    for a, b in zip(g_q8, g_ref):
+        assert torch.equal(a, b)
+
 def test_fp8_full_size_deepseek_shape_bit_identical():
     """The HBM-bound workload FP8 weights are for: 256 experts, H = 7168, 128 rows per expert."""
     import moe_expert_dispatch_stable_gb300 as moe
