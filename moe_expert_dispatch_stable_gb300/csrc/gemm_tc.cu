@@ -608,13 +608,11 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                         float hv[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) hv[i] = swiglu_f(gv[i], uv[i]);
-                        uint4* dg = reinterpret_cast<uint4*>(GU + (int64_t)p * 2 * I + n);
-                        uint4* du = reinterpret_cast<uint4*>(GU + (int64_t)p * 2 * I + I + n);
-                        uint4* dh = reinterpret_cast<uint4*>(Hh + (int64_t)p * I + n);
-                        // GU is only read again by the backward: stream it past L2 (evict-first)
-                        __stcs(dg, pack8_bf16(gv)); __stcs(dg + 1, pack8_bf16(gv + 8));
-                        __stcs(du, pack8_bf16(uv)); __stcs(du + 1, pack8_bf16(uv + 8));
-                        dh[0] = pack8_bf16(hv); dh[1] = pack8_bf16(hv + 8);
+                        // one full 32-byte sector per thread and store; GU is only read again
+                        // by the backward: stream it past L2 (evict-first)
+                        tc::st32_cs(GU + (int64_t)p * 2 * I + n, pack8_bf16(gv), pack8_bf16(gv + 8));
+                        tc::st32_cs(GU + (int64_t)p * 2 * I + I + n, pack8_bf16(uv), pack8_bf16(uv + 8));
+                        tc::st32(Hh + (int64_t)p * I + n, pack8_bf16(hv), pack8_bf16(hv + 8));
                     }
                 }
             } else if constexpr (EPI == EPI_DSWIGLU) {
@@ -627,10 +625,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 {
                     const int n = nt * BN + c0;
                     if (valid && n < I) {
-                        pg0 = __ldg(reinterpret_cast<const uint4*>(grow + n));
-                        pg1 = __ldg(reinterpret_cast<const uint4*>(grow + n) + 1);
-                        pu0 = __ldg(reinterpret_cast<const uint4*>(grow + I + n));
-                        pu1 = __ldg(reinterpret_cast<const uint4*>(grow + I + n) + 1);
+                        tc::ld32_nc(grow + n, pg0, pg1);
+                        tc::ld32_nc(grow + I + n, pu0, pu1);
                     }
                 }
 #pragma unroll 1
@@ -639,10 +635,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                     const int n = nt * BN + c;
                     const int nn = n + 16;
                     if (c + 16 < c0 + kSpan && valid && nn < I) {
-                        pg0 = __ldg(reinterpret_cast<const uint4*>(grow + nn));
-                        pg1 = __ldg(reinterpret_cast<const uint4*>(grow + nn) + 1);
-                        pu0 = __ldg(reinterpret_cast<const uint4*>(grow + I + nn));
-                        pu1 = __ldg(reinterpret_cast<const uint4*>(grow + I + nn) + 1);
+                        tc::ld32_nc(grow + nn, pg0, pg1);
+                        tc::ld32_nc(grow + I + nn, pu0, pu1);
                     }
                     float dh[16];
                     tc::tmem_ld16(tb + c, dh);
@@ -653,10 +647,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                         unpack8_bf16(u0, uu); unpack8_bf16(u1, uu + 8);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) dswiglu_f(dh[i], gg[i], uu[i], dg[i], du[i]);
-                        uint4* og = reinterpret_cast<uint4*>(dGU + (int64_t)p * 2 * I + n);
-                        uint4* ou = reinterpret_cast<uint4*>(dGU + (int64_t)p * 2 * I + I + n);
-                        og[0] = pack8_bf16(dg); og[1] = pack8_bf16(dg + 8);
-                        ou[0] = pack8_bf16(du); ou[1] = pack8_bf16(du + 8);
+                        tc::st32(dGU + (int64_t)p * 2 * I + n, pack8_bf16(dg), pack8_bf16(dg + 8));
+                        tc::st32(dGU + (int64_t)p * 2 * I + I + n, pack8_bf16(du), pack8_bf16(du + 8));
                     }
                 }
             } else if constexpr (EPI == EPI_PROJ) {
@@ -669,9 +661,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                     if (valid) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v[i] *= g.scale;
-                        uint4* o = reinterpret_cast<uint4*>(out + (int64_t)p * BN + c);
-                        o[0] = pack8_bf16(v);
-                        o[1] = pack8_bf16(v + 8);
+                        tc::st32(out + (int64_t)p * BN + c, pack8_bf16(v), pack8_bf16(v + 8));
                     }
                 }
             } else if constexpr (EPI == EPI_BF16) {
@@ -683,10 +673,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                     tc::tmem_ld_wait();
                     const int n = nt * BN + c;
                     if (valid && n < g.Ncols) {
-                        uint4* o = reinterpret_cast<uint4*>(out + (int64_t)p * g.ldo + n);
                         // read once by the combine and once by the backward: evict-first
-                        __stcs(o, pack8_bf16(v));
-                        __stcs(o + 1, pack8_bf16(v + 8));
+                        tc::st32_cs(out + (int64_t)p * g.ldo + n, pack8_bf16(v), pack8_bf16(v + 8));
                     }
                 }
             } else {
@@ -698,10 +686,11 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                     tc::tmem_ld_wait();
                     const int n = nt * BN + c;
                     if (valid && n < g.Ncols) {
-                        float4* o = reinterpret_cast<float4*>(out + (int64_t)p * g.ldo + n);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)   // read once by the combine: evict-first
-                            __stcs(o + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                        float* o = out + (int64_t)p * g.ldo + n;
+                        const uint4* u = reinterpret_cast<const uint4*>(v);
+                        // read once by the combine: evict-first
+                        tc::st32_cs(o, u[0], u[1]);
+                        tc::st32_cs(o + 8, u[2], u[3]);
                     }
                 }
             }
