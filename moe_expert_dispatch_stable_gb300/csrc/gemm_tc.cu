@@ -73,6 +73,7 @@ struct Geo {
 
 struct TcParams {
     CUtensorMap tm_a, tm_b, tm_a2, tm_b2;
+    CUtensorMap tm_a64, tm_a2_64;   // SM pairs: 64-row boxes of A / A2 for half tiles
     GroupedGemm g;
     int num_kb;         // K / 64
     int lora_k16;       // RP / 16 (0: no LoRA step)
@@ -117,6 +118,24 @@ template <bool PAIRED, int BN>
 __device__ __forceinline__ int b_col(int j, int nt, int ncols) {
     if (PAIRED) return (j < 2 ? 0 : ncols) + nt * (BN / 2) + (j & 1) * 64;
     return nt * BN + j * 64;
+}
+
+// SM pairs: first column of box jj (0, 1) of CTA `rank`'s half of B.  A full tile (M = 256)
+// gives CTA 0 the instruction's columns [0, 128) and CTA 1 [128, 256): for gate/up pairs
+// that is (gate 0-63, gate 64-127 | up 0-63, up 64-127).  A half tile (M = 128, 64 rows per
+// CTA) folds the columns [128, 256) onto TMEM lanes 64-127 of the same TMEM columns, so for
+// gate/up pairs it takes (gate 0-63, up 0-63 | gate 64-127, up 64-127): each epilogue thread
+// then holds the gate and the up accumulator of the same output column.
+template <bool PAIRED, int BN>
+__device__ __forceinline__ int b_col_pair(bool half, int rank, int jj, int nt, int ncols) {
+    if (PAIRED && half) return (jj == 0 ? 0 : ncols) + nt * (BN / 2) + rank * 64;
+    return b_col<PAIRED, BN>(2 * rank + jj, nt, ncols);
+}
+
+// SM pairs: a tile holds 256 rows of one expert; the expert's last tile is a half tile
+// (one M = 128 instruction, 64 rows per CTA) when at most 128 of its rows are left.
+__device__ __forceinline__ bool half_tile(const int32_t* s_off, int e, int mt) {
+    return s_off[e + 1] - (s_off[e] + mt * 2 * BM) <= BM;
 }
 
 // ---- e4m3 -> bf16 by bit placement.  A code c = s|eeee|mmm placed as the bf16 bit
@@ -266,9 +285,11 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&P.tm_a);
         tc::prefetch_tmap(&P.tm_b);
+        if (PAIR) tc::prefetch_tmap(&P.tm_a64);
         if (P.lora_k16) {
             tc::prefetch_tmap(&P.tm_a2);
             tc::prefetch_tmap(&P.tm_b2);
+            if (PAIR) tc::prefetch_tmap(&P.tm_a2_64);
         }
     }
     if (warp == 1) {
@@ -295,7 +316,12 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             for (int t = tile0; t < total_tiles && !*s_abort; t += tile_step) {
                 int e, mt, nt;
                 decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
-                const int m0 = s_off[e] + mt * TM + (int)rank * BM;      // this CTA's 128 rows
+                const bool half = PAIR && half_tile(s_off, e, mt);
+                const int m0 = s_off[e] + mt * TM + (int)rank * (half ? BM / 2 : BM);   // this CTA's rows
+                const CUtensorMap* tma = half ? &P.tm_a64 : &P.tm_a;
+                const CUtensorMap* tma2 = half ? &P.tm_a2_64 : &P.tm_a2;
+                const int a_bytes = half ? kABytes / 2 : kABytes;
+                const int a2_bytes = half ? P.a2_bytes / 2 : P.a2_bytes;
                 const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : P.num_kb + (P.lora_k16 ? 1 : 0);
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!tc::mbar_wait(tc::smem_u32(&empty_bar[stage]), phase ^ 1)) {
@@ -309,8 +335,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                         // both CTAs' loads complete on the leader's full barrier
                         const uint32_t fb = tc::mapa(fb_local, 0);
                         if (kb < P.num_kb && Q8) {
-                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * kABytes + kSignalBytes);
-                            tc::tma_load_2d_pair(sa, &P.tm_a, fb, kb * BK, m0);
+                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * a_bytes + kSignalBytes);
+                            tc::tma_load_2d_pair(sa, tma, fb, kb * BK, m0);
                             const uint32_t sq = sb + G::kQBytes;
                             const uint32_t qb = tc::smem_u32(&staged_bar[stage]);
                             tc::mbar_arrive_expect_tx(qb, G::kQBytes);
@@ -318,28 +344,28 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
 #pragma unroll
                                 for (int jj = 0; jj < 2; ++jj)
                                     tc::tma_load_3d(sq + jj * (kBoxMN / 2), &P.tm_b, qb,
-                                                    b_col<PAIRED, BN>(2 * (int)rank + jj, nt, g.Ncols), kb * BK, e);
+                                                    b_col_pair<PAIRED, BN>(half, (int)rank, jj, nt, g.Ncols), kb * BK, e);
                             } else {
                                 tc::tma_load_3d(sq, &P.tm_b, qb, kb * BK, nt * BN + (int)rank * (BN / 2), e);
                             }
                         } else if (kb < P.num_kb) {
-                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * (kABytes + G::kBBytes));
-                            tc::tma_load_2d_pair(sa, &P.tm_a, fb, kb * BK, m0);
+                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * (a_bytes + G::kBBytes));
+                            tc::tma_load_2d_pair(sa, tma, fb, kb * BK, m0);
                             if (B_MN) {
 #pragma unroll
                                 for (int jj = 0; jj < 2; ++jj)
                                     tc::tma_load_3d_pair(sb + jj * kBoxMN, &P.tm_b, fb,
-                                                         b_col<PAIRED, BN>(2 * (int)rank + jj, nt, g.Ncols), kb * BK, e);
+                                                         b_col_pair<PAIRED, BN>(half, (int)rank, jj, nt, g.Ncols), kb * BK, e);
                             } else {
                                 tc::tma_load_3d_pair(sb, &P.tm_b, fb, kb * BK, nt * BN + (int)rank * (BN / 2), e);
                             }
                         } else {
-                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * (P.a2_bytes + 2 * P.b2_box_bytes));
-                            tc::tma_load_2d_pair(sa, &P.tm_a2, fb, 0, m0);
+                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * (a2_bytes + 2 * P.b2_box_bytes));
+                            tc::tma_load_2d_pair(sa, tma2, fb, 0, m0);
 #pragma unroll
                             for (int jj = 0; jj < 2; ++jj)
                                 tc::tma_load_3d_pair(sb + jj * P.b2_box_bytes, &P.tm_b2, fb,
-                                                     b_col<PAIRED, BN>(2 * (int)rank + jj, nt, g.Ncols), 0, e);
+                                                     b_col_pair<PAIRED, BN>(half, (int)rank, jj, nt, g.Ncols), 0, e);
                         }
                     } else if constexpr (G::KW > 1) {
                         // narrow tile: KW consecutive 64-column boxes of A and of B per stage
@@ -397,8 +423,11 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader only for pairs)
         if (lane == 0 && rank == 0) {
-            const uint32_t idesc = tc::idesc_bf16(TM, BN, false, B_MN);
-            const uint32_t idesc2 = tc::idesc_bf16(TM, BN, false, true);
+            const uint32_t idesc_full = tc::idesc_bf16(TM, BN, false, B_MN);
+            const uint32_t idesc2_full = tc::idesc_bf16(TM, BN, false, true);
+            // SM pairs, half tile: M = 128 (64 rows per CTA)
+            const uint32_t idesc_half = tc::idesc_bf16(BM, BN, false, B_MN);
+            const uint32_t idesc2_half = tc::idesc_bf16(BM, BN, false, true);
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -411,6 +440,14 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 }
                 tc::fence_after_sync();
                 const uint32_t d = tmem_base + acc * kAccCols;
+                bool half = false;
+                if constexpr (PAIR) {
+                    int e, mt, nt;
+                    decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
+                    half = half_tile(s_off, e, mt);
+                }
+                const uint32_t idesc = half ? idesc_half : idesc_full;
+                const uint32_t idesc2 = half ? idesc2_half : idesc2_full;
                 const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : P.num_kb + (P.lora_k16 ? 1 : 0);
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -497,7 +534,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                     // MN-major: a chunk's scales depend on its columns only, fixed for the tile
 #pragma unroll
                     for (int j = 0; j < kBoxes; ++j) {
-                        const int col = b_col<PAIRED, BN>((PAIR ? 2 * (int)rank : 0) + j, nt, g.Ncols) + cc * 8;
+                        const int col = (PAIR ? b_col_pair<PAIRED, BN>(half_tile(s_off, e, mt), (int)rank, j, nt, g.Ncols)
+                                              : b_col<PAIRED, BN>(j, nt, g.Ncols)) + cc * 8;
                         const bool in = col < g.ldb;
                         const float4 a = in ? __ldg(reinterpret_cast<const float4*>(se + col)) : make_float4(0, 0, 0, 0);
                         const float4 b = in ? __ldg(reinterpret_cast<const float4*>(se + col) + 1) : make_float4(0, 0, 0, 0);
@@ -567,20 +605,27 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
     } else {
         // ------------------------------------------------------------ epilogue
         // warp w reads TMEM lanes 32*(w%4)..+31 (one row per thread); the two warps of a
-        // lane quarter split the columns in halves.
+        // lane quarter split the columns in halves.  Half tiles (SM pairs, M = 128): lane L
+        // holds row L mod 64, lanes 64-127 the upper half of the columns in the same TMEM
+        // columns, so each warp covers half as many TMEM columns.
         const int q = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int hw = (warp - 2) >> 2;
         const int row = q * 32 + lane;
         constexpr int kSpan = PAIRED ? BN / 4 : (BN >= 32 ? BN / 2 : BN);   // columns per warp
-        const int c0 = (BN >= 32 || PAIRED) ? half * kSpan : 0;
-        const bool active = (BN >= 32 || PAIRED) || half == 0;
+        const int c0 = (BN >= 32 || PAIRED) ? hw * kSpan : 0;
+        const bool active = (BN >= 32 || PAIRED) || hw == 0;
         int it = 0;
         const uint32_t tempty_leader0 = PAIR ? tc::mapa(tc::smem_u32(&tempty_bar[0]), 0) : 0u;
         for (int t = tile0; t < total_tiles; t += tile_step, ++it) {
             int e, mt, nt;
             decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
-            const int m0 = s_off[e] + mt * TM + (int)rank * BM;
+            const bool htile = PAIR && half_tile(s_off, e, mt);
+            const int m0 = s_off[e] + mt * TM + (int)rank * (htile ? BM / 2 : BM);
             const int row_end = s_off[e + 1];
+            const int span = htile ? kSpan / 2 : kSpan;                 // TMEM columns of this warp
+            const int cb0 = htile ? hw * span : c0;
+            const int nbase = htile ? (q >> 1) * (PAIRED ? BN / 4 : BN / 2) : 0;   // output column offset
+            const int up_off = htile ? BN / 4 : BN / 2;                 // gate/up pairs: up's TMEM column - gate's
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             const bool ok = tc::mbar_wait(tc::smem_u32(&tfull_bar[acc]), acc_phase);
@@ -590,7 +635,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             }
             tc::fence_after_sync();
             const uint32_t tb = tmem_base + acc * kAccCols + ((uint32_t)(q * 32) << 16);
-            const int p = m0 + row;
+            const int p = m0 + (htile ? (row & 63) : row);
             const bool valid = p < row_end;
             if (!active) {
             } else if constexpr (EPI == EPI_SWIGLU) {
@@ -598,12 +643,12 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 bf16* GU = (bf16*)g.out0;
                 bf16* Hh = (bf16*)g.out1;
 #pragma unroll 1
-                for (int c = c0; c < c0 + kSpan; c += 16) {
+                for (int c = cb0; c < cb0 + span; c += 16) {
                     float gv[16], uv[16];
                     tc::tmem_ld16(tb + c, gv);
-                    tc::tmem_ld16(tb + BN / 2 + c, uv);
+                    tc::tmem_ld16(tb + up_off + c, uv);
                     tc::tmem_ld_wait();
-                    const int n = nt * (BN / 2) + c;
+                    const int n = nt * (BN / 2) + nbase + c;
                     if (valid && n < I) {
                         float hv[16];
 #pragma unroll
@@ -623,18 +668,18 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 // prefetch the (g, u) pair of the next 16 columns while this chunk computes
                 uint4 pg0 = make_uint4(0, 0, 0, 0), pg1 = pg0, pu0 = pg0, pu1 = pg0;
                 {
-                    const int n = nt * BN + c0;
+                    const int n = nt * BN + nbase + cb0;
                     if (valid && n < I) {
                         tc::ld32_nc(grow + n, pg0, pg1);
                         tc::ld32_nc(grow + I + n, pu0, pu1);
                     }
                 }
 #pragma unroll 1
-                for (int c = c0; c < c0 + kSpan; c += 16) {
+                for (int c = cb0; c < cb0 + span; c += 16) {
                     const uint4 g0 = pg0, g1 = pg1, u0 = pu0, u1 = pu1;
-                    const int n = nt * BN + c;
+                    const int n = nt * BN + nbase + c;
                     const int nn = n + 16;
-                    if (c + 16 < c0 + kSpan && valid && nn < I) {
+                    if (c + 16 < cb0 + span && valid && nn < I) {
                         tc::ld32_nc(grow + nn, pg0, pg1);
                         tc::ld32_nc(grow + I + nn, pu0, pu1);
                     }
@@ -654,7 +699,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             } else if constexpr (EPI == EPI_PROJ) {
                 bf16* out = (bf16*)g.out0;
 #pragma unroll
-                for (int c = c0; c < c0 + kSpan; c += 16) {
+                for (int c = cb0; c < cb0 + span; c += 16) {
                     float v[16];
                     tc::tmem_ld16(tb + c, v);
                     tc::tmem_ld_wait();
@@ -667,11 +712,11 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             } else if constexpr (EPI == EPI_BF16) {
                 bf16* out = (bf16*)g.out0;
 #pragma unroll 1
-                for (int c = c0; c < c0 + kSpan; c += 16) {
+                for (int c = cb0; c < cb0 + span; c += 16) {
                     float v[16];
                     tc::tmem_ld16(tb + c, v);
                     tc::tmem_ld_wait();
-                    const int n = nt * BN + c;
+                    const int n = nt * BN + nbase + c;
                     if (valid && n < g.Ncols) {
                         // read once by the combine and once by the backward: evict-first
                         tc::st32_cs(out + (int64_t)p * g.ldo + n, pack8_bf16(v), pack8_bf16(v + 8));
@@ -680,11 +725,11 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             } else {
                 float* out = (float*)g.out0;
 #pragma unroll 1
-                for (int c = c0; c < c0 + kSpan; c += 16) {
+                for (int c = cb0; c < cb0 + span; c += 16) {
                     float v[16];
                     tc::tmem_ld16(tb + c, v);
                     tc::tmem_ld_wait();
-                    const int n = nt * BN + c;
+                    const int n = nt * BN + nbase + c;
                     if (valid && n < g.Ncols) {
                         float* o = out + (int64_t)p * g.ldo + n;
                         const uint4* u = reinterpret_cast<const uint4*>(v);
@@ -834,6 +879,8 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
         const uint64_t st[1] = {(uint64_t)g.K * 2};
         const uint32_t box[2] = {BK, BM};
         if (!encode(&P.tm_a, g.A, 2, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        const uint32_t box64[2] = {BK, BM / 2};      // half tiles of SM pairs
+        if (pair && !encode(&P.tm_a64, g.A, 2, dims, st, box64, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     // B: expert stack
     {
@@ -859,6 +906,9 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
         const uint64_t st[1] = {(uint64_t)rp * 2};
         const uint32_t box[2] = {(uint32_t)rp, BM};
         if (!encode(&P.tm_a2, g.A2, 2, dims, st, box, swizzle_for_bytes(rp * 2))) return cudaErrorInvalidValue;
+        const uint32_t box64[2] = {(uint32_t)rp, BM / 2};
+        if (pair && !encode(&P.tm_a2_64, g.A2, 2, dims, st, box64, swizzle_for_bytes(rp * 2)))
+            return cudaErrorInvalidValue;
         P.a2_bytes = BM * rp * 2;
         P.a2_sbo = 8 * rp * 2;
         P.a2_swz = rp >= 64 ? tc::kSw128 : (rp >= 32 ? tc::kSw64 : tc::kSw32);

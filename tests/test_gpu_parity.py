@@ -133,6 +133,30 @@ def test_layer_parity_full(name):
             assert torch.count_nonzero(got[e]).item() == 0
 
 
+
+@pytest.mark.parametrize("counts", [[128, 129, 384, 1000], [385, 513]])
+def test_pairs_half_tile_boundaries(counts):
+    """SM pairs round each expert to 256-row tiles and run the last one as a half tile
+    (M = 128, 64 rows per CTA) when at most 128 rows are left: 128 rows (one half tile),
+    129 (one full tile), 384 (full + a half tile of exactly 128), 385 (full + full), 513
+    (two full + a half tile of one row).  Routing built by hand, k = 1."""
+    E = len(counts)
+    N = int(sum(counts))
+    assert N >= 384 * E                                       # the expert GEMMs run on SM pairs
+    cfg = mi.MoEConfig("half_tiles", T=N, H=128, E=E, k=1, I=192, r=8, alpha=16)
+    _, _, ts = make_case(cfg, seed=3)
+    rng = np.random.default_rng(7)
+    idx = rng.permutation(np.repeat(np.arange(E), counts)).reshape(N, 1).astype(np.int64)
+    w = rng.uniform(0.2, 1.0, size=(N, 1)).astype(np.float32)
+    layer, grads = run_layer(cfg, idx, w, ts)
+    assert int(layer.dev_status.item()) == 0
+    got_counts, _ = _check_route(layer, idx, cfg.E)
+    assert got_counts.tolist() == counts
+    y_ref, g_ref = _oracle_full(cfg, idx, w, ts)
+    assert_close("y", to64(layer.y), y_ref)
+    for nm, got, ref in zip(["dx", "dA_gu", "dB_gu", "dA_d", "dB_d"], grads, g_ref):
+        assert_close(nm, to64(got), ref)
+
 def test_B_zero_gives_exactly_zero_dA():
     cfg = SMALL_CASES["ragged"]
     idx, w, ts = make_case(cfg, seed=3, zero_B=True)
