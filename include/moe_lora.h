@@ -24,7 +24,9 @@
  * Conventions for every function:
  *  - All tensors are dense row-major; bf16 tensors are passed as uint16_t*.
  *  - Every pointer is a DEVICE pointer unless stated otherwise, 16-byte aligned,
- *    owned by the caller.  Buffers whose size is a multiple of T (x, y, dy, dx,
+ *    owned by the caller; the activation buffers x, y, dy, dx, saved and the
+ *    workspaces of moe_lora_fwd / moe_lora_bwd (and their _fp8 forms) are 32-byte
+ *    aligned (their rows are moved with 32-byte accesses).  Buffers whose size is a multiple of T (x, y, dy, dx,
  *    perm, inv_perm, w_sorted, saved, workspaces) may be NULL when T == 0.  The library allocates no device memory and keeps no
  *    state beyond a per-device cache of the SM count and of a driver entry point.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
@@ -62,7 +64,7 @@ enum {
     MOE_OK = 0,
     MOE_ERR_NULL_ARG = 1,      /* a required pointer is NULL */
     MOE_ERR_BAD_DIMS = 2,      /* sizes outside the supported range */
-    MOE_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+    MOE_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte (activation buffers: 32-byte) aligned */
     MOE_ERR_WORKSPACE = 4,     /* workspace / saved buffer smaller than required */
     MOE_ERR_CUDA = 5,          /* a CUDA runtime / driver call failed */
     MOE_ERR_UNSUPPORTED = 6    /* device is not sm_103 or a needed driver entry point is missing */

@@ -59,6 +59,9 @@ cudaError_t timed(const char* name, cudaStream_t s, F&& f, int n_ops = 1) {
 constexpr size_t kAlign = 256;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// activation rows (x, y, dy, dx and the saved / workspace buffers) are moved with 32-byte
+// accesses, one full L2 sector per thread
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 moe_status check_dims(const moe_dims* d) {
     if (d == nullptr) return MOE_ERR_NULL_ARG;
@@ -251,11 +254,11 @@ static moe_status fwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     // token-sized buffers may be NULL when T == 0; the forward workspace is unused (size 0)
     const void* tok[] = {x, y, saved};
     const void* always[] = {W_gu, A_gu, B_gu, W_d, A_d, B_d, dev_status};
-    if (!aligned16(workspace)) return MOE_ERR_MISALIGNED;
     for (const void* p : always) if (p == nullptr) return MOE_ERR_NULL_ARG;
     if (Nr > 0) for (const void* p : tok) if (p == nullptr) return MOE_ERR_NULL_ARG;
     for (const void* p : always) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
-    for (const void* p : tok) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    for (const void* p : tok) if (!aligned32(p)) return MOE_ERR_MISALIGNED;
+    if (!aligned32(workspace)) return MOE_ERR_MISALIGNED;
     const SavedLayout L = saved_layout(d);
     const FwdWs W = fwd_ws(d);
     if (saved_bytes < L.total || workspace_bytes < W.total) return MOE_ERR_WORKSPACE;
@@ -314,7 +317,7 @@ static moe_status bwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     for (const void* p : always) if (p == nullptr) return MOE_ERR_NULL_ARG;
     if (Nr > 0) for (const void* p : tok) if (p == nullptr) return MOE_ERR_NULL_ARG;
     for (const void* p : always) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
-    for (const void* p : tok) if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    for (const void* p : tok) if (!aligned32(p)) return MOE_ERR_MISALIGNED;
     if (!aligned16(d_topk_w)) return MOE_ERR_MISALIGNED;
     const SavedLayout L = saved_layout(d);
     const BwdWs W = bwd_ws(d);

@@ -4,6 +4,7 @@
 // with a couple of flops per element.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 #include <algorithm>
 
@@ -86,10 +87,50 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ src, int vpr, const
     }
 }
 
+// Unweighted gather (the forward's x -> x_perm): one warp per (sorted row, chunk of
+// 32 * kUpl 32-byte units), each lane issuing all its 32-byte loads before its stores.
+// Rows are 32-byte aligned (H % 16 == 0, 32-byte aligned buffers).
+constexpr int kUpl = 4;
+
+__global__ void gather_rows32_kernel(const uint8_t* __restrict__ src, int units, const int32_t* __restrict__ perm,
+                                     int64_t N, int k, uint8_t* __restrict__ dst) {
+    const int lane = threadIdx.x & 31;
+    const int cpr = (units + 32 * kUpl - 1) / (32 * kUpl);
+    const int64_t tasks = N * cpr;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t row_bytes = (int64_t)units * 32;
+    for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < tasks; task += nwarps) {
+        const int64_t p = task / cpr;
+        const int c = (int)(task - p * cpr);
+        const int64_t t = perm[p] / k;
+        const uint8_t* s = src + t * row_bytes;
+        uint8_t* d = dst + p * row_bytes;
+        uint4 a[kUpl], b[kUpl];
+#pragma unroll
+        for (int i = 0; i < kUpl; ++i) {
+            const int u = (c * kUpl + i) * 32 + lane;
+            if (u < units) tc::ld32_nc(s + (int64_t)u * 32, a[i], b[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < kUpl; ++i) {
+            const int u = (c * kUpl + i) * 32 + lane;
+            if (u < units) tc::st32(d + (int64_t)u * 32, a[i], b[i]);
+        }
+    }
+}
+
 cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, const float* w_sorted,
                                int64_t N, int k, void* dst, const void* O, float* d_w, cudaStream_t s) {
     if (N == 0) return cudaSuccess;
     const int threads = 256;
+    if (w_sorted == nullptr && H % 16 == 0) {
+        const int units = H / 16;
+        const int64_t tasks = N * ((units + 32 * kUpl - 1) / (32 * kUpl));
+        const int64_t blocks = std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms() * 16);
+        gather_rows32_kernel<<<(unsigned)blocks, threads, 0, s>>>((const uint8_t*)src, units, perm, N, k,
+                                                                 (uint8_t*)dst);
+        return cudaGetLastError();
+    }
     const int64_t blocks = std::min<int64_t>((N + 7) / 8, (int64_t)num_sms() * 16);
     gather_rows_kernel<<<(unsigned)blocks, threads, 0, s>>>((const uint4*)src, H / 8, perm, w_sorted, N, k,
                                                            (uint4*)dst, (const uint4*)O, d_w);
@@ -97,43 +138,76 @@ cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, cons
 }
 
 // ---------------------------------------------------------------- combine
-// One warp per token: out[t] = sum_{j=0}^{k-1} src[inv_perm[t*k+j]] in that order,
-// summed in fp32, 8 columns per lane per step (bf16 or fp32 source rows).
+// out[t] = sum_{j=0}^{k-1} w_j * src[inv_perm[t*k+j]] in that order, summed in fp32.
+// One warp per (token, chunk of 32 * combine_upl units of 16 columns); each lane loads the k
+// slots' 16 columns with 32-byte accesses (bf16 rows: one, fp32 rows: two per slot).
 template <typename SrcT>
-__device__ __forceinline__ void load8(const SrcT* row, int v, float* a);
+__device__ __forceinline__ void load16(const SrcT* row, int u, float* a);
 
 template <>
-__device__ __forceinline__ void load8<bf16>(const bf16* row, int v, float* a) {
-    unpack8(__ldcs(reinterpret_cast<const uint4*>(row) + v), a);
+__device__ __forceinline__ void load16<bf16>(const bf16* row, int u, float* a) {
+    uint4 x, y;
+    tc::ld32_cs(row + (int64_t)u * 16, x, y);
+    unpack8(x, a);
+    unpack8(y, a + 8);
 }
 
 template <>
-__device__ __forceinline__ void load8<float>(const float* row, int v, float* a) {
-    const float4 lo = __ldcs(reinterpret_cast<const float4*>(row) + 2 * v);
-    const float4 hi = __ldcs(reinterpret_cast<const float4*>(row) + 2 * v + 1);
-    a[0] = lo.x; a[1] = lo.y; a[2] = lo.z; a[3] = lo.w;
-    a[4] = hi.x; a[5] = hi.y; a[6] = hi.z; a[7] = hi.w;
+__device__ __forceinline__ void load16<float>(const float* row, int u, float* a) {
+    uint4 v[4];
+    tc::ld32_cs(row + (int64_t)u * 16, v[0], v[1]);
+    tc::ld32_cs(row + (int64_t)u * 16 + 8, v[2], v[3]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = __uint_as_float(reinterpret_cast<const uint32_t*>(v)[i]);
 }
+
+// units per lane and task (measured: one keeps the most warps resident)
+template <typename SrcT>
+__host__ __device__ constexpr int combine_upl() { return 1; }
 
 template <typename SrcT>
 __global__ void combine_kernel(const SrcT* __restrict__ src, const float* __restrict__ w_sorted,
                                const int32_t* __restrict__ inv_perm, int64_t T, int k, int H,
-                               uint4* __restrict__ out) {
+                               bf16* __restrict__ out) {
+    constexpr int kC = combine_upl<SrcT>();
     const int lane = threadIdx.x & 31;
-    const int vpr = H / 8;
+    const int units = H / 16;
+    const int cpr = (units + 32 * kC - 1) / (32 * kC);
+    const int64_t tasks = T * cpr;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
-        for (int v = lane; v < vpr; v += 32) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int j = 0; j < k; ++j) {
-                const int64_t row = inv_perm[t * k + j];
-                const float w = w_sorted != nullptr ? w_sorted[row] : 1.0f;
-                float a[8];
-                load8<SrcT>(src + row * H, v, a);
+    for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < tasks; task += nwarps) {
+        const int64_t t = task / cpr;
+        const int c = (int)(task - t * cpr);
+        float acc[kC][16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, a[i], acc[i]);
+        for (int i = 0; i < kC; ++i)
+#pragma unroll
+            for (int q = 0; q < 16; ++q) acc[i][q] = 0.f;
+        // the slots' rows and weights, 32 at a time one per lane, broadcast in slot order
+        for (int j0 = 0; j0 < k; j0 += 32) {
+            const int kj = min(32, k - j0);
+            const int64_t my_row = lane < kj ? inv_perm[t * k + j0 + lane] : 0;
+            const float my_w = (lane < kj && w_sorted != nullptr) ? w_sorted[my_row] : 1.0f;
+#pragma unroll 4
+            for (int j = 0; j < kj; ++j) {
+                const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
+                const float w = __shfl_sync(0xffffffffu, my_w, j);
+#pragma unroll
+                for (int i = 0; i < kC; ++i) {
+                    const int u = (c * kC + i) * 32 + lane;
+                    if (u < units) {
+                        float a[16];
+                        load16<SrcT>(src + row * H, u, a);
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) acc[i][q] = fmaf(w, a[q], acc[i][q]);
+                    }
+                }
             }
-            out[t * vpr + v] = pack8(acc);
+        }
+#pragma unroll
+        for (int i = 0; i < kC; ++i) {
+            const int u = (c * kC + i) * 32 + lane;
+            if (u < units) tc::st32(out + t * H + (int64_t)u * 16, pack8(acc[i]), pack8(acc[i] + 8));
         }
     }
 }
@@ -141,14 +215,18 @@ __global__ void combine_kernel(const SrcT* __restrict__ src, const float* __rest
 cudaError_t launch_combine(const void* src, bool src_f32, const float* w_sorted, const int32_t* inv_perm, int64_t T,
                            int k, int H, void* out, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
+    if (H % 16 != 0) return cudaErrorInvalidValue;
     const int threads = 256;
-    const int64_t blocks = std::min<int64_t>((T + 7) / 8, (int64_t)num_sms() * 16);
+    const int units = H / 16;
+    const int upl = src_f32 ? combine_upl<float>() : combine_upl<bf16>();
+    const int64_t tasks = T * ((units + 32 * upl - 1) / (32 * upl));
+    const int64_t blocks = std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms() * 16);
     if (src_f32)
         combine_kernel<float><<<(unsigned)blocks, threads, 0, s>>>((const float*)src, w_sorted, inv_perm, T, k, H,
-                                                                   (uint4*)out);
+                                                                   (bf16*)out);
     else
         combine_kernel<bf16><<<(unsigned)blocks, threads, 0, s>>>((const bf16*)src, w_sorted, inv_perm, T, k, H,
-                                                                  (uint4*)out);
+                                                                  (bf16*)out);
     return cudaGetLastError();
 }
 

@@ -110,6 +110,13 @@ __device__ __forceinline__ void st32_cs(void* p, const uint4& a, const uint4& b)
                  : "memory");
 }
 
+// 32 bytes read once (evict-first)
+__device__ __forceinline__ void ld32_cs(const void* p, uint4& a, uint4& b) {
+    asm volatile("ld.global.cs.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(p));
+}
+
 // 32 bytes of read-only data
 __device__ __forceinline__ void ld32_nc(const void* p, uint4& a, uint4& b) {
     asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"

@@ -88,18 +88,25 @@ def test_null_and_misaligned_arguments_rejected_before_launch(lib):
     assert lib.moe_route(ctypes.c_void_p(16), 2, ctypes.c_void_p(16), 8, 2, 4, ctypes.byref(rt),
                          ctypes.c_void_p(16), 1 << 20, ctypes.c_void_p(16), None) == 2
     d = b.Dims(8, 64, 64, 4, 2, 4, 2.0).c_struct()
-    p = [ctypes.c_void_p(16)] * 8
-    assert lib.moe_lora_fwd(ctypes.byref(d), ctypes.byref(rt), *p[:7], None, ctypes.c_void_p(16), 1 << 30,
-                            ctypes.c_void_p(16), 1 << 30, ctypes.c_void_p(16), None) == 1
-    assert lib.moe_lora_fwd(ctypes.byref(d), ctypes.byref(rt), *p, ctypes.c_void_p(16), 1,
-                            ctypes.c_void_p(16), 1 << 30, ctypes.c_void_p(16), None) == 4
-    assert lib.moe_lora_bwd(ctypes.byref(d), ctypes.byref(rt), *p[:7], ctypes.c_void_p(16), 1 << 30,
-                            ctypes.c_void_p(24), *p[:4], None, ctypes.c_void_p(16), 1 << 30, ctypes.c_void_p(16),
-                            None) == 3
+    # weights 16-byte aligned, activation buffers (x, y, dy, dx, saved, workspace) 32-byte aligned
+    w16, a32, a16 = ctypes.c_void_p(16), ctypes.c_void_p(32), ctypes.c_void_p(48)
+    wts = [w16] * 6
+    assert lib.moe_lora_fwd(ctypes.byref(d), ctypes.byref(rt), a32, *wts, None, a32, 1 << 30,
+                            a32, 1 << 30, w16, None) == 1
+    assert lib.moe_lora_fwd(ctypes.byref(d), ctypes.byref(rt), a32, *wts, a32, a32, 1,
+                            a32, 1 << 30, w16, None) == 4
+    # x, y, saved or workspace only 16-byte aligned
+    for bad in range(4):
+        acts = [a16 if i == bad else a32 for i in range(4)]
+        assert lib.moe_lora_fwd(ctypes.byref(d), ctypes.byref(rt), acts[0], *wts, acts[1], acts[2], 1 << 30,
+                                acts[3], 1 << 30, w16, None) == 3
+    assert lib.moe_lora_bwd(ctypes.byref(d), ctypes.byref(rt), a32, *wts, a32, 1 << 30,
+                            ctypes.c_void_p(24), *[w16] * 4, None, a32, 1 << 30, w16, None) == 3
+    assert lib.moe_lora_bwd(ctypes.byref(d), ctypes.byref(rt), a32, *wts, a32, 1 << 30,
+                            a16, *[w16] * 4, None, a32, 1 << 30, w16, None) == 3
     # misaligned d_topk_w
-    assert lib.moe_lora_bwd(ctypes.byref(d), ctypes.byref(rt), *p[:7], ctypes.c_void_p(16), 1 << 30,
-                            ctypes.c_void_p(16), *p[:4], ctypes.c_void_p(20), ctypes.c_void_p(16), 1 << 30,
-                            ctypes.c_void_p(16), None) == 3
+    assert lib.moe_lora_bwd(ctypes.byref(d), ctypes.byref(rt), a32, *wts, a32, 1 << 30,
+                            a32, *[w16] * 4, ctypes.c_void_p(20), a32, 1 << 30, w16, None) == 3
     # router: bad sizes, NULL outputs, misaligned logits
     assert lib.moe_router_topk(ctypes.c_void_p(16), 8, 4, 5, ctypes.c_void_p(16), ctypes.c_void_p(16), None) == 2
     assert lib.moe_router_topk(ctypes.c_void_p(16), 8, 2048, 2, ctypes.c_void_p(16), ctypes.c_void_p(16), None) == 2

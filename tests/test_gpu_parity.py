@@ -30,6 +30,8 @@ SMALL_CASES = {
     "one_token": mi.MoEConfig("one", T=1, H=64, E=4, k=2, I=64, r=2, alpha=4),
     # rank 64
     "r64": mi.MoEConfig("r64", T=130, H=128, E=4, k=2, I=128, r=64, alpha=64),
+    # more than 32 slots per token: the combine broadcasts the slots 32 at a time
+    "k40": mi.MoEConfig("k40", T=40, H=64, E=48, k=40, I=64, r=4, alpha=8),
     # >= 384 rows per expert: the expert GEMMs run on SM pairs (256-row tiles, cta_group::2)
     "pairs_ragged": mi.MoEConfig("pairs", T=1000, H=256, E=4, k=2, I=320, r=16, alpha=32),
     # SM pairs with a skewed router: empty experts and last tiles with only the leader's rows
