@@ -6,8 +6,11 @@ unless --config says otherwise.  Prints ONE JSON line (rank 0).
 
   value        tokens/s of the whole job, device-timed (CUDA events around every
                step, inputs resident in HBM, L2 flushed between steps)
-  e2e          the same metric with the step's inputs copied from pinned host
-               memory and its results copied back inside the timed region
+  e2e          the same metric with every step's inputs copied from pinned host
+               memory and its results (y, dx, LoRA gradients) copied back inside
+               one timed span; two step slots on three streams, so copies of
+               neighbouring steps overlap a step's compute (no L2 flush there:
+               the weights alone exceed L2)
   roofline     the dominant kernel (largest share of the step), its algorithmic
                flops (or bytes) per launch over its event-timed duration
   gemm         all grouped-GEMM kernels together: algorithmic TFLOP/s and the
@@ -87,7 +90,8 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
 # DRAM bytes (read + write) per launch from ncu captures of the current kernels
 # (profiles/), keyed by (workload, kernel); None where no capture of the current code exists.
 MEASURED_TRAFFIC = {
-    ("gptoss20b", "gemm_gate_up_fwd"): 1.453e9 + 0.264e9,
+    ("gptoss20b", "gemm_gate_up_fwd"): 1.384e9 + 0.264e9,
+    ("gptoss20b", "gemm_gate_up_bwd"): 1.467e9 + 0.180e9,
 }
 
 
@@ -405,37 +409,58 @@ def main():
     total_ms = max_over_ranks(sum(step_ms), dev)
     value = job_throughput(cfg.T, args.steps, world, total_ms)
 
-    # ---- end to end through host buffers
+    # ---- end to end through host buffers: every step copies its inputs from pinned host
+    # memory and its results (y, dx, LoRA gradients) back.  Two step slots (inputs and a
+    # layer each) on three streams, so that step i+1's upload and step i-1's download run
+    # while step i computes; one continuous timed span from the first upload to the last
+    # download.  No L2 flush in this span: the weights alone (>= 1.6 GB) exceed L2.
     h_x = ts["x"].cpu().pin_memory(); h_dy = ts["dy"].cpu().pin_memory()
     h_idx = torch.from_numpy(idx).pin_memory(); h_w = torch.from_numpy(w).pin_memory()
     h_y = torch.empty_like(h_x).pin_memory(); h_dx = torch.empty_like(h_x).pin_memory()
     h_g = [torch.empty(g.shape, dtype=g.dtype).pin_memory() for g in layer.grads]
-    d_x = torch.empty_like(ts["x"]); d_dy = torch.empty_like(ts["dy"])
-    d_idx = torch.empty_like(t_idx); d_w = torch.empty_like(t_w)
+    slots = [layer, moe.MoELoRALayer(layer.d, layer.w, dev)]
+    d_in = [(torch.empty_like(ts["x"]), torch.empty_like(ts["dy"]), torch.empty_like(t_idx), torch.empty_like(t_w))
+            for _ in slots]
     bytes_in = sum(t.numel() * t.element_size() for t in (h_x, h_dy, h_idx, h_w))
     bytes_out = sum(t.numel() * t.element_size() for t in (h_y, h_dx, *h_g))
-    def e2e_step():
-        d_x.copy_(h_x, non_blocking=True); d_dy.copy_(h_dy, non_blocking=True)
-        d_idx.copy_(h_idx, non_blocking=True); d_w.copy_(h_w, non_blocking=True)
-        layer.step(d_idx, d_w, d_x, d_dy, with_topk_grad=False)
-        h_y.copy_(layer.y, non_blocking=True); h_dx.copy_(layer.dx, non_blocking=True)
-        for h, g in zip(h_g, layer.grads):
-            h.copy_(g, non_blocking=True)
-    for _ in range(2):
-        e2e_step()
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    computed = [torch.cuda.Event() for _ in slots]     # the slot's step has run
+    loaded = [torch.cuda.Event() for _ in slots]       # the slot's inputs are on the device
+    fetched = [torch.cuda.Event() for _ in slots]      # the slot's results are on the host
+
+    def e2e_steps(n):
+        for i in range(n):
+            sl = i % 2
+            lay, (d_x, d_dy, d_idx, d_w) = slots[sl], d_in[sl]
+            with torch.cuda.stream(up):
+                up.wait_event(computed[sl])            # the slot's previous step has read its inputs
+                d_x.copy_(h_x, non_blocking=True); d_dy.copy_(h_dy, non_blocking=True)
+                d_idx.copy_(h_idx, non_blocking=True); d_w.copy_(h_w, non_blocking=True)
+                loaded[sl].record(up)
+            stream.wait_event(loaded[sl])
+            stream.wait_event(fetched[sl])             # the slot's previous results are out
+            lay.step(d_idx, d_w, d_x, d_dy, with_topk_grad=False)
+            computed[sl].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[sl])
+                h_y.copy_(lay.y, non_blocking=True); h_dx.copy_(lay.dx, non_blocking=True)
+                for h, g in zip(h_g, lay.grads):
+                    h.copy_(g, non_blocking=True)
+                fetched[sl].record(down)
+
+    e2e_steps(4)
     torch.cuda.synchronize()
-    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.zero_()
-        e_s[i].record(stream)
-        e2e_step()
-        e_e[i].record(stream)
+    if world > 1:
+        dist.barrier()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(up)
+    e2e_steps(args.steps)
+    e_end.record(down)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)), dev)
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
     clk = clocks.stop()
     e2e_value = job_throughput(cfg.T, args.steps, world, e2e_ms)
-    assert int(layer.dev_status.item()) == 0, "device status flag set"
+    assert all(int(l.dev_status.item()) == 0 for l in slots), "device status flag set"
 
     # ---- roofline of the dominant kernel and the GEMM aggregate
     peaks = load_peaks()
