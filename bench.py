@@ -318,12 +318,13 @@ def offload_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, L: int, reps: int)
     for nb in (2, 1):
         stack = OffloadedMoEStack(layer.d, weights, dev, buffers=nb)
         out["saved_bytes_per_layer"] = stack.saved_bytes
+        out["h2d_bytes_per_layer"] = stack.transfer_bytes
         stack.forward(ts["x"], routing)
         torch.cuda.synchronize()
         out[f"bwd_ms_{'double' if nb == 2 else 'single'}"] = timed(lambda: stack.backward(ts["dy"]))
         del stack
     torch.cuda.empty_cache()
-    out["h2d_gb_per_bwd"] = L * out["saved_bytes_per_layer"] / 1e9
+    out["h2d_gb_per_bwd"] = L * out["h2d_bytes_per_layer"] / 1e9
     return out
 
 

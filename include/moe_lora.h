@@ -162,6 +162,17 @@ MOE_API moe_status moe_lora_fwd_sizes(const moe_dims* d, size_t* saved_bytes, si
  * output of each slot).  For inspection and tests. */
 MOE_API moe_status moe_lora_saved_layout(const moe_dims* d, size_t offsets[6], int32_t* rp);
 
+/* Re-create the x_perm section of `saved` from the layer input x with the forward's
+ * own gather (x_perm[p] = x[perm[p] / k]), bit-identical to what moe_lora_fwd wrote.
+ * For a caller that keeps only the other sections between forward and backward (the
+ * reload of offloaded activations in the blog post "Unsloth와 NVIDIA의 협업은 LLM 학습
+ * 병목을 커널 밖에서 줄인다", section "핵심 아이디어 / 구조 / 동작 방식", moves GU .. HA_s back
+ * and regathers x_perm instead of copying it).  x [T, H] bf16 (32-byte aligned), `rt`
+ * the routing of the forward, `saved` as for moe_lora_fwd; nothing else in `saved` is
+ * touched.  Asynchronous on `stream`. */
+MOE_API moe_status moe_lora_saved_regather(const moe_dims* d, const moe_routing* rt, const uint16_t* x, void* saved,
+                                           size_t saved_bytes, void* stream);
+
 /* Forward of the MoE-LoRA expert layer (Split-LoRA, SwiGLU, weighted combine).
  *  x     [T, H]                  W_gu [E, H, 2I] (gate = cols [0,I), up = [I,2I))
  *  A_gu  [E, r, H] (A^T, the PEFT lora_A layout)   B_gu [E, r, 2I]

@@ -39,10 +39,10 @@ class moe_routing(ctypes.Structure):
 
 
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_launch_count", "moe_route_workspace_size", "moe_route",
-            "moe_lora_fwd_sizes", "moe_lora_saved_layout", "moe_lora_fwd",
+            "moe_lora_fwd_sizes", "moe_lora_saved_layout", "moe_lora_saved_regather", "moe_lora_fwd",
             "moe_lora_bwd_workspace_size", "moe_lora_bwd", "moe_timing_enable", "moe_timing_read",
             "moe_router_topk", "moe_router_bwd", "moe_quantize_fp8", "moe_lora_fwd_fp8", "moe_lora_bwd_fp8")
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 _lib = None
 
@@ -65,6 +65,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_route.argtypes = [vp, i32, vp, i64, i32, i32, P(moe_routing), vp, sz, vp, vp]
     lib.moe_lora_fwd_sizes.argtypes = [P(moe_dims), P(sz), P(sz)]
     lib.moe_lora_saved_layout.argtypes = [P(moe_dims), P(sz), P(i32)]
+    lib.moe_lora_saved_regather.argtypes = [P(moe_dims), P(moe_routing), vp, vp, sz, vp]
     lib.moe_lora_fwd.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 8 + [vp, sz, vp, sz, vp, vp]
     lib.moe_lora_bwd_workspace_size.argtypes = [P(moe_dims), P(sz)]
     lib.moe_lora_bwd.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 7 + [vp, sz] + [vp] * 6 + [vp, sz, vp, vp]
@@ -190,6 +191,14 @@ def moe_lora_saved_layout(d: Dims):
     rp = ctypes.c_int32()
     _check(load_library().moe_lora_saved_layout(ctypes.byref(d.c_struct()), offs, ctypes.byref(rp)))
     return list(offs), rp.value
+
+
+def moe_lora_saved_regather(d: Dims, rt: "Routing", x, saved, stream=None):
+    """Re-create the x_perm section of `saved` from the layer input x (the forward's gather)."""
+    _need(x, "x", torch.bfloat16, (d.T, d.H))
+    dd, rr = d.c_struct(), rt.c_struct()
+    _check(load_library().moe_lora_saved_regather(ctypes.byref(dd), ctypes.byref(rr), _ptr(x), _ptr(saved),
+                                                  saved.numel() * saved.element_size(), _stream(stream)))
 
 
 def moe_lora_bwd_workspace_size(d: Dims) -> int:

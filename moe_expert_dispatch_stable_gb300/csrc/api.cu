@@ -151,7 +151,7 @@ cudaError_t project(const void* In, int K, const void* Wt, int r, int rp, float 
 
 extern "C" {
 
-int32_t moe_abi_version(void) { return 2; }
+int32_t moe_abi_version(void) { return 3; }
 
 const char* moe_status_string(moe_status s) {
     switch (s) {
@@ -228,6 +228,25 @@ moe_status moe_lora_saved_layout(const moe_dims* d, size_t offsets[6], int32_t* 
     offsets[0] = L.x_perm; offsets[1] = L.gu; offsets[2] = L.h; offsets[3] = L.xa; offsets[4] = L.ha;
     offsets[5] = L.o;
     *rp = L.rp;
+    return MOE_OK;
+}
+
+moe_status moe_lora_saved_regather(const moe_dims* d, const moe_routing* rt, const uint16_t* x, void* saved,
+                                   size_t saved_bytes, void* stream) {
+    moe_status st = check_dims(d);
+    if (st != MOE_OK) return st;
+    const int64_t N = d->T * (int64_t)d->k;
+    if ((st = check_routing(rt, N)) != MOE_OK) return st;
+    if (N > 0 && (x == nullptr || saved == nullptr)) return MOE_ERR_NULL_ARG;
+    if (!aligned32(x) || !aligned32(saved)) return MOE_ERR_MISALIGNED;
+    const SavedLayout L = saved_layout(d);
+    if (saved_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (N == 0) return MOE_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    void* x_perm = static_cast<uint8_t*>(saved) + L.x_perm;
+    MOE_TRY(timed("gather_x", s, [&] {
+        return launch_gather_rows(x, d->H, rt->perm, nullptr, N, d->k, x_perm, nullptr, nullptr, s);
+    }));
     return MOE_OK;
 }
 

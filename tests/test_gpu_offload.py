@@ -62,3 +62,24 @@ def test_offloaded_stack_is_bit_identical_to_resident(buffers, L):
     dx2 = stack.backward(dy).clone()
     torch.cuda.synchronize()
     assert torch.equal(y2, y) and torch.equal(dx2, dx0)
+
+
+def test_saved_regather_reproduces_x_perm_bit_for_bit():
+    import moe_expert_dispatch_stable_gb300 as moe
+    cfg = mi.MoEConfig("regather", T=300, H=128, E=5, k=2, I=192, r=8, alpha=16)
+    d = moe.Dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r, cfg.scale)
+    weights, routing, x0, _ = _stack_inputs(cfg, 1)
+    layer = moe.MoELoRALayer(d, weights[0])
+    layer.route(*routing[0])
+    layer.forward(x0)
+    offs, _ = moe.moe_lora_saved_layout(d)
+    N = cfg.T * cfg.k
+    ref = layer.saved.clone()
+    layer.saved[offs[0]:offs[0] + N * cfg.H * 2].fill_(0x5A)      # scribble over the x_perm rows only
+    moe.moe_lora_saved_regather(d, layer.rt, x0, layer.saved)
+    torch.cuda.synchronize()
+    assert torch.equal(layer.saved, ref)
+    # the section really is x gathered in expert order
+    xp = layer.saved[offs[0]:offs[0] + N * cfg.H * 2].view(torch.bfloat16).view(N, cfg.H)
+    perm = layer.rt.perm.long()
+    assert torch.equal(xp, x0[perm // cfg.k])
