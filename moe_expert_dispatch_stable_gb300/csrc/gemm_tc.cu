@@ -46,6 +46,7 @@ constexpr int kConvWarps = 8;                 // FP8 weights: dequantising warps
 #endif
 constexpr int kConvGroups = MOE_CONV_GROUPS;
 constexpr int kSignalBytes = 4;                // FP8 pairs: the peer's "B half converted" store
+constexpr unsigned kPaceNs = 500;              // epilogue store pacing (see the epilogue)
 static_assert(kConvWarps % kConvGroups == 0 && (kConvGroups & (kConvGroups - 1)) == 0, "converter groups");
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 __host__ __device__ constexpr int threads_of(bool q8) { return kThreads + (q8 ? 32 * kConvWarps : 0); }
@@ -623,6 +624,12 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             const int m0 = s_off[e] + mt * TM + (int)rank * (htile ? BM / 2 : BM);
             const int row_end = s_off[e + 1];
             const int span = htile ? kSpan / 2 : kSpan;                 // TMEM columns of this warp
+            // Store pacing: all CTAs reach tile boundaries together, and their epilogue store
+            // bursts slow the next tile's first TMA loads.  While the CTA has another tile
+            // queued (the MMAs are busy with it, and this accumulator is not needed before the
+            // tile after that) the plain-store epilogues spread their chunks 0.5 us apart
+            // (measured: 2-10 % faster gate_up backward and down forward).
+            const bool pace = (EPI == EPI_BF16 || EPI == EPI_PLAIN_F32) && t + tile_step < total_tiles;
             const int cb0 = htile ? hw * span : c0;
             const int nbase = htile ? (q >> 1) * (PAIRED ? BN / 4 : BN / 2) : 0;   // output column offset
             const int up_off = htile ? BN / 4 : BN / 2;                 // gate/up pairs: up's TMEM column - gate's
@@ -713,6 +720,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 bf16* out = (bf16*)g.out0;
 #pragma unroll 1
                 for (int c = cb0; c < cb0 + span; c += 16) {
+                    if (pace && c != cb0) __nanosleep(kPaceNs);
                     float v[16];
                     tc::tmem_ld16(tb + c, v);
                     tc::tmem_ld_wait();
@@ -726,6 +734,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 float* out = (float*)g.out0;
 #pragma unroll 1
                 for (int c = cb0; c < cb0 + span; c += 16) {
+                    if (pace && c != cb0) __nanosleep(kPaceNs);
                     float v[16];
                     tc::tmem_ld16(tb + c, v);
                     tc::tmem_ld_wait();
