@@ -91,7 +91,6 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
 # (profiles/), keyed by (workload, kernel); None where no capture of the current code exists.
 MEASURED_TRAFFIC = {
     ("gptoss20b", "gemm_gate_up_fwd"): 1.384e9 + 0.264e9,
-    ("gptoss20b", "gemm_gate_up_bwd"): 1.467e9 + 0.180e9,
 }
 
 
