@@ -135,8 +135,8 @@ MOE_API moe_status moe_route(const void* topk_idx, int32_t idx_bytes, const floa
  * outputs); the routing scratch lives instead in one file-scope device array of
  * MOE_ROUTE_STATIC_SCRATCH_BYTES that every GPU loading the library holds until
  * the process exits.  The call needs moe_route_workspace_size(T, k, E) <=
- * MOE_ROUTE_STATIC_SCRATCH_BYTES, i.e. ceil(T*k / 4096) * E * 4 + 512 bytes at
- * most (for example T*k <= 258048 slots at E = 1024, or T*k <= 2093056 at
+ * MOE_ROUTE_STATIC_SCRATCH_BYTES, i.e. ceil(T*k / 1024) * E * 4 + 512 bytes at
+ * most (for example T*k <= 64512 slots at E = 1024, or T*k <= 523264 at
  * E = 128); larger sizes return MOE_ERR_WORKSPACE and launch nothing.
  *
  * The first call on a device looks up the array's device address (once per

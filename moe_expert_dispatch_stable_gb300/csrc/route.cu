@@ -5,14 +5,14 @@
 // expert by: flatten the top-k assignment, stable-sort it by expert id,
 // bincount once, slice by offsets.  Here the three steps are two kernels:
 //
-//   route_count   each CTA histograms a 4096-slot chunk (warp-aggregated with
+//   route_count   each CTA histograms a 1024-slot chunk (warp-aggregated with
 //                 __match_any_sync into shared-memory counters) and writes its
 //                 per-expert counts; the last CTA to finish (atomic ticket after
 //                 a fence; no spinning) sums them, scans them to offsets and
 //                 tile offsets and turns the per-CTA counts into each CTA's
 //                 starting position inside every expert segment.
 //   route_scatter each CTA re-reads its chunk; every warp owns a contiguous
-//                 256-slot sub-chunk, so a slot's position is
+//                 64-slot sub-chunk, so a slot's position is
 //                   CTA base[e] + earlier warps' count[e] + earlier rounds' count[e]
 //                   + lanes below it with the same expert (popc of the match mask)
 //                 which is exactly its rank among equal keys in flat order: a
@@ -24,9 +24,9 @@
 
 namespace moe {
 
-constexpr int kRouteChunk = 4096;
+constexpr int kRouteChunk = 1024;            // slots per CTA: >= 16 CTAs at 16K slots
 constexpr int kCountThreads = 1024;
-constexpr int kScatterThreads = 512;                  // 16 warps x 256 slots
+constexpr int kScatterThreads = 512;                  // 16 warps x 64 slots
 constexpr int kScatterWarps = kScatterThreads / 32;
 constexpr int kSlotsPerWarp = kRouteChunk / kScatterWarps;
 

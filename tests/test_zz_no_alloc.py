@@ -67,14 +67,14 @@ def test_route_static_matches_route_on_consecutive_calls(lib):
 
 
 def test_route_static_rejects_sizes_beyond_its_scratch(lib):
-    # E = 1024 and 64 chunks of 4096 slots need 256 KiB + 256 B of scratch: refused before any launch
-    T, k, E = 65536, 4, 1024
+    # E = 1024 and 64 chunks of 1024 slots need 256 KiB + 256 B of scratch: refused before any launch
+    T, k, E = 16384, 4, 1024
     idx = torch.zeros((T, k), dtype=torch.int32, device="cuda")
     w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     st, _ = _static_route(lib, idx, w, E, status)
     assert st == 4                                          # MOE_ERR_WORKSPACE
     # one chunk fewer fits
-    st, _ = _static_route(lib, idx[: 63 * 1024], w[: 63 * 1024], E, status)
+    st, _ = _static_route(lib, idx[: 63 * 256], w[: 63 * 256], E, status)
     torch.cuda.synchronize()
     assert st == 0 and int(status.item()) == 0
