@@ -12,7 +12,12 @@ unless --config says otherwise.  Prints ONE JSON line (rank 0).
                neighbouring steps overlap a step's compute (no L2 flush there:
                the weights alone exceed L2)
   roofline     the dominant kernel (largest share of the step), its algorithmic
-               flops (or bytes) per launch over its event-timed duration
+               flops (or bytes) per launch over its event-timed duration (CUDA
+               events around each library launch, in a second timed pass of the
+               same steps: they cost ~2 % of a step, so the value pass runs
+               without them)
+  graph_ms_per_step  the same step replayed from a captured CUDA graph (launch
+               gaps removed), for information
   gemm         all grouped-GEMM kernels together: algorithmic TFLOP/s and the
                fraction of the measured dense bf16 peak
   cpu_baseline the CPU oracle timed on a bounded token sample (rank 0, N=1)
@@ -382,7 +387,7 @@ def main():
     torch.cuda.synchronize()
     assert int(layer.dev_status.item()) == 0, "device status flag set during warm-up"
 
-    # ---- device-timed region
+    # ---- device-timed region: the public-API step, CUDA events around every step
     clocks = ClockSampler(local)
     clocks.start()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -391,7 +396,6 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = moe.moe_launch_count()
-    moe.moe_timing_enable(True)
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()
@@ -402,12 +406,45 @@ def main():
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
-    moe.moe_timing_enable(False)
     launches = moe.moe_launch_count() - launches0
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    kt = moe.moe_timing_read()
     total_ms = max_over_ranks(sum(step_ms), dev)
     value = job_throughput(cfg.T, args.steps, world, total_ms)
+
+    # ---- per-kernel durations: a second timed pass of the same steps with the library's
+    # CUDA events around each of its launches (on the caller's stream); they add ~2 % to
+    # a step, so the pass above runs without them
+    torch.cuda.synchronize()
+    moe.moe_timing_enable(True)
+    for i in range(args.steps):
+        flush.zero_()
+        layer.step(t_idx, t_w, ts["x"], ts["dy"], with_topk_grad=False)
+    torch.cuda.synchronize()
+    moe.moe_timing_enable(False)
+    kt = moe.moe_timing_read()
+
+    # ---- the same step replayed from a CUDA graph (for information: launch gaps)
+    graph_ms = None
+    try:
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            layer.step(t_idx, t_w, ts["x"], ts["dy"], with_topk_grad=False)
+        torch.cuda.synchronize()
+        g_tot = 0.0
+        for i in range(max(10, args.steps // 4)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            g_tot += a.elapsed_time(b)
+        graph_ms = g_tot / max(10, args.steps // 4)
+        del g
+    except RuntimeError as exc:                          # capture unsupported: report why
+        graph_ms = f"unavailable: {exc}"
 
     # ---- end to end through host buffers: every step copies its inputs from pinned host
     # memory and its results (y, dx, LoRA gradients) back.  Two step slots (inputs and a
@@ -495,6 +532,7 @@ def main():
         "config": config_dict(cfg), "clocks": clk,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out},
         "gpu_launches": int(launches),
+        "graph_ms_per_step": graph_ms,
         "roofline": roof, "gemm": gemm,
         "layer_tflops": step_flops(cfg) / (total_ms / args.steps / 1e3) / 1e12,
         "wall_s_timed": wall,
