@@ -18,6 +18,35 @@ __device__ __forceinline__ bf16 f2bf(float v) { return __float2bfloat16_rn(v); }
 
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
 
+// ---- programmatic dependent launch
+// The library's kernels are launched with programmatic stream serialisation, so that a
+// kernel's launch overlaps the tail of the kernel before it on the stream.  Every kernel
+// starts with pdl_wait() (before any global-memory access or TMEM allocation: it then sees
+// every result of the previous kernel, exactly as with plain stream order).  The short
+// kernels (routing, gathers, combines, router) then call pdl_trigger(), so the next
+// kernel's launch proceeds while they run; the grouped GEMMs do not, since CTAs of the
+// next kernel waiting through a GEMM's whole duration measured slower.  Both are no-ops
+// for a kernel launched without the attribute.  Measured: the T = 64 layer's step
+// 0.114 -> 0.077 ms, the Qwen3-30B-shaped step 1.71 -> 1.67 ms.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Rounded-up padded LoRA rank used for the [N, RP] rank-r activations.
 inline int lora_rp(int r) { return r <= 16 ? 16 : (r <= 32 ? 32 : 64); }
 

@@ -213,6 +213,7 @@ __device__ __forceinline__ uint4 fp8x8_to_bf16(uint2 q, const uint32_t* m, bool 
 
 template <int EPI, bool B_MN, int BN, bool PAIR, bool Q8>
 __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams P) {
+    pdl_wait();      // no early trigger: dependents launch when this long kernel completes
     constexpr bool PAIRED = (EPI == EPI_SWIGLU);
     using G = Geo<BN, PAIR, Q8>;
     static_assert(!Q8 || BN == 256, "FP8 weights are for the expert GEMMs");
@@ -827,11 +828,10 @@ cudaError_t launch_tc(const TcParams& P, int64_t max_tiles, size_t smem, cudaStr
     if (e != cudaSuccess) return e;
     if constexpr (!PAIR) {
         const int grid = (int)std::min<int64_t>(sm_count(), max_tiles);
-        k<<<grid, kThr, smem, s>>>(P);
-        return cudaGetLastError();
+        return launch_pdl(k, dim3(grid), dim3(kThr), smem, s, P);
     } else {
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
@@ -848,6 +848,9 @@ cudaError_t launch_tc(const TcParams& P, int64_t max_tiles, size_t smem, cudaStr
         if (clusters < 1) return cudaErrorNotSupported;     // caller falls back to single-CTA tiles
         const int64_t pairs = std::min<int64_t>(clusters, max_tiles);
         cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see launch_pdl
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
         return cudaLaunchKernelEx(&cfg, k, P);
     }
 }

@@ -56,6 +56,7 @@ __device__ __forceinline__ void wg_decode(const WgradParams& P, int t, int& prob
 
 template <int RP>
 __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __grid_constant__ WgradParams P) {
+    pdl_wait();      // no early trigger: dependents launch when this long kernel completes
     constexpr int kBBytes = WK * RP * 2;
     constexpr int kStageBytes = kWABytes + ((kBBytes + 1023) / 1024) * 1024;
     constexpr int kAcc = RP;
@@ -295,8 +296,7 @@ cudaError_t launch_wg(const WgradParams& P, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int total = P.E * (P.m_tiles[0] + (P.nprob > 1 ? P.m_tiles[1] : 0));
     const int grid = std::min(wg_sm_count(), total);
-    k<<<grid, kWThreads, smem, s>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(grid), dim3(kWThreads), smem, s, P);
 }
 
 }  // namespace

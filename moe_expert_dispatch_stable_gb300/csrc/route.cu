@@ -73,6 +73,8 @@ route_count_kernel(const IdxT* __restrict__ idx, int64_t N, int E,
                    int32_t* __restrict__ block_counts, unsigned int* __restrict__ ticket,
                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                    int32_t* __restrict__ tile_offsets, int32_t* __restrict__ dev_status) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ int32_t hist[];                  // [E]
     __shared__ int warp_sums[32];
     __shared__ int scan_total;
@@ -133,6 +135,8 @@ route_scatter_kernel(const IdxT* __restrict__ idx, const float* __restrict__ top
                      const int32_t* __restrict__ block_base,
                      int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm,
                      float* __restrict__ w_sorted) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ int32_t wcnt[];                  // [kScatterWarps][E]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) wcnt[i] = 0;
@@ -194,26 +198,18 @@ cudaError_t launch_route(const void* idx, int idx_bytes, const float* topk_w, in
     if (err != cudaSuccess) return err;
     const size_t sm_count = (size_t)E * sizeof(int32_t);
     const size_t sm_scatter = (size_t)kScatterWarps * E * sizeof(int32_t);
-    if (idx_bytes == 8) {
-        auto kc = route_count_kernel<long long>;
-        auto ks = route_scatter_kernel<long long>;
-        cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scatter);
-        kc<<<nb, kCountThreads, sm_count, s>>>((const long long*)idx, N, E, block_counts, ticket,
-                                                 out.counts, out.offsets, out.tile_offsets, dev_status);
-        if (N > 0)
-            ks<<<nb, kScatterThreads, sm_scatter, s>>>((const long long*)idx, topk_w, N, E, block_counts,
-                                                       out.perm, out.inv_perm, out.w_sorted);
-    } else {
-        auto kc = route_count_kernel<int32_t>;
-        auto ks = route_scatter_kernel<int32_t>;
-        cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scatter);
-        kc<<<nb, kCountThreads, sm_count, s>>>((const int32_t*)idx, N, E, block_counts, ticket,
-                                                 out.counts, out.offsets, out.tile_offsets, dev_status);
-        if (N > 0)
-            ks<<<nb, kScatterThreads, sm_scatter, s>>>((const int32_t*)idx, topk_w, N, E, block_counts,
-                                                       out.perm, out.inv_perm, out.w_sorted);
-    }
-    return cudaGetLastError();
+    auto run = [&](auto kc, auto ks, const auto* ix) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scatter);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(kc, dim3(nb), dim3(kCountThreads), sm_count, s, ix, N, E, block_counts, ticket, out.counts,
+                       out.offsets, out.tile_offsets, dev_status);
+        if (e != cudaSuccess || N == 0) return e;
+        return launch_pdl(ks, dim3(nb), dim3(kScatterThreads), sm_scatter, s, ix, topk_w, N, E,
+                          (const int32_t*)block_counts, out.perm, out.inv_perm, out.w_sorted);
+    };
+    if (idx_bytes == 8)
+        return run(route_count_kernel<long long>, route_scatter_kernel<long long>, (const long long*)idx);
+    return run(route_count_kernel<int32_t>, route_scatter_kernel<int32_t>, (const int32_t*)idx);
 }
 
 // ---------------------------------------------------------------- fixed scratch

@@ -55,6 +55,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 __global__ void __launch_bounds__(32 * kRouterWarps)
 router_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ topk_idx,
                    float* __restrict__ topk_w) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ float zsh[];                              // [kRouterWarps][E] + masks
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float* z = zsh + warp * E;
@@ -98,6 +100,8 @@ router_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, in
 __global__ void __launch_bounds__(32 * kRouterWarps)
 router_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
                   const float* __restrict__ d_topk_w, int64_t T, int E, int k, float* __restrict__ d_logits) {
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int64_t t = (int64_t)blockIdx.x * kRouterWarps + warp; t < T; t += (int64_t)gridDim.x * kRouterWarps) {
         const float* row = logits + t * E;
@@ -129,16 +133,16 @@ cudaError_t launch_router_topk(const float* logits, int64_t T, int E, int k, int
     cudaError_t e = cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t blocks = std::min<int64_t>((T + kRouterWarps - 1) / kRouterWarps, 152 * 16);
-    router_topk_kernel<<<(unsigned)blocks, 32 * kRouterWarps, smem, s>>>(logits, T, E, k, topk_idx, topk_w);
-    return cudaGetLastError();
+    return launch_pdl(router_topk_kernel, dim3((unsigned)blocks), dim3(32 * kRouterWarps), smem, s, logits, T, E, k,
+                      topk_idx, topk_w);
 }
 
 cudaError_t launch_router_bwd(const float* logits, const int32_t* topk_idx, const float* d_topk_w, int64_t T, int E,
                               int k, float* d_logits, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int64_t blocks = std::min<int64_t>((T + kRouterWarps - 1) / kRouterWarps, 152 * 16);
-    router_bwd_kernel<<<(unsigned)blocks, 32 * kRouterWarps, 0, s>>>(logits, topk_idx, d_topk_w, T, E, k, d_logits);
-    return cudaGetLastError();
+    return launch_pdl(router_bwd_kernel, dim3((unsigned)blocks), dim3(32 * kRouterWarps), 0, s, logits, topk_idx,
+                      d_topk_w, T, E, k, d_logits);
 }
 
 }  // namespace moe

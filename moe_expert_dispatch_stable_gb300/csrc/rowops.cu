@@ -53,6 +53,8 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 __global__ void gather_rows_kernel(const uint4* __restrict__ src, int vpr, const int32_t* __restrict__ perm,
                                    const float* __restrict__ w_sorted, int64_t N, int k,
                                    uint4* __restrict__ dst, const uint4* __restrict__ O, float* __restrict__ d_w) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t p = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < N; p += nwarps) {
@@ -94,6 +96,8 @@ constexpr int kUpl = 4;
 
 __global__ void gather_rows32_kernel(const uint8_t* __restrict__ src, int units, const int32_t* __restrict__ perm,
                                      int64_t N, int k, uint8_t* __restrict__ dst) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int cpr = (units + 32 * kUpl - 1) / (32 * kUpl);
     const int64_t tasks = N * cpr;
@@ -127,14 +131,12 @@ cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, cons
         const int units = H / 16;
         const int64_t tasks = N * ((units + 32 * kUpl - 1) / (32 * kUpl));
         const int64_t blocks = std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms() * 16);
-        gather_rows32_kernel<<<(unsigned)blocks, threads, 0, s>>>((const uint8_t*)src, units, perm, N, k,
-                                                                 (uint8_t*)dst);
-        return cudaGetLastError();
+        return launch_pdl(gather_rows32_kernel, dim3((unsigned)blocks), dim3(threads), 0, s, (const uint8_t*)src,
+                          units, perm, N, k, (uint8_t*)dst);
     }
     const int64_t blocks = std::min<int64_t>((N + 7) / 8, (int64_t)num_sms() * 16);
-    gather_rows_kernel<<<(unsigned)blocks, threads, 0, s>>>((const uint4*)src, H / 8, perm, w_sorted, N, k,
-                                                           (uint4*)dst, (const uint4*)O, d_w);
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(threads), 0, s, (const uint4*)src, H / 8, perm,
+                      w_sorted, N, k, (uint4*)dst, (const uint4*)O, d_w);
 }
 
 // ---------------------------------------------------------------- combine
@@ -169,6 +171,8 @@ template <typename SrcT>
 __global__ void combine_kernel(const SrcT* __restrict__ src, const float* __restrict__ w_sorted,
                                const int32_t* __restrict__ inv_perm, int64_t T, int k, int H,
                                bf16* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int kC = combine_upl<SrcT>();
     const int lane = threadIdx.x & 31;
     const int units = H / 16;
@@ -222,12 +226,10 @@ cudaError_t launch_combine(const void* src, bool src_f32, const float* w_sorted,
     const int64_t tasks = T * ((units + 32 * upl - 1) / (32 * upl));
     const int64_t blocks = std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms() * 16);
     if (src_f32)
-        combine_kernel<float><<<(unsigned)blocks, threads, 0, s>>>((const float*)src, w_sorted, inv_perm, T, k, H,
-                                                                   (bf16*)out);
-    else
-        combine_kernel<bf16><<<(unsigned)blocks, threads, 0, s>>>((const bf16*)src, w_sorted, inv_perm, T, k, H,
-                                                                  (bf16*)out);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<float>, dim3((unsigned)blocks), dim3(threads), 0, s, (const float*)src,
+                          w_sorted, inv_perm, T, k, H, (bf16*)out);
+    return launch_pdl(combine_kernel<bf16>, dim3((unsigned)blocks), dim3(threads), 0, s, (const bf16*)src, w_sorted,
+                      inv_perm, T, k, H, (bf16*)out);
 }
 
 }  // namespace moe
