@@ -545,17 +545,31 @@ def main():
     d_lg = torch.empty_like(logits)
     moe.moe_router_bwd(logits, r_idx, d_tw, d_logits=d_lg)
     torch.cuda.synchronize()
-    moe.moe_timing_enable(True)
-    for _ in range(args.steps):
-        moe.moe_router_topk(logits, cfg.k, topk_idx=r_idx, topk_w=r_w)
-        moe.moe_router_bwd(logits, r_idx, d_tw, d_logits=d_lg)
-    torch.cuda.synchronize()
-    moe.moe_timing_enable(False)
-    rt_t = moe.moe_timing_read()
+    # device time per launch: each kernel replayed from a CUDA graph of 20 launches (a
+    # Python loop of launches would time the host, not these few-microsecond kernels)
     te = cfg.T * cfg.E * 4
     r_bytes = {"router_topk": te + cfg.T * cfg.k * 8, "router_bwd": 2 * te + cfg.T * cfg.k * 8}
-    line["router"] = {n: {"us_per_launch": 1e3 * ms / cnt, "gbs": r_bytes[n] / (ms / cnt / 1e3) / 1e9}
-                      for n, (ms, cnt) in rt_t.items() if n in r_bytes}
+    r_ops = {"router_topk": lambda: moe.moe_router_topk(logits, cfg.k, topk_idx=r_idx, topk_w=r_w),
+             "router_bwd": lambda: moe.moe_router_bwd(logits, r_idx, d_tw, d_logits=d_lg)}
+    line["router"] = {}
+    gs = torch.cuda.Stream(dev)
+    for n, op in r_ops.items():
+        gs.wait_stream(stream)
+        rg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(rg, stream=gs):
+            for _ in range(20):
+                op()
+        torch.cuda.synchronize()
+        reps = max(5, args.steps // 20)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            rg.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = 1e3 * a.elapsed_time(b) / (20 * reps)
+        line["router"][n] = {"us_per_launch": us, "gbs": r_bytes[n] / (us / 1e6) / 1e9}
+        del rg
     # ---- the same step with FP8 (e4m3) base weights, dequantised inside the GEMMs
     if not args.no_fp8:
         line["fp8_base"] = fp8_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, max(10, args.steps // 4), flush)

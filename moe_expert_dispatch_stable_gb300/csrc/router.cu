@@ -14,6 +14,7 @@
 #include "kernels.h"
 
 #include <algorithm>
+#include <mutex>
 
 namespace moe {
 
@@ -130,8 +131,20 @@ cudaError_t launch_router_topk(const float* logits, int64_t T, int E, int k, int
                                cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const size_t smem = (size_t)kRouterWarps * E * sizeof(float) + kRouterWarps * 32 * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    // raise the kernel's dynamic shared-memory limit only when a call needs more than before
+    {
+        static std::mutex mu;
+        static int granted[64] = {0};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64 || (int)smem > granted[dev]) {
+            cudaError_t e =
+                cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) granted[dev] = (int)smem;
+        }
+    }
     const int64_t blocks = std::min<int64_t>((T + kRouterWarps - 1) / kRouterWarps, 152 * 16);
     return launch_pdl(router_topk_kernel, dim3((unsigned)blocks), dim3(32 * kRouterWarps), smem, s, logits, T, E, k,
                       topk_idx, topk_w);
