@@ -36,6 +36,9 @@ SMALL_CASES = {
     "pairs_ragged": mi.MoEConfig("pairs", T=1000, H=256, E=4, k=2, I=320, r=16, alpha=32),
     # SM pairs with a skewed router: empty experts and last tiles with only the leader's rows
     "pairs_skew": mi.MoEConfig("pairs_skew", T=2000, H=128, E=8, k=2, I=192, r=8, alpha=16, zipf_s=1.2),
+    # SM pairs with the wider LoRA ranks: RP = 32 (64-byte swizzled A2) and RP = 64 (128-byte)
+    "pairs_r32": mi.MoEConfig("pairs_r32", T=1000, H=256, E=4, k=2, I=320, r=32, alpha=64),
+    "pairs_r64": mi.MoEConfig("pairs_r64", T=1000, H=192, E=4, k=2, I=256, r=64, alpha=64),
 }
 
 
