@@ -250,6 +250,18 @@ def config_dict(cfg):
             "l2": "flushed between steps (256 MiB write); inputs+weights also exceed L2"}
 
 
+def routing_summary(idx, E: int) -> dict:
+    """Expert row counts of the workload's routing (the skewed workload's histogram shows
+    its empty experts and hot ones)."""
+    counts = np.bincount(np.asarray(idx).reshape(-1), minlength=E)
+    mean = counts.sum() / E
+    out = {"min": int(counts.min()), "max": int(counts.max()), "mean": float(mean),
+           "zero_experts": int((counts == 0).sum()), "above_10x_mean": int((counts > 10 * mean).sum())}
+    if E <= 256:
+        out["counts"] = counts.tolist()
+    return out
+
+
 # ----------------------------------------------------------------------------- fp8 base weights
 def fp8_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, steps: int, flush) -> dict:
     """route + fwd + bwd with the expert base weights in FP8 (e4m3 codes + power-of-two
@@ -537,6 +549,13 @@ def main():
         "layer_tflops": step_flops(cfg) / (total_ms / args.steps / 1e3) / 1e12,
         "wall_s_timed": wall,
         "kernels_ms_per_step": {n: round(v, 4) for n, v in sorted(kernel_ms_step.items(), key=lambda kv: -kv[1])},
+        # HBM-bound kernels (routing, gathers, combines, projections, LoRA reductions):
+        # algorithmic bytes per launch over the event-timed launch duration
+        "kernels_hbm": {n: {"gbs": round(work[n]["bytes"] / (kt[n][0] / kt[n][1] / 1e3) / 1e9, 1),
+                            "frac_of_hbm": round(work[n]["bytes"] / (kt[n][0] / kt[n][1] / 1e3) / 1e9
+                                                 / peaks["hbm_gbs"], 3)}
+                        for n in sorted(kt) if n in work and work[n]["bound"] == "hbm" and kt[n][0] > 0},
+        "routing": routing_summary(idx, cfg.E),
     }
     # ---- router step in front of the layer (softmax + top-k and its backward), HBM-bound
     logits = torch.from_numpy(mi.router_logits(cfg, args.seed + rank)).float().to(dev)

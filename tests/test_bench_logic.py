@@ -49,3 +49,15 @@ def test_clock_sampler_parses_nvidia_smi_csv(tmp_path, monkeypatch):
 def test_load_peaks_reads_measured_file():
     pk = bench.load_peaks()
     assert pk["hbm_gbs"] > 1000 and pk["bf16_tflops"] > 100
+
+
+def test_routing_summary_shows_the_skew():
+    import bench
+    cfg = mi.CONFIGS["gptoss120b_skew"]
+    idx, _ = mi.make_routing(cfg, 0)
+    r = bench.routing_summary(idx, cfg.E)
+    assert sum(r["counts"]) == cfg.T * cfg.k and len(r["counts"]) == cfg.E
+    assert r["zero_experts"] > 0 and r["above_10x_mean"] > 0      # many empty experts, a few hot ones
+    flat = mi.CONFIGS["gptoss20b"]
+    r2 = bench.routing_summary(mi.make_routing(flat, 0)[0], flat.E)
+    assert r2["zero_experts"] == 0 and r2["above_10x_mean"] == 0
