@@ -158,7 +158,7 @@ const char* moe_status_string(moe_status s) {
         case MOE_OK: return "ok";
         case MOE_ERR_NULL_ARG: return "a required pointer is NULL";
         case MOE_ERR_BAD_DIMS: return "sizes outside the supported range";
-        case MOE_ERR_MISALIGNED: return "a pointer is not 16-byte aligned";
+        case MOE_ERR_MISALIGNED: return "a pointer is not 16-byte aligned (activation buffers: 32-byte)";
         case MOE_ERR_WORKSPACE: return "workspace or saved buffer too small";
         case MOE_ERR_CUDA: return "a CUDA call failed";
         case MOE_ERR_UNSUPPORTED: return "unsupported device or driver";
