@@ -95,7 +95,8 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
 # DRAM bytes (read + write) per launch from ncu captures of the current kernels
 # (profiles/), keyed by (workload, kernel); None where no capture of the current code exists.
 MEASURED_TRAFFIC = {
-    ("gptoss20b", "gemm_gate_up_fwd"): 1.384e9 + 0.264e9,
+    ("gptoss20b", "gemm_gate_up_fwd"): 1.426e9 + 0.265e9,
+    ("gptoss20b", "gemm_gate_up_bwd"): 1.480e9 + 0.179e9,
 }
 
 

@@ -89,13 +89,16 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ src, int vpr, const
     }
 }
 
-// Unweighted gather (the forward's x -> x_perm): one warp per (sorted row, chunk of
-// 32 * kUpl 32-byte units), each lane issuing all its 32-byte loads before its stores.
-// Rows are 32-byte aligned (H % 16 == 0, 32-byte aligned buffers).
+// Gather without the weight gradient (the forward's x -> x_perm, the backward's weighted
+// dy -> dY_perm): one warp per (sorted row, chunk of 32 * kUpl 32-byte units), each lane
+// issuing all its 32-byte loads before its stores.  Rows are 32-byte aligned (H % 16 == 0,
+// 32-byte aligned buffers).  With w_sorted, every element is scaled by the row's routing
+// weight (fp32 product, rounded to bf16), the same arithmetic as the one-warp-per-row kernel.
 constexpr int kUpl = 4;
 
 __global__ void gather_rows32_kernel(const uint8_t* __restrict__ src, int units, const int32_t* __restrict__ perm,
-                                     int64_t N, int k, uint8_t* __restrict__ dst) {
+                                     const float* __restrict__ w_sorted, int64_t N, int k,
+                                     uint8_t* __restrict__ dst) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
@@ -107,6 +110,7 @@ __global__ void gather_rows32_kernel(const uint8_t* __restrict__ src, int units,
         const int64_t p = task / cpr;
         const int c = (int)(task - p * cpr);
         const int64_t t = perm[p] / k;
+        const float w = w_sorted != nullptr ? w_sorted[p] : 1.0f;
         const uint8_t* s = src + t * row_bytes;
         uint8_t* d = dst + p * row_bytes;
         uint4 a[kUpl], b[kUpl];
@@ -118,7 +122,18 @@ __global__ void gather_rows32_kernel(const uint8_t* __restrict__ src, int units,
 #pragma unroll
         for (int i = 0; i < kUpl; ++i) {
             const int u = (c * kUpl + i) * 32 + lane;
-            if (u < units) tc::st32(d + (int64_t)u * 32, a[i], b[i]);
+            if (u < units) {
+                if (w_sorted != nullptr) {
+                    float f[16];
+                    unpack8(a[i], f);
+                    unpack8(b[i], f + 8);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) f[q] *= w;
+                    a[i] = pack8(f);
+                    b[i] = pack8(f + 8);
+                }
+                tc::st32(d + (int64_t)u * 32, a[i], b[i]);
+            }
         }
     }
 }
@@ -127,12 +142,12 @@ cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, cons
                                int64_t N, int k, void* dst, const void* O, float* d_w, cudaStream_t s) {
     if (N == 0) return cudaSuccess;
     const int threads = 256;
-    if (w_sorted == nullptr && H % 16 == 0) {
+    if (d_w == nullptr && H % 16 == 0) {
         const int units = H / 16;
         const int64_t tasks = N * ((units + 32 * kUpl - 1) / (32 * kUpl));
         const int64_t blocks = std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms() * 16);
         return launch_pdl(gather_rows32_kernel, dim3((unsigned)blocks), dim3(threads), 0, s, (const uint8_t*)src,
-                          units, perm, N, k, (uint8_t*)dst);
+                          units, perm, w_sorted, N, k, (uint8_t*)dst);
     }
     const int64_t blocks = std::min<int64_t>((N + 7) / 8, (int64_t)num_sms() * 16);
     return launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(threads), 0, s, (const uint4*)src, H / 8, perm,
