@@ -84,12 +84,24 @@ struct TcParams {
     uint32_t a2_sbo, a2_swz;
 };
 
+// Tile order: expert by expert; inside an expert, bands of kRasterRows row tiles, and in a
+// band the column tiles outer, the row tiles inner.  The CTAs that run at the same time then
+// share each weight slab (one expert's column tile) while it is in L2, instead of every
+// expert that straddles two waves of tiles loading all its slabs twice.  Each tile is
+// computed the same way whatever its place in the order, so results do not depend on it.
+constexpr int kRasterRows = 4;
+
 __device__ __forceinline__ void decode_tile(int t, int n_tiles, const int32_t* s_toff, int E, int& e, int& mt,
                                             int& nt) {
-    const int mg = t / n_tiles;
-    nt = t - mg * n_tiles;
-    e = expert_of_row(s_toff, E, mg);
-    mt = mg - s_toff[e];
+    e = expert_of_row(s_toff, E, t / n_tiles);
+    const int rt = s_toff[e + 1] - s_toff[e];              // row tiles of expert e (>= 1)
+    const int local = t - s_toff[e] * n_tiles;
+    const int band = local / (kRasterRows * n_tiles);
+    const int r0 = band * kRasterRows;
+    const int rows = min(kRasterRows, rt - r0);
+    const int r = local - r0 * n_tiles;
+    nt = r / rows;
+    mt = r0 + (r - nt * rows);
 }
 
 __device__ __forceinline__ void set_timeout(const GroupedGemm& g, volatile int* s_abort) {
