@@ -10,7 +10,8 @@
 //                 per-expert counts; the last CTA to finish (atomic ticket after
 //                 a fence; no spinning) sums them, scans them to offsets and
 //                 tile offsets and turns the per-CTA counts into each CTA's
-//                 starting position inside every expert segment.
+//                 starting position relative to every expert segment (the
+//                 scatter adds the segment's offset).
 //   route_scatter each CTA re-reads its chunk; every warp owns a contiguous
 //                 64-slot sub-chunk, so a slot's position is
 //                   CTA base[e] + earlier warps' count[e] + earlier rounds' count[e]
@@ -106,11 +107,19 @@ route_count_kernel(const IdxT* __restrict__ idx, int64_t N, int E,
     const int e = threadIdx.x;                         // E <= blockDim.x
     int run = 0;
     if (e < E) {
-        for (int b = 0; b < nb; ++b) {
-            int32_t* p = block_counts + (int64_t)b * E + e;
-            const int c = __ldcg(p);
-            *p = run;                                  // exclusive within expert e
-            run += c;
+        // exclusive prefix over the CTAs within expert e; each batch issues all its loads
+        // before its stores, so a batch costs one L2 round trip instead of one per CTA
+        constexpr int kBatch = 16;
+        for (int b0 = 0; b0 < nb; b0 += kBatch) {
+            const int nbat = min(kBatch, nb - b0);
+            int c[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) c[j] = j < nbat ? __ldcg(block_counts + (int64_t)(b0 + j) * E + e) : 0;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                if (j < nbat) block_counts[(int64_t)(b0 + j) * E + e] = run;
+                run += c[j];
+            }
         }
     }
     const int off = block_exclusive_scan(e < E ? run : 0, warp_sums, &scan_total);
@@ -118,9 +127,8 @@ route_count_kernel(const IdxT* __restrict__ idx, int64_t N, int E,
     const int toff = block_exclusive_scan(tiles, warp_sums, &scan_total);
     if (e < E) {
         counts[e] = run;
-        offsets[e] = off;
+        offsets[e] = off;                              // the scatter adds it to each CTA's base
         tile_offsets[e] = toff;
-        for (int b = 0; b < nb; ++b) block_counts[(int64_t)b * E + e] += off;   // absolute CTA base
     }
     if (e == E - 1) {
         offsets[E] = off + run;
@@ -132,7 +140,7 @@ route_count_kernel(const IdxT* __restrict__ idx, int64_t N, int E,
 template <typename IdxT>
 __global__ void __launch_bounds__(kScatterThreads)
 route_scatter_kernel(const IdxT* __restrict__ idx, const float* __restrict__ topk_w, int64_t N, int E,
-                     const int32_t* __restrict__ block_base,
+                     const int32_t* __restrict__ block_base, const int32_t* __restrict__ offsets,
                      int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm,
                      float* __restrict__ w_sorted) {
     pdl_wait();
@@ -157,7 +165,7 @@ route_scatter_kernel(const IdxT* __restrict__ idx, const float* __restrict__ top
     __syncthreads();
     // 2) exclusive scan over warps, seeded with this CTA's base inside each segment
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = block_base[(int64_t)blockIdx.x * E + e];
+        int run = offsets[e] + block_base[(int64_t)blockIdx.x * E + e];
         for (int w = 0; w < kScatterWarps; ++w) {
             const int c = wcnt[w * E + e];
             wcnt[w * E + e] = run;
@@ -205,7 +213,8 @@ cudaError_t launch_route(const void* idx, int idx_bytes, const float* topk_w, in
                        out.offsets, out.tile_offsets, dev_status);
         if (e != cudaSuccess || N == 0) return e;
         return launch_pdl(ks, dim3(nb), dim3(kScatterThreads), sm_scatter, s, ix, topk_w, N, E,
-                          (const int32_t*)block_counts, out.perm, out.inv_perm, out.w_sorted);
+                          (const int32_t*)block_counts, (const int32_t*)out.offsets, out.perm, out.inv_perm,
+                          out.w_sorted);
     };
     if (idx_bytes == 8)
         return run(route_count_kernel<long long>, route_scatter_kernel<long long>, (const long long*)idx);

@@ -87,8 +87,8 @@ def test_route_edge_cases():
                        torch.zeros((0, 2), dtype=torch.float32, device="cuda"), 5)
     torch.cuda.synchronize()
     assert rt.counts.cpu().tolist() == [0] * 5 and rt.offsets.cpu().tolist() == [0] * 6
-    # E = 1; all slots on one expert; sizes straddling the 4096-slot chunks
-    for N in (1, 4095, 4096, 4097, 3 * 4096 + 5):
+    # E = 1; all slots on one expert; sizes straddling the 1024-slot chunks
+    for N in (1, 4095, 4096, 4097, 3 * 4096 + 5, 16385, 3 * 16384 + 1023):
         idx = np.zeros((N, 1), dtype=np.int64)
         rt = moe.moe_route(torch.from_numpy(idx).cuda(), torch.ones((N, 1), device="cuda"), 1)
         torch.cuda.synchronize()
@@ -101,6 +101,27 @@ def test_route_edge_cases():
     torch.cuda.synchronize()
     counts, offsets, perm, inv = orc.route(idx, 1024)
     assert np.array_equal(rt.perm.cpu().numpy(), perm) and np.array_equal(rt.offsets.cpu().numpy(), offsets)
+
+
+@pytest.mark.parametrize("E", [7, 256, 257])
+@pytest.mark.parametrize("N", [16383, 16384, 16385])
+def test_route_around_16_chunks(N, E):
+    """Random ids with a heavy expert, at 16 chunks of 1024 slots and one slot either side,
+    for expert counts around 256: the oracle's routing bit for bit."""
+    import moe_expert_dispatch_stable_gb300 as moe
+    rng = np.random.default_rng(N + E)
+    idx = rng.integers(0, E, size=(N, 1)).astype(np.int64)
+    idx[: N // 3, 0] = E - 1                                  # a heavy expert
+    w = rng.random((N, 1)).astype(np.float32)
+    rt = moe.moe_route(torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(), E)
+    torch.cuda.synchronize()
+    counts, offsets, perm, inv = orc.route(idx, E)
+    assert np.array_equal(rt.counts.cpu().numpy(), counts)
+    assert np.array_equal(rt.offsets.cpu().numpy(), offsets)
+    assert np.array_equal(rt.tile_offsets.cpu().numpy(), orc.tile_offsets(counts, 128))
+    assert np.array_equal(rt.perm.cpu().numpy(), perm)
+    assert np.array_equal(rt.inv_perm.cpu().numpy(), inv)
+    assert np.array_equal(rt.w_sorted.cpu().numpy().view(np.uint32), w.reshape(-1)[perm].view(np.uint32))
 
 
 def test_route_out_of_range_id_sets_status_flag():
