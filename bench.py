@@ -95,8 +95,8 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
 # DRAM bytes (read + write) per launch from ncu captures of the current kernels
 # (profiles/), keyed by (workload, kernel); None where no capture of the current code exists.
 MEASURED_TRAFFIC = {
-    ("gptoss20b", "gemm_gate_up_fwd"): 1.426e9 + 0.265e9,
-    ("gptoss20b", "gemm_gate_up_bwd"): 1.480e9 + 0.179e9,
+    ("gptoss20b", "gemm_gate_up_fwd"): 1.181e9 + 0.263e9,
+    ("gptoss20b", "gemm_gate_up_bwd"): 1.322e9 + 0.178e9,
 }
 
 
@@ -306,18 +306,18 @@ def offload_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, L: int, reps: int)
     out = {"layers": L, "saved_bytes_per_layer": None}
     resident = [moe.MoELoRALayer(layer.d, layer.w, dev) for _ in range(L)]
 
+    def once(fn):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e)
+
     def timed(fn):
         fn()
         torch.cuda.synchronize()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        total = 0.0
-        for _ in range(reps):
-            s.record()
-            fn()
-            e.record()
-            torch.cuda.synchronize()
-            total += s.elapsed_time(e)
-        return total / reps
+        return statistics.median(once(fn) for _ in range(reps))
 
     def res_fwd():
         x = ts["x"]
@@ -332,14 +332,22 @@ def offload_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, L: int, reps: int)
     res_fwd()
     out["bwd_ms_resident"] = timed(res_bwd)
     del resident
-    for nb in (2, 1):
-        stack = OffloadedMoEStack(layer.d, weights, dev, buffers=nb)
-        out["saved_bytes_per_layer"] = stack.saved_bytes
-        out["h2d_bytes_per_layer"] = stack.transfer_bytes
-        stack.forward(ts["x"], routing)
-        torch.cuda.synchronize()
-        out[f"bwd_ms_{'double' if nb == 2 else 'single'}"] = timed(lambda: stack.backward(ts["dy"]))
-        del stack
+    # both stacks live at once and their repetitions alternate, so that the two reload
+    # schedules see the same host-link conditions (it is shared with other work on the host)
+    stacks = {name: OffloadedMoEStack(layer.d, weights, dev, buffers=nb) for name, nb in (("double", 2), ("single", 1))}
+    for st in stacks.values():
+        out["saved_bytes_per_layer"] = st.saved_bytes
+        out["h2d_bytes_per_layer"] = st.transfer_bytes
+        st.forward(ts["x"], routing)
+        st.backward(ts["dy"])
+    torch.cuda.synchronize()
+    samples = {name: [] for name in stacks}
+    for _ in range(reps):
+        for name, st in stacks.items():
+            samples[name].append(once(lambda: st.backward(ts["dy"])))
+    for name in stacks:
+        out[f"bwd_ms_{name}"] = statistics.median(samples[name])
+    del stacks
     torch.cuda.empty_cache()
     out["h2d_gb_per_bwd"] = L * out["h2d_bytes_per_layer"] / 1e9
     return out
