@@ -35,24 +35,31 @@ Timing& timing() {
 template <typename F>
 cudaError_t timed(const char* name, cudaStream_t s, F&& f, int n_ops = 1) {
     Timing& t = timing();
-    TimedLaunch* slot = nullptr;
+    // the event handles are copied out under the lock: another thread's push_back may move
+    // the pool's elements
+    cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
     {
         std::lock_guard<std::mutex> g(t.mu);
         t.launches += n_ops;
         if (t.on) {
             if (t.used == t.pool.size()) {
                 TimedLaunch tl{name, nullptr, nullptr};
-                if (cudaEventCreate(&tl.start) != cudaSuccess || cudaEventCreate(&tl.stop) != cudaSuccess)
+                if (cudaEventCreate(&tl.start) != cudaSuccess) return cudaErrorMemoryAllocation;
+                if (cudaEventCreate(&tl.stop) != cudaSuccess) {
+                    cudaEventDestroy(tl.start);
                     return cudaErrorMemoryAllocation;
+                }
                 t.pool.push_back(tl);
             }
-            slot = &t.pool[t.used++];
-            slot->name = name;
+            TimedLaunch& slot = t.pool[t.used++];
+            slot.name = name;
+            ev_start = slot.start;
+            ev_stop = slot.stop;
         }
     }
-    if (slot) cudaEventRecord(slot->start, s);
+    if (ev_start) cudaEventRecord(ev_start, s);
     cudaError_t e = f();
-    if (slot) cudaEventRecord(slot->stop, s);
+    if (ev_stop) cudaEventRecord(ev_stop, s);
     return e;
 }
 
