@@ -579,6 +579,16 @@ def main():
     r_bytes = {"router_topk": te + cfg.T * cfg.k * 8, "router_bwd": 2 * te + cfg.T * cfg.k * 8}
     r_ops = {"router_topk": lambda: moe.moe_router_topk(logits, cfg.k, topk_idx=r_idx, topk_w=r_w),
              "router_bwd": lambda: moe.moe_router_bwd(logits, r_idx, d_tw, d_logits=d_lg)}
+    # ---- packed-sequence metadata of the batch (samples of up to 2048 tokens: the
+    # GPT-OSS-20B-shaped workload's two packed sequences of 2048), built once per batch
+    pos = torch.cat([torch.arange(min(2048, cfg.T - b), dtype=torch.int32) for b in range(0, cfg.T, 2048)]).to(dev)
+    meta = moe.moe_packed_metadata(pos)
+    pmask = moe.moe_packed_causal_mask(meta)
+    torch.cuda.synchronize()
+    r_bytes["packed_meta"] = cfg.T * 8 + (int(meta.n_seqs.item()) + 1) * 4 + 8
+    r_bytes["packed_mask"] = cfg.T * cfg.T + cfg.T * 4
+    r_ops["packed_meta"] = lambda: moe.moe_packed_metadata(pos, out=meta)
+    r_ops["packed_mask"] = lambda: moe.moe_packed_causal_mask(meta, mask=pmask)
     line["router"] = {}
     gs = torch.cuda.Stream(dev)
     for n, op in r_ops.items():
@@ -598,6 +608,10 @@ def main():
         us = 1e3 * a.elapsed_time(b) / (20 * reps)
         line["router"][n] = {"us_per_launch": us, "gbs": r_bytes[n] / (us / 1e6) / 1e9}
         del rg
+    line["packed_metadata"] = {"T": cfg.T, "n_seqs": int(meta.n_seqs.item()),
+                               "max_seqlen": int(meta.max_seqlen.item()),
+                               "meta_us": line["router"].pop("packed_meta")["us_per_launch"],
+                               **{"mask_" + k: v for k, v in line["router"].pop("packed_mask").items()}}
     # ---- the same step with FP8 (e4m3) base weights, dequantised inside the GEMMs
     if not args.no_fp8:
         line["fp8_base"] = fp8_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, max(10, args.steps // 4), flush)

@@ -274,6 +274,37 @@ MOE_API moe_status moe_router_topk(const float* logits, int64_t T, int32_t E, in
 MOE_API moe_status moe_router_bwd(const float* logits, const int32_t* topk_idx, const float* d_topk_w,
                                   int64_t T, int32_t E, int32_t k, float* d_logits, void* stream);
 
+/* ---------------------------------------------------------------- packed-sequence metadata
+ * The "Unsloth and NVIDIA" blog post (section "core idea / structure / how it
+ * works", packed-sequence metadata caching): a packed batch concatenates several
+ * samples into one token stream, and every layer needs the samples' boundaries
+ * (cu_seqlens), the longest sample and the attention structure.  These are the
+ * same for all layers of one batch, so they are built once per batch and reused;
+ * here on the device, without copies to the host or synchronisation.  The pages
+ * do not say how a packed batch is described: read as position ids that restart
+ * at 0 at each sample, so a sample starts at token 0 and at every token whose
+ * position id is 0.
+ *  position_ids [T] int32 or int64 (pos_bytes 4 or 8), device, aligned to its width
+ *  cu_seqlens   [T+1] int32 out: entries 0..n are the samples' first tokens, then T
+ *               (entries past n are left untouched)
+ *  seq_id       [T] int32 out: the sample of each token
+ *  n_seqs       [1] int32 out: the number of samples n (0 when T = 0)
+ *  max_seqlen   [1] int32 out: the longest sample (0 when T = 0)
+ * The outputs are int32 and 4-byte aligned; 0 <= T < 2^31 - 1 (MOE_ERR_BAD_DIMS
+ * otherwise).  The caller owns every buffer; one single-CTA kernel, no workspace,
+ * enqueued on `stream`. */
+MOE_API moe_status moe_packed_metadata(const void* position_ids, int32_t pos_bytes, int64_t T,
+                                       int32_t* cu_seqlens, int32_t* seq_id, int32_t* n_seqs,
+                                       int32_t* max_seqlen, void* stream);
+
+/* The attention structure of the packed batch, as the dense block-diagonal causal
+ * mask that masked attention takes: mask[i * T + j] = 1 when tokens i and j lie in
+ * the same sample and j <= i, else 0 (uint8, row-major [T, T]; a torch.bool view).
+ * cu_seqlens and seq_id are moe_packed_metadata's outputs for the same batch.
+ * mask must be 16-byte aligned and hold T * T bytes. */
+MOE_API moe_status moe_packed_causal_mask(const int32_t* cu_seqlens, const int32_t* seq_id, int64_t T,
+                                          uint8_t* mask, void* stream);
+
 /* ---------------------------------------------------------------- diagnostics
  * Per-kernel timing.  moe_timing_enable(1) clears the record and makes every
  * later kernel launch of moe_route / moe_lora_fwd / moe_lora_bwd bracketed by

@@ -41,8 +41,9 @@ class moe_routing(ctypes.Structure):
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_launch_count", "moe_route_workspace_size", "moe_route",
             "moe_lora_fwd_sizes", "moe_lora_saved_layout", "moe_lora_saved_regather", "moe_lora_fwd",
             "moe_lora_bwd_workspace_size", "moe_lora_bwd", "moe_timing_enable", "moe_timing_read",
-            "moe_router_topk", "moe_router_bwd", "moe_quantize_fp8", "moe_lora_fwd_fp8", "moe_lora_bwd_fp8")
-ABI_VERSION = 3
+            "moe_router_topk", "moe_router_bwd", "moe_quantize_fp8", "moe_lora_fwd_fp8", "moe_lora_bwd_fp8",
+            "moe_packed_metadata", "moe_packed_causal_mask")
+ABI_VERSION = 4
 
 _lib = None
 
@@ -74,6 +75,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_lora_fwd_fp8.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 10 + [vp, sz, vp, sz, vp, vp]
     lib.moe_lora_bwd_fp8.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 10 + [sz] + [vp] * 6 + [vp, sz, vp, vp]
     lib.moe_router_bwd.argtypes = [vp, vp, vp, i64, i32, i32, vp, vp]
+    lib.moe_packed_metadata.argtypes = [vp, i32, i64, vp, vp, vp, vp, vp]
+    lib.moe_packed_causal_mask.argtypes = [vp, vp, i64, vp, vp]
     lib.moe_launch_count.restype = ctypes.c_uint64
     lib.moe_timing_enable.argtypes = [i32]
     lib.moe_timing_read.argtypes = [i32, ctypes.c_char_p, sz, P(ctypes.c_double), P(i32)]
@@ -283,6 +286,85 @@ def moe_router_topk(logits: torch.Tensor, k: int, topk_idx=None, topk_w=None, st
     _need(topk_w, "topk_w", torch.float32, (T, k))
     _check(load_library().moe_router_topk(_ptr(logits), T, E, k, _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
     return topk_idx, topk_w
+
+
+@dataclass
+class PackedMetadata:
+    """Device-side metadata of one packed batch (moe_packed_metadata); nothing here is on the host."""
+    cu_seqlens: torch.Tensor   # [T+1] int32: entries 0..n are the samples' first tokens, then T
+    seq_id: torch.Tensor       # [T] int32: the sample of each token
+    n_seqs: torch.Tensor       # [1] int32: the number of samples n
+    max_seqlen: torch.Tensor   # [1] int32: the longest sample
+    T: int
+
+
+def moe_packed_metadata(position_ids: torch.Tensor, out: PackedMetadata | None = None, stream=None) -> PackedMetadata:
+    """Samples of a packed batch from its position ids (a sample starts at token 0 and at
+    every token whose position id is 0): cu_seqlens, seq_id, n and the longest sample, built
+    on the device without a host synchronisation.  `out` (same T) reuses its buffers."""
+    if not isinstance(position_ids, torch.Tensor) or position_ids.dtype not in (torch.int32, torch.int64):
+        raise MoEError("position_ids must be an int32 or int64 torch.Tensor")
+    pos = position_ids.reshape(-1)
+    _need(pos, "position_ids", pos.dtype)
+    T = pos.numel()
+    dev = pos.device
+    if out is not None:
+        if out.T != T:
+            raise MoEError(f"out holds metadata for {out.T} tokens, position_ids has {T}")
+        cu, seq_id, n, mx = out.cu_seqlens, out.seq_id, out.n_seqs, out.max_seqlen
+    else:
+        cu = torch.empty(T + 1, dtype=torch.int32, device=dev)
+        seq_id = torch.empty(T, dtype=torch.int32, device=dev)
+        n = torch.empty(1, dtype=torch.int32, device=dev)
+        mx = torch.empty(1, dtype=torch.int32, device=dev)
+    _need(cu, "cu_seqlens", torch.int32, (T + 1,))
+    _need(seq_id, "seq_id", torch.int32, (T,))
+    _check(load_library().moe_packed_metadata(_ptr(pos), pos.element_size(), T, _ptr(cu), _ptr(seq_id), _ptr(n),
+                                              _ptr(mx), _stream(stream)))
+    return PackedMetadata(cu, seq_id, n, mx, T)
+
+
+def moe_packed_causal_mask(meta: PackedMetadata, mask=None, stream=None) -> torch.Tensor:
+    """The block-diagonal causal mask of a packed batch: mask[i, j] is True when tokens i
+    and j lie in the same sample and j <= i (bool [T, T])."""
+    T = meta.T
+    if mask is None:
+        mask = torch.empty((T, T), dtype=torch.bool, device=meta.seq_id.device)
+    _need(mask, "mask", torch.bool, (T, T))
+    _check(load_library().moe_packed_causal_mask(_ptr(meta.cu_seqlens), _ptr(meta.seq_id), T, _ptr(mask),
+                                                 _stream(stream)))
+    return mask
+
+
+class PackedBatch:
+    """Metadata of one packed batch, built once and reused by every layer.
+
+    The device tensors are built on construction; the mask on its first request; the
+    host integers (n, longest sample) on their first request, with the one host
+    synchronisation that reading them costs, once per batch instead of once per layer.
+    """
+
+    def __init__(self, position_ids: torch.Tensor, stream=None):
+        self.meta = moe_packed_metadata(position_ids, stream=stream)
+        self._stream = stream
+        self._mask = None
+        self._host = None
+
+    def causal_mask(self) -> torch.Tensor:
+        if self._mask is None:
+            self._mask = moe_packed_causal_mask(self.meta, stream=self._stream)
+        return self._mask
+
+    def host_sizes(self):
+        """(n_seqs, max_seqlen) as Python ints, read from the device once."""
+        if self._host is None:
+            both = torch.cat([self.meta.n_seqs, self.meta.max_seqlen]).cpu()
+            self._host = (int(both[0]), int(both[1]))
+        return self._host
+
+    def cu_seqlens(self) -> torch.Tensor:
+        """cu_seqlens trimmed to its n + 1 valid entries (uses host_sizes)."""
+        return self.meta.cu_seqlens[: self.host_sizes()[0] + 1]
 
 
 def moe_router_bwd(logits: torch.Tensor, topk_idx: torch.Tensor, d_topk_w: torch.Tensor, d_logits=None,

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_lora_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["route.cu", "router.cu", "rowops.cu", "quant.cu", "gemm_tc.cu", "gemm_wgrad.cu", "api.cu"]
+SOURCES = ["route.cu", "router.cu", "rowops.cu", "quant.cu", "packed.cu", "gemm_tc.cu", "gemm_wgrad.cu", "api.cu"]
 
 
 def _nvcc() -> str:

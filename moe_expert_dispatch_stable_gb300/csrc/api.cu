@@ -158,7 +158,7 @@ cudaError_t project(const void* In, int K, const void* Wt, int r, int rp, float 
 
 extern "C" {
 
-int32_t moe_abi_version(void) { return 3; }
+int32_t moe_abi_version(void) { return 4; }
 
 const char* moe_status_string(moe_status s) {
     switch (s) {
@@ -476,6 +476,32 @@ moe_status moe_router_bwd(const float* logits, const int32_t* topk_idx, const fl
         return MOE_ERR_MISALIGNED;
     return cuda_status(timed("router_bwd", (cudaStream_t)stream, [&] {
         return launch_router_bwd(logits, topk_idx, d_topk_w, T, E, k, d_logits, (cudaStream_t)stream);
+    }, T > 0 ? 1 : 0));
+}
+
+moe_status moe_packed_metadata(const void* position_ids, int32_t pos_bytes, int64_t T, int32_t* cu_seqlens,
+                               int32_t* seq_id, int32_t* n_seqs, int32_t* max_seqlen, void* stream) {
+    if (T < 0 || T >= (int64_t(1) << 31) - 1 || (pos_bytes != 4 && pos_bytes != 8)) return MOE_ERR_BAD_DIMS;
+    if (cu_seqlens == nullptr || n_seqs == nullptr || max_seqlen == nullptr) return MOE_ERR_NULL_ARG;
+    if (T > 0 && (position_ids == nullptr || seq_id == nullptr)) return MOE_ERR_NULL_ARG;
+    const uintptr_t pw = (uintptr_t)position_ids;
+    if ((pw & (uintptr_t)(pos_bytes - 1)) != 0) return MOE_ERR_MISALIGNED;
+    for (const void* p : {(const void*)cu_seqlens, (const void*)seq_id, (const void*)n_seqs, (const void*)max_seqlen})
+        if (((uintptr_t)p & 3u) != 0) return MOE_ERR_MISALIGNED;
+    return cuda_status(timed("packed_meta", (cudaStream_t)stream, [&] {
+        return launch_packed_metadata(position_ids, pos_bytes, T, cu_seqlens, seq_id, n_seqs, max_seqlen,
+                                      (cudaStream_t)stream);
+    }));
+}
+
+moe_status moe_packed_causal_mask(const int32_t* cu_seqlens, const int32_t* seq_id, int64_t T, uint8_t* mask,
+                                  void* stream) {
+    if (T < 0 || T >= (int64_t(1) << 31) - 1) return MOE_ERR_BAD_DIMS;
+    if (T > 0 && (cu_seqlens == nullptr || seq_id == nullptr || mask == nullptr)) return MOE_ERR_NULL_ARG;
+    if (((uintptr_t)cu_seqlens & 3u) != 0 || ((uintptr_t)seq_id & 3u) != 0 || !aligned16(mask))
+        return MOE_ERR_MISALIGNED;
+    return cuda_status(timed("packed_mask", (cudaStream_t)stream, [&] {
+        return launch_packed_mask(cu_seqlens, seq_id, T, mask, (cudaStream_t)stream);
     }, T > 0 ? 1 : 0));
 }
 

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.moe_abi_version() == 3
+    assert lib.moe_abi_version() == 4
     for code in range(0, 7):
         assert lib.moe_status_string(code)
 
@@ -118,6 +118,24 @@ def test_null_and_misaligned_arguments_rejected_before_launch(lib):
     assert lib.moe_router_topk(ctypes.c_void_p(20), 8, 4, 2, ctypes.c_void_p(16), ctypes.c_void_p(16), None) == 3
     assert lib.moe_router_bwd(ctypes.c_void_p(16), ctypes.c_void_p(16), None, 8, 4, 2, ctypes.c_void_p(16),
                               None) == 1
+
+
+def test_packed_metadata_host_checks(lib):
+    v = ctypes.c_void_p
+    # T out of range, bad position width
+    assert lib.moe_packed_metadata(v(16), 4, -1, v(16), v(16), v(16), v(16), None) == 2
+    assert lib.moe_packed_metadata(v(16), 4, 1 << 31, v(16), v(16), v(16), v(16), None) == 2
+    assert lib.moe_packed_metadata(v(16), 2, 8, v(16), v(16), v(16), v(16), None) == 2
+    # NULL outputs; NULL position ids with T > 0
+    assert lib.moe_packed_metadata(v(16), 4, 8, None, v(16), v(16), v(16), None) == 1
+    assert lib.moe_packed_metadata(None, 4, 8, v(16), v(16), v(16), v(16), None) == 1
+    # int64 position ids aligned to 4 only; a misaligned int32 output
+    assert lib.moe_packed_metadata(v(20), 8, 8, v(16), v(16), v(16), v(16), None) == 3
+    assert lib.moe_packed_metadata(v(16), 4, 8, v(18), v(16), v(16), v(16), None) == 3
+    # the mask: NULL, 16-byte alignment, T out of range
+    assert lib.moe_packed_causal_mask(v(16), v(16), 8, None, None) == 1
+    assert lib.moe_packed_causal_mask(v(16), v(16), 8, v(24), None) == 3
+    assert lib.moe_packed_causal_mask(v(16), v(16), -3, v(16), None) == 2
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
