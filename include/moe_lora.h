@@ -290,7 +290,7 @@ MOE_API moe_status moe_router_bwd(const float* logits, const int32_t* topk_idx, 
  *  seq_id       [T] int32 out: the sample of each token
  *  n_seqs       [1] int32 out: the number of samples n (0 when T = 0)
  *  max_seqlen   [1] int32 out: the longest sample (0 when T = 0)
- * The outputs are int32 and 4-byte aligned; 0 <= T < 2^31 - 1 (MOE_ERR_BAD_DIMS
+ * The outputs are int32 and 4-byte aligned; 0 <= T <= 2^30 (MOE_ERR_BAD_DIMS
  * otherwise).  The caller owns every buffer; one single-CTA kernel, no workspace,
  * enqueued on `stream`. */
 MOE_API moe_status moe_packed_metadata(const void* position_ids, int32_t pos_bytes, int64_t T,
@@ -301,7 +301,7 @@ MOE_API moe_status moe_packed_metadata(const void* position_ids, int32_t pos_byt
  * mask that masked attention takes: mask[i * T + j] = 1 when tokens i and j lie in
  * the same sample and j <= i, else 0 (uint8, row-major [T, T]; a torch.bool view).
  * cu_seqlens and seq_id are moe_packed_metadata's outputs for the same batch.
- * mask must be 16-byte aligned and hold T * T bytes. */
+ * mask must be 16-byte aligned and hold T * T bytes; 0 <= T <= 2^30. */
 MOE_API moe_status moe_packed_causal_mask(const int32_t* cu_seqlens, const int32_t* seq_id, int64_t T,
                                           uint8_t* mask, void* stream);
 

@@ -479,9 +479,13 @@ moe_status moe_router_bwd(const float* logits, const int32_t* topk_idx, const fl
     }, T > 0 ? 1 : 0));
 }
 
+// Packed batches of up to 2^30 tokens: the kernels' token indices (and a chunk past the
+// last token) stay within int32.
+constexpr int64_t kPackedMaxTokens = int64_t(1) << 30;
+
 moe_status moe_packed_metadata(const void* position_ids, int32_t pos_bytes, int64_t T, int32_t* cu_seqlens,
                                int32_t* seq_id, int32_t* n_seqs, int32_t* max_seqlen, void* stream) {
-    if (T < 0 || T >= (int64_t(1) << 31) - 1 || (pos_bytes != 4 && pos_bytes != 8)) return MOE_ERR_BAD_DIMS;
+    if (T < 0 || T > kPackedMaxTokens || (pos_bytes != 4 && pos_bytes != 8)) return MOE_ERR_BAD_DIMS;
     if (cu_seqlens == nullptr || n_seqs == nullptr || max_seqlen == nullptr) return MOE_ERR_NULL_ARG;
     if (T > 0 && (position_ids == nullptr || seq_id == nullptr)) return MOE_ERR_NULL_ARG;
     const uintptr_t pw = (uintptr_t)position_ids;
@@ -496,7 +500,7 @@ moe_status moe_packed_metadata(const void* position_ids, int32_t pos_bytes, int6
 
 moe_status moe_packed_causal_mask(const int32_t* cu_seqlens, const int32_t* seq_id, int64_t T, uint8_t* mask,
                                   void* stream) {
-    if (T < 0 || T >= (int64_t(1) << 31) - 1) return MOE_ERR_BAD_DIMS;
+    if (T < 0 || T > kPackedMaxTokens) return MOE_ERR_BAD_DIMS;
     if (T > 0 && (cu_seqlens == nullptr || seq_id == nullptr || mask == nullptr)) return MOE_ERR_NULL_ARG;
     if (((uintptr_t)cu_seqlens & 3u) != 0 || ((uintptr_t)seq_id & 3u) != 0 || !aligned16(mask))
         return MOE_ERR_MISALIGNED;

@@ -39,7 +39,7 @@ cudaError_t launch_router_bwd(const float* logits, const int32_t* topk_idx, cons
 // ---- packed-sequence metadata (packed.cu)
 // One CTA: a token starts a sample when it is token 0 or position_ids[t] == 0;
 // cu_seqlens[0..n] = the samples' first tokens then T, seq_id[t] = the token's sample,
-// *n_seqs = n, *max_seqlen = the longest sample.  T < 2^31 - 1.
+// *n_seqs = n, *max_seqlen = the longest sample.  T <= 2^30.
 cudaError_t launch_packed_metadata(const void* position_ids, int pos_bytes, int64_t T, int32_t* cu_seqlens,
                                    int32_t* seq_id, int32_t* n_seqs, int32_t* max_seqlen, cudaStream_t s);
 // mask[i * T + j] = (cu_seqlens[seq_id[i]] <= j <= i), uint8 [T, T] row-major; mask 16-byte aligned.

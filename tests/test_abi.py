@@ -124,7 +124,7 @@ def test_packed_metadata_host_checks(lib):
     v = ctypes.c_void_p
     # T out of range, bad position width
     assert lib.moe_packed_metadata(v(16), 4, -1, v(16), v(16), v(16), v(16), None) == 2
-    assert lib.moe_packed_metadata(v(16), 4, 1 << 31, v(16), v(16), v(16), v(16), None) == 2
+    assert lib.moe_packed_metadata(v(16), 4, (1 << 30) + 1, v(16), v(16), v(16), v(16), None) == 2
     assert lib.moe_packed_metadata(v(16), 2, 8, v(16), v(16), v(16), v(16), None) == 2
     # NULL outputs; NULL position ids with T > 0
     assert lib.moe_packed_metadata(v(16), 4, 8, None, v(16), v(16), v(16), None) == 1
