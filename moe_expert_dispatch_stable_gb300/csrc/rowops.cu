@@ -49,7 +49,9 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 // One warp per sorted row: dst[p] = src[perm[p] / k] (x k-fold, in expert order),
 // optionally scaled by the row's routing weight.  With O / d_w: the backward's
 // routing-weight gradient d_w[perm[p]] = <src row, O[p]> (the unweighted expert
-// output of the slot), accumulated in fp32 while the row is in registers.
+// output of the slot), accumulated in fp32 while the row is in registers.  Used for
+// that gradient and for rows that are not a multiple of 16 columns; every other
+// gather takes the chunked kernel below.
 __global__ void gather_rows_kernel(const uint4* __restrict__ src, int vpr, const int32_t* __restrict__ perm,
                                    const float* __restrict__ w_sorted, int64_t N, int k,
                                    uint4* __restrict__ dst, const uint4* __restrict__ O, float* __restrict__ d_w) {
