@@ -120,6 +120,31 @@ def test_null_and_misaligned_arguments_rejected_before_launch(lib):
                               None) == 1
 
 
+def test_fp8_entry_points_host_checks(lib):
+    from moe_expert_dispatch_stable_gb300 import binding as b
+    v = ctypes.c_void_p
+    # quantiser: negative sizes, NULL buffers with a non-empty tensor, misalignment
+    assert lib.moe_quantize_fp8(v(16), -1, 4, 64, v(16), v(16), None) == 2
+    assert lib.moe_quantize_fp8(None, 2, 4, 64, v(16), v(16), None) == 1
+    assert lib.moe_quantize_fp8(v(16), 2, 4, 64, v(24), v(16), None) == 3
+    rt = b.moe_routing(16, 16, 16, 16, 16, 16)
+    d = b.Dims(8, 64, 64, 4, 2, 4, 2.0).c_struct()
+    w16, a32 = v(16), v(32)
+
+    def fwd(s_gu, s_d):
+        return lib.moe_lora_fwd_fp8(ctypes.byref(d), ctypes.byref(rt), a32, w16, s_gu, w16, w16, w16, s_d, w16, w16,
+                                    a32, a32, 1 << 30, a32, 1 << 30, w16, None)
+
+    def bwd(s_gu, s_d):
+        return lib.moe_lora_bwd_fp8(ctypes.byref(d), ctypes.byref(rt), a32, w16, s_gu, w16, w16, w16, s_d, w16, w16,
+                                    a32, 1 << 30, a32, w16, w16, w16, w16, None, a32, 1 << 30, w16, None)
+
+    # the column scales are required and 16-byte aligned
+    for call in (fwd, bwd):
+        assert call(None, w16) == 1 and call(w16, None) == 1
+        assert call(v(20), w16) == 3 and call(w16, v(20)) == 3
+
+
 def test_packed_metadata_host_checks(lib):
     v = ctypes.c_void_p
     # T out of range, bad position width
