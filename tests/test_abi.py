@@ -145,6 +145,19 @@ def test_fp8_entry_points_host_checks(lib):
         assert call(v(20), w16) == 3 and call(w16, v(20)) == 3
 
 
+def test_timing_diagnostics_host_side(lib):
+    """Timing diagnostics without a launch: NULL outputs, and an index past the last name."""
+    name = ctypes.create_string_buffer(64)
+    ms, n = ctypes.c_double(), ctypes.c_int32()
+    assert lib.moe_timing_enable(1) == 0           # clears the record
+    assert lib.moe_timing_read(0, None, 64, ctypes.byref(ms), ctypes.byref(n)) == 1
+    assert lib.moe_timing_read(0, name, 0, ctypes.byref(ms), ctypes.byref(n)) == 1
+    assert lib.moe_timing_read(0, name, 64, ctypes.byref(ms), ctypes.byref(n)) == 2
+    assert lib.moe_timing_read(-1, name, 64, ctypes.byref(ms), ctypes.byref(n)) == 2
+    assert lib.moe_timing_enable(0) == 0
+    assert lib.moe_launch_count() >= 0
+
+
 def test_packed_metadata_host_checks(lib):
     v = ctypes.c_void_p
     # T out of range, bad position width
