@@ -19,8 +19,16 @@ unless --config says otherwise.  Prints ONE JSON line (rank 0).
   graph_ms_per_step  the same step replayed from a captured CUDA graph (launch
                gaps removed), for information
   gemm         all grouped-GEMM kernels together: algorithmic TFLOP/s and the
-               fraction of the measured dense bf16 peak
-  cpu_baseline the CPU oracle timed on a bounded token sample (rank 0, N=1)
+               fraction of the measured dense bf16 peak (the burst figure when the
+               median SM clock of the run stayed within 5 % of its maximum, else the
+               sustained one; the other is kept beside it)
+  other_configs  the Qwen3-30B-A3B, skewed GPT-OSS-120B and DeepSeek-V3 shapes, a
+               short run each (10 steps): ms/step, tokens/s, grouped-GEMM TFLOP/s,
+               the dominant kernel against its roofline, the routing histogram, and
+               the FP8-base step of the DeepSeek-V3 shape
+  cpu_baseline the CPU oracle timed on a bounded token sample (rank 0, N=1): route,
+               forward and backward separately, the threads used, and the tiny layer
+               on one thread
 
 --impl reference times the CPU oracle (the only reference this layer has) on
 the host cores, on bounded token samples of the same workload.
@@ -116,6 +124,17 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def tensor_peak(peaks: dict, clk: dict) -> tuple[float, str]:
+    """Dense bf16 peak to hold a kernel against: the burst figure (a short GEMM at full
+    clock) when the run's median SM clock under load stayed within 5 % of the maximum, as
+    it does for the few-millisecond steps timed here; the sustained figure (a seconds-long
+    GEMM loop that settles under the power cap) otherwise."""
+    mhz, mx = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    if mhz is not None and mx and mhz >= 0.95 * mx:
+        return peaks["bf16_tflops"], f"{peaks['source']} bf16 burst (median SM clock {mhz:.0f} of {mx:.0f} MHz)"
+    return peaks["bf16_tflops_sustained"], f"{peaks['source']} bf16 sustained (median SM clock {mhz} of {mx} MHz)"
+
+
 # ----------------------------------------------------------------------------- ranks
 def max_over_ranks(value: float, device=None) -> float:
     """Largest `value` over all ranks (identity without torch.distributed): the job's
@@ -189,16 +208,60 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
-def oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, S: int) -> float:
+def oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, S: int, parts: dict | None = None) -> float:
     """Route the full batch and run forward + backward of the oracle on the first
-    S tokens as a batch of their own; returns seconds."""
+    S tokens as a batch of their own; returns seconds (and, in `parts`, the seconds
+    of the route, the forward and the backward)."""
     from oracle import moe_oracle as orc
     t0 = time.perf_counter()
     orc.route(idx, cfg.E)
+    t1 = time.perf_counter()
     sub_idx, sub_w = idx[:S], w[:S]
     orc.lora_fwd(x_cpu[:S], sub_idx, sub_w, *wts_cpu, cfg.scale)
+    t2 = time.perf_counter()
     orc.lora_bwd(dy_cpu[:S], x_cpu[:S], sub_idx, sub_w, *wts_cpu, cfg.scale)
-    return time.perf_counter() - t0
+    t3 = time.perf_counter()
+    if parts is not None:
+        parts.update(route_s=t1 - t0, fwd_s=t2 - t1, bwd_s=t3 - t2)
+    return t3 - t0
+
+
+def oracle_threads() -> dict:
+    """Threads the oracle runs on: numpy's BLAS (its float64 matmuls) and torch's
+    intra-op pool (the bf16 -> float64 conversions)."""
+    import torch
+    out = {"torch_threads": torch.get_num_threads(), "blas_threads": None}
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        out["blas_threads"] = max(n) if n else None
+    except ImportError:
+        env = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+        out["blas_threads"] = int(env) if env else os.cpu_count()
+    return out
+
+
+def tiny_oracle_one_thread(seed: int = 0, reps: int = 5) -> dict:
+    """The tiny layer (T = 64) through the oracle in a child process pinned to one
+    thread (BLAS and torch): median seconds of route, forward and backward."""
+    code = (
+        "import json,os,sys,time,statistics;sys.path.insert(0,%r);import torch;torch.set_num_threads(1);"
+        "import moe_inputs as mi;from oracle import moe_oracle as orc;cfg=mi.CONFIGS['tiny'];"
+        "idx,w=mi.make_routing(cfg,%d);ts=mi.make_tensors(cfg,%d,'cpu');"
+        "wts=[ts[n] for n in ('W_gu','A_gu','B_gu','W_d','A_d','B_d')];r=[]\n"
+        "for _ in range(%d):\n"
+        " t0=time.perf_counter();orc.route(idx,cfg.E);t1=time.perf_counter();"
+        "orc.lora_fwd(ts['x'],idx,w,*wts,cfg.scale);t2=time.perf_counter();"
+        "orc.lora_bwd(ts['dy'],ts['x'],idx,w,*wts,cfg.scale);t3=time.perf_counter();r.append((t1-t0,t2-t1,t3-t2))\n"
+        "m=[statistics.median(v) for v in zip(*r)];"
+        "print(json.dumps({'route_s':m[0],'fwd_s':m[1],'bwd_s':m[2],'tokens_per_s':cfg.T/sum(m)}))"
+    ) % (ROOT, seed, seed, reps)
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=300)
+        return json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else {"error": r.stderr[-300:]}
+    except (subprocess.TimeoutExpired, IndexError, ValueError) as exc:
+        return {"error": str(exc)}
 
 
 def cpu_baseline(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, budget_s: float = 25.0) -> dict:
@@ -208,10 +271,14 @@ def cpu_baseline(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, budget_s: float = 25.0) ->
     t8 = oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, 8)
     slope = max((t8 - t2) / 6.0, 1e-6)
     S = int(max(8, min(cfg.T, 8 + (budget_s - t8) / slope)))
-    t = oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, S)
-    return {"value": S / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+    parts = {}
+    t = oracle_sample_step(cfg, idx, w, x_cpu, dy_cpu, wts_cpu, S, parts)
+    return {"value": S / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", **oracle_threads(),
             "sample": f"route of all {cfg.T} tokens + fp64 forward and backward of the first {S} tokens "
-                      f"as a batch ({t:.1f} s)"}
+                      f"as a batch ({t:.1f} s)",
+            "route_s": parts["route_s"], "fwd_s": parts["fwd_s"], "bwd_s": parts["bwd_s"],
+            "route_tokens_per_s": cfg.T / parts["route_s"], "fwd_bwd_tokens_per_s": S / (parts["fwd_s"] + parts["bwd_s"]),
+            "tiny_layer_1_thread": tiny_oracle_one_thread()}
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -353,6 +420,74 @@ def offload_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, L: int, reps: int)
     return out
 
 
+# ----------------------------------------------------------------------------- the other workloads
+def workload_measurement(name: str, moe, dev, flush, steps: int, peaks: dict, seed: int, fp8: bool) -> dict:
+    """A short run of another workload on the same line: route + fwd + bwd per step
+    (CUDA events around each step, L2 flushed between steps), its grouped GEMMs against
+    the dense bf16 peak, the dominant kernel against its roofline, and, with `fp8`, the
+    same step with FP8 base weights.  The clocks of the main run decide burst or
+    sustained peak; this short run sits right after it."""
+    import torch
+    cfg = mi.CONFIGS[name]
+    idx, w = mi.make_routing(cfg, seed)
+    ts = mi.make_tensors(cfg, seed, dev)
+    layer = moe.MoELoRALayer(moe.Dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r, cfg.scale), ts, dev)
+    t_idx, t_w = torch.from_numpy(idx).to(dev), torch.from_numpy(w).to(dev)
+
+    def run(lay, timing: bool):
+        for _ in range(3):
+            lay.step(t_idx, t_w, ts["x"], ts["dy"], with_topk_grad=False)
+        torch.cuda.synchronize()
+        if timing:
+            moe.moe_timing_enable(True)
+        ms = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            lay.step(t_idx, t_w, ts["x"], ts["dy"], with_topk_grad=False)
+            b.record()
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        if timing:
+            moe.moe_timing_enable(False)
+        assert int(lay.dev_status.item()) == 0, f"device status flag set ({name})"
+        return sum(ms) / steps, (moe.moe_timing_read() if timing else None)
+
+    step_ms, _ = run(layer, False)
+    _, kt = run(layer, True)
+    work = kernel_work(cfg)
+    g_ms = sum(kt[n][0] for n in GEMM_KERNELS if n in kt) / steps
+    g_fl = sum(work[n]["flops"] for n in GEMM_KERNELS)
+    dom = max(kt, key=lambda n: kt[n][0])
+    d_ms = kt[dom][0] / kt[dom][1]
+    out = {"workload": config_dict(cfg)["workload"], "steps": steps, "ms_per_step": step_ms,
+           "tokens_per_s": cfg.T / (step_ms / 1e3),
+           "layer_tflops": step_flops(cfg) / (step_ms / 1e3) / 1e12,
+           "gemm": {"ms_per_step": g_ms, "tflops": g_fl / (g_ms / 1e3) / 1e12,
+                    "frac_of_bf16_burst": g_fl / (g_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                    "frac_of_bf16_sustained": g_fl / (g_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"]},
+           "dominant_kernel": {"kernel": dom, "ms_per_launch": d_ms, "bound": work[dom]["bound"],
+                               "hbm_gbs": work[dom]["bytes"] / (d_ms / 1e3) / 1e9,
+                               "frac_of_hbm": work[dom]["bytes"] / (d_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                               "tflops": work[dom]["flops"] / (d_ms / 1e3) / 1e12,
+                               "frac_of_bf16_burst": work[dom]["flops"] / (d_ms / 1e3) / 1e12 / peaks["bf16_tflops"]},
+           "kernels_ms_per_step": {n: round(v[0] / steps, 4) for n, v in sorted(kt.items(), key=lambda kv: -kv[1][0])},
+           "routing": routing_summary(idx, cfg.E)}
+    if fp8:
+        wq = moe.quantize_expert_weights(layer.w)
+        q8 = moe.MoELoRALayer(layer.d, wq, dev)
+        f_ms, f_kt = run(q8, True)
+        out["fp8_base"] = {"ms_per_step": f_ms, "tokens_per_s": cfg.T / (f_ms / 1e3),
+                           "gemm_ms_per_step": sum(f_kt[n][0] for n in GEMM_KERNELS if n in f_kt) / steps,
+                           "gemm_kernels_ms_per_step": {n: round(f_kt[n][0] / steps, 4) for n in GEMM_KERNELS
+                                                        if n in f_kt}}
+        del q8, wq
+    del layer, ts
+    torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -367,6 +502,11 @@ def main():
     ap.add_argument("--no-offload", action="store_true", help="skip the offloaded-stack measurement")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-base-weight measurement")
     ap.add_argument("--offload-layers", type=int, default=4)
+    ap.add_argument("--other-steps", type=int, default=10,
+                    help="timed steps of each other workload on the line (0: none)")
+    ap.add_argument("--steps-only", action="store_true",
+                    help="run the warm-up and timed steps of the layer, print the line's step time and exit "
+                         "(a short command for profilers)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = mi.CONFIGS[args.config]
@@ -431,6 +571,15 @@ def main():
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = max_over_ranks(sum(step_ms), dev)
     value = job_throughput(cfg.T, args.steps, world, total_ms)
+    if args.steps_only:
+        clocks.stop()
+        assert int(layer.dev_status.item()) == 0, "device status flag set"
+        if rank == 0:
+            print(json.dumps({"steps_only": True, "config": config_dict(cfg), "ms_per_step": total_ms / args.steps,
+                              "value": value, "unit": UNIT}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     # ---- per-kernel durations: a second timed pass of the same steps with the library's
     # CUDA events around each of its launches (on the caller's stream); they add ~2 % to
@@ -527,13 +676,15 @@ def main():
     dom = max(kt, key=lambda n: kt[n][0])
     ms_launch = kt[dom][0] / kt[dom][1]
     wk = work[dom]
+    t_peak, t_src = tensor_peak(peaks, clk)
     if wk["bound"] == "tensor":
         ach = wk["flops"] / (ms_launch / 1e3) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"],
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": t_peak,
+                "unit": "TFLOP/s", "frac": ach / t_peak,
+                "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
                 "traffic": MEASURED_TRAFFIC.get((cfg.name, dom)),
                 "algorithmic_flops_per_launch": wk["flops"], "ms_per_launch": ms_launch,
-                "peak_source": f"{peaks['source']} bf16 sustained"}
+                "sm_mhz_median": clk.get("sm_mhz"), "peak_source": t_src}
     else:
         ach = wk["bytes"] / (ms_launch / 1e3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -543,8 +694,8 @@ def main():
     g_ms = sum(kt[n][0] for n in GEMM_KERNELS if n in kt) / args.steps
     g_fl = sum(work[n]["flops"] for n in GEMM_KERNELS)
     g_tf = g_fl / (g_ms / 1e3) / 1e12 if g_ms > 0 else 0.0
-    gemm = {"tflops": g_tf, "frac_of_bf16_peak": g_tf / peaks["bf16_tflops_sustained"],
-            "peak": peaks["bf16_tflops_sustained"], "ms_per_step": g_ms, "flops_per_step": g_fl}
+    gemm = {"tflops": g_tf, "frac_of_bf16_peak": g_tf / t_peak, "peak": t_peak, "peak_source": t_src,
+            "frac_of_sustained": g_tf / peaks["bf16_tflops_sustained"], "ms_per_step": g_ms, "flops_per_step": g_fl}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -620,6 +771,13 @@ def main():
     if not args.no_offload:
         line["offload"] = offload_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, args.offload_layers,
                                               max(3, args.steps // 20))
+    # ---- the other workload shapes, a short run each (rank 0 of a single-GPU run)
+    if rank == 0 and world == 1 and args.other_steps > 0:
+        line["other_configs"] = {}
+        for name in ("qwen3_30b", "gptoss120b_skew", "dsv3"):
+            if name != cfg.name:
+                line["other_configs"][name] = workload_measurement(name, moe, dev, flush, args.other_steps, peaks,
+                                                                   args.seed, fp8=not args.no_fp8 and name == "dsv3")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         wts = [ts[n].cpu() for n in ("W_gu", "A_gu", "B_gu", "W_d", "A_d", "B_d")]
         line["cpu_baseline"] = cpu_baseline(cfg, idx, w, ts["x"].cpu(), ts["dy"].cpu(), wts)

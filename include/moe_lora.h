@@ -37,7 +37,8 @@
  *    the caller zeroes and reads when it wants): MOE_DEV_BAD_EXPERT_ID for an
  *    expert id outside [0, E), MOE_DEV_TIMEOUT when a bounded wait inside a
  *    kernel gave up.  When a bit is set the outputs are unspecified.
- *  - No function blocks the host; all of them can be captured in a CUDA graph.
+ *  - No function blocks the host.  moe_route, moe_lora_fwd, moe_lora_bwd (and the
+ *    _fp8 forms) can be captured in a CUDA graph.
  *
  * Sizes supported: 1 <= k <= E <= 1024, H and I multiples of 64, 1 <= r <= 64,
  * T >= 0 and T*k < 2^31.
@@ -125,23 +126,28 @@ MOE_API moe_status moe_route(const void* topk_idx, int32_t idx_bytes, const floa
 /* Routing for callers that cannot allocate device memory.
  *
  * No passage of the pages has a counterpart to this entry point: it exists for
- * callers of this library that cannot call cudaMalloc -- code running while a
- * stream is being captured into a CUDA graph (allocation is not allowed there),
- * hosts whose device memory is entirely owned by another allocator or a fixed
- * pool, and latency-critical loops where an allocation could synchronise the
- * device.  Such a caller still passes every input and output, but no workspace.
+ * callers of this library that cannot call cudaMalloc -- hosts whose device
+ * memory is entirely owned by another allocator or a fixed pool (a framework's
+ * caching allocator that must account for every byte, an embedded runtime with a
+ * fixed arena), and latency-critical loops where an allocation could synchronise
+ * the device.  Such a caller still passes every input and output, but no
+ * workspace.
  *
  * It computes exactly what moe_route computes (same kernels, bit-identical
  * outputs); the routing scratch lives instead in one file-scope device array of
  * MOE_ROUTE_STATIC_SCRATCH_BYTES that every GPU loading the library holds until
  * the process exits.  The call needs moe_route_workspace_size(T, k, E) <=
- * MOE_ROUTE_STATIC_SCRATCH_BYTES, i.e. ceil(T*k / 1024) * E * 4 + 512 bytes at
- * most (for example T*k <= 64512 slots at E = 1024, or T*k <= 523264 at
- * E = 128); larger sizes return MOE_ERR_WORKSPACE and launch nothing.
+ * MOE_ROUTE_STATIC_SCRATCH_BYTES; that size is exactly
+ * align_up(ceil(T*k / 1024) * E * 4, 256) + 256 bytes (for example T*k <= 64512
+ * slots at E = 1024, or T*k <= 523264 at E = 128).  Larger sizes return
+ * MOE_ERR_WORKSPACE and launch nothing.
  *
  * The first call on a device looks up the array's device address (once per
- * device, with that device current): make that first call before any stream
- * capture.  The call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * device, with that device current) and keeps it for the life of the process:
+ * make that first call before any stream capture.  A device reset
+ * (cudaDeviceReset, or destroying and re-creating the primary context) leaves
+ * the kept address stale, so a process that resets a device must not call
+ * moe_route_static on it again.  The call allocates nothing (no cudaMalloc, cudaFree or allocating
  * library routine) and clears the part of the array that must start at zero on
  * every call.  All calls share the array, so calls whose kernels overlap on the
  * GPU (several streams, or several host threads) race: serialise them. */

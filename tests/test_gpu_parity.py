@@ -1,10 +1,9 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
 
 Routing is compared bit for bit; outputs and gradients within rel-L2 <= 5e-3
-and max-abs <= 2e-2 * max|oracle|.  Small layers are compared element by
-element in full; the five workload shapes at full size are compared on
-sampled tokens (y, dx) and sampled experts (LoRA gradients), which the oracle
-computes exactly per token / per expert.
+and max-abs <= 2e-2 * max|oracle|.  Small layers and the four large workload
+shapes at full size are compared element by element in full: y and dx on every
+token, the LoRA gradients on every expert (and per expert).
 """
 import numpy as np
 import pytest
@@ -288,31 +287,36 @@ def test_graph_capture_route_fwd_bwd():
         assert torch.equal(a, b)
 
 
-# ------------------------------------------------------------------ full-size workloads, sampled
+# ------------------------------------------------------------------ full-size workloads, every element
 FULL = ["gptoss20b", "qwen3_30b", "gptoss120b_skew", "dsv3"]
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_parity_sampled(name):
+def test_full_size_parity(name):
+    """The four large workloads at full size, compared with the fp64 oracle element by
+    element: y and dx on every token, and dA_gu, dB_gu, dA_d, dB_d on every expert (each
+    non-empty expert within the bound on its own, so an error confined to one expert --
+    a band or wave boundary of the tile order, a half tile, one hot expert of the skewed
+    router -- cannot hide in the whole-tensor norm), exact zeros for empty experts."""
     cfg = mi.CONFIGS[name]
     idx, w, ts = make_case(cfg, seed=0)
     layer, grads = run_layer(cfg, idx, w, ts)
     assert int(layer.dev_status.item()) == 0
     counts, _ = _check_route(layer, idx, cfg.E)
-    rng = np.random.default_rng(0)
-    n_tok = 16 if cfg.H * cfg.I > 10_000_000 else 32
-    toks = np.sort(rng.choice(cfg.T, n_tok, replace=False))
-    nz = np.where(counts > 0)[0]
-    experts = sorted({int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])]), int(rng.choice(nz))})
     lazy = {n: LazyExperts(ts[n]) for n in WEIGHT_NAMES}
     x = ts["x"].cpu(); dy = ts["dy"].cpu()
     wts = [lazy[n] for n in WEIGHT_NAMES]
-    y_ref = orc.lora_fwd(x, idx, w, *wts, cfg.scale, token_subset=toks)
-    assert_close("y[sample]", to64(layer.y)[toks], y_ref[toks])
-    g_ref = orc.lora_bwd(dy, x, idx, w, *wts, cfg.scale, token_subset=toks, expert_subset=experts)
-    assert_close("dx[sample]", to64(grads[0])[toks], g_ref[0][toks])
+    y_ref = orc.lora_fwd(x, idx, w, *wts, cfg.scale)
+    assert_close("y", to64(layer.y), y_ref)
+    del y_ref
+    g_ref = orc.lora_bwd(dy, x, idx, w, *wts, cfg.scale)
+    assert_close("dx", to64(grads[0]), g_ref[0])
+    nz = np.where(counts > 0)[0]
     for nm, got, ref in zip(["dA_gu", "dB_gu", "dA_d", "dB_d"], grads[1:], g_ref[1:]):
-        assert_close(f"{nm}[{experts}]", to64(got[experts]), ref[experts])
+        got = to64(got)
+        assert_close(nm, got, ref)
+        for e in nz:
+            assert_close(f"{nm}[expert {e}, {counts[e]} rows]", got[e], ref[e])
     for e in np.where(counts == 0)[0]:
         for got in grads[1:]:
             assert torch.count_nonzero(got[e]).item() == 0

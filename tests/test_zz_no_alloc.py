@@ -1,15 +1,14 @@
 """moe_route_static: routing for callers that cannot allocate device memory.
 
-Some callers of this library cannot call cudaMalloc: code that runs while a
-stream is being captured into a CUDA graph, hosts whose device memory belongs
-to another allocator or a fixed pool, and latency-critical loops where an
-allocation might synchronise the device.  moe_route_static serves them: it
+Some callers of this library cannot call cudaMalloc: hosts whose device memory
+belongs to another allocator or a fixed pool, and latency-critical loops where
+an allocation might synchronise the device.  moe_route_static serves them: it
 takes no workspace and keeps its scratch in a fixed device array inside the
 library.  This test calls it through the C ABI (ctypes on the shared library)
 twice in a row, with different sizes, and checks that each call's outputs are
 bit-identical to those of moe_route, the entry point with a caller-provided
-workspace (routing parity in this project is bit-exact).  It is collected last
-and also runs on its own in a fresh process.
+workspace (routing parity in this project is bit-exact).  It is collected last,
+so that a run stopping at its first failure has run every other test before it.
 """
 import ctypes
 
