@@ -328,6 +328,20 @@ MOE_API moe_status moe_timing_read(int32_t index, char* name, size_t name_len,
  * library has issued since it was loaded, counted on the host. */
 MOE_API uint64_t moe_launch_count(void);
 
+/* Failure-path test hook.  Every mbarrier wait inside the tensor-core kernels is
+ * bounded (2 s); a wait that runs out sets MOE_DEV_TIMEOUT in *dev_status, the
+ * kernel stops issuing work, waits (again bounded by 2 s) until the copies and
+ * MMAs it already issued have landed, frees its TMEM and returns, so the context
+ * stays usable.  This call makes that happen on purpose: the launch_index-th
+ * (0-based) launch from now of a single-CTA tensor-core kernel -- a grouped GEMM
+ * on single-CTA tiles, a rank-r projection or a LoRA reduction; SM-pair launches
+ * are not counted -- bounds its ordinary waits by limit_ns and has its epilogue
+ * warps first wait on an mbarrier that nothing arrives on, so those waits run
+ * out.  The outputs of the call that contains that launch are unspecified; the
+ * next calls are unaffected.  limit_ns in [1000, 2e9] (MOE_ERR_BAD_DIMS
+ * otherwise); launch_index < 0 disarms.  Counted on the host, process-wide. */
+MOE_API moe_status moe_diag_force_timeout(int32_t launch_index, uint64_t limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,8 +42,8 @@ EXPORTED = ("moe_abi_version", "moe_status_string", "moe_launch_count", "moe_rou
             "moe_lora_fwd_sizes", "moe_lora_saved_layout", "moe_lora_saved_regather", "moe_lora_fwd",
             "moe_lora_bwd_workspace_size", "moe_lora_bwd", "moe_timing_enable", "moe_timing_read",
             "moe_router_topk", "moe_router_bwd", "moe_quantize_fp8", "moe_lora_fwd_fp8", "moe_lora_bwd_fp8",
-            "moe_packed_metadata", "moe_packed_causal_mask")
-ABI_VERSION = 4
+            "moe_packed_metadata", "moe_packed_causal_mask", "moe_diag_force_timeout")
+ABI_VERSION = 5
 
 _lib = None
 
@@ -80,6 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_launch_count.restype = ctypes.c_uint64
     lib.moe_timing_enable.argtypes = [i32]
     lib.moe_timing_read.argtypes = [i32, ctypes.c_char_p, sz, P(ctypes.c_double), P(i32)]
+    lib.moe_diag_force_timeout.argtypes = [i32, ctypes.c_uint64]
     for name in EXPORTED[3:]:
         getattr(lib, name).restype = i32
     if lib.moe_abi_version() != ABI_VERSION:
@@ -442,6 +443,12 @@ def moe_lora_bwd_fp8(d: Dims, rt: Routing, dy, w: dict, saved, dx, grads, worksp
 def moe_launch_count() -> int:
     """Launch operations the library has issued so far (host-side count)."""
     return int(load_library().moe_launch_count())
+
+
+def moe_diag_force_timeout(launch_index: int, limit_ns: int = 1_000_000) -> None:
+    """Make the launch_index-th single-CTA tensor-core launch from now give up its waits
+    (failure-path test hook of the C ABI; launch_index < 0 disarms)."""
+    _check(load_library().moe_diag_force_timeout(int(launch_index), int(limit_ns)))
 
 
 def moe_timing_enable(on: bool) -> None:

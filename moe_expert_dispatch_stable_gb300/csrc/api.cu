@@ -4,13 +4,28 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <atomic>
 #include <mutex>
 #include <string.h>
 #include <vector>
 
+#include "tc_ptx.cuh"
+
 using namespace moe;
 
 namespace {
+
+// ---- diagnostics: a chosen single-CTA tensor-core launch fails on purpose
+struct ForcedTimeout {
+    std::atomic<int64_t> target{-1};      // index of the launch to fail among those counted, -1: none
+    std::atomic<int64_t> seen{0};         // single-CTA tensor-core launches counted since arming
+    std::atomic<uint64_t> limit_ns{tc::kWaitTimeoutNs};
+};
+
+ForcedTimeout& forced() {
+    static ForcedTimeout f;
+    return f;
+}
 
 // ---- diagnostics: per-kernel CUDA-event timing and a launch counter
 struct TimedLaunch {
@@ -156,9 +171,19 @@ cudaError_t project(const void* In, int K, const void* Wt, int r, int rp, float 
 
 }  // namespace
 
+DiagWait moe::diag_next_single_cta_launch() {
+    ForcedTimeout& f = forced();
+    const int64_t target = f.target.load();
+    if (target >= 0 && f.seen.fetch_add(1) == target) {
+        int64_t expect = target;
+        if (f.target.compare_exchange_strong(expect, -1)) return DiagWait{f.limit_ns.load(), true};
+    }
+    return DiagWait{tc::kWaitTimeoutNs, false};
+}
+
 extern "C" {
 
-int32_t moe_abi_version(void) { return 4; }
+int32_t moe_abi_version(void) { return 5; }
 
 const char* moe_status_string(moe_status s) {
     switch (s) {
@@ -507,6 +532,20 @@ moe_status moe_packed_causal_mask(const int32_t* cu_seqlens, const int32_t* seq_
     return cuda_status(timed("packed_mask", (cudaStream_t)stream, [&] {
         return launch_packed_mask(cu_seqlens, seq_id, T, mask, (cudaStream_t)stream);
     }, T > 0 ? 1 : 0));
+}
+
+moe_status moe_diag_force_timeout(int32_t launch_index, uint64_t limit_ns) {
+    ForcedTimeout& f = forced();
+    if (launch_index < 0) {
+        f.target.store(-1);
+        return MOE_OK;
+    }
+    if (limit_ns < 1000 || limit_ns > tc::kWaitTimeoutNs) return MOE_ERR_BAD_DIMS;
+    f.target.store(-1);
+    f.limit_ns.store(limit_ns);
+    f.seen.store(0);
+    f.target.store(launch_index);
+    return MOE_OK;
 }
 
 moe_status moe_timing_enable(int32_t on) {

@@ -82,6 +82,8 @@ struct TcParams {
     int a2_bytes;       // bytes of the A2 tile
     int b2_box_bytes;   // bytes of one B2 box (64 columns x RP rows)
     uint32_t a2_sbo, a2_swz;
+    uint64_t wait_ns;   // limit of the ordinary bounded waits
+    int stall;          // diagnostics: the epilogue first waits on a barrier nothing arrives on
 };
 
 // Tile order: expert by expert; inside an expert, bands of kRasterRows row tiles, and in a
@@ -243,10 +245,16 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
     uint64_t* tfull_bar = empty_bar + kStages;
     uint64_t* tempty_bar = tfull_bar + 2;
     uint64_t* staged_bar = tempty_bar + 2;          // FP8 codes landed in the staging slot
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(staged_bar + kStages);
+    uint64_t* drain_bar = staged_bar + kStages;     // after an abort: the MMA issuer's last commit
+    uint64_t* stall_bar = drain_bar + 1;            // diagnostics: nothing ever arrives on it
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stall_bar + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     uint32_t* sig_slot = tmem_slot + 2;             // FP8 pairs: target of the peer's stage signals
-    int32_t* s_off = reinterpret_cast<int32_t*>(tmem_slot + 4);
+    // what the roles issued, read by the abort drain: [0] the producer's stage fills,
+    // [1 + g] the stages converter group g signalled (FP8)
+    volatile int* s_issued = reinterpret_cast<volatile int*>(tmem_slot + 4);
+    int32_t* s_off = reinterpret_cast<int32_t*>(tmem_slot + 8);
+    static_assert((3 * kStages + 6) * 8 + 32 <= 256, "barriers and flags fit the 256-byte tail");
     const GroupedGemm& g = P.g;
     const int E = g.E;
     int32_t* s_toff = s_off + (E + 1);
@@ -273,7 +281,10 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             tc::mbar_init(tc::smem_u32(&tfull_bar[a]), 1);
             tc::mbar_init(tc::smem_u32(&tempty_bar[a]), PAIR ? 2 * kEpiWarps : kEpiWarps);
         }
+        tc::mbar_init(tc::smem_u32(drain_bar), 1);
+        tc::mbar_init(tc::smem_u32(stall_bar), 1);
         *s_abort = 0;
+        for (int i = 0; i < 1 + kConvGroups; ++i) s_issued[i] = 0;
         tc::fence_mbar_init();
     }
     if constexpr (PAIR) {
@@ -321,6 +332,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     const int total_tiles = s_toff[E] * P.n_tiles;
+    const uint64_t lim = P.wait_ns;
+    int fills = 0;                                  // the producer's stage fills (lane 0 of warp 0)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -338,7 +351,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 const int a2_bytes = half ? P.a2_bytes / 2 : P.a2_bytes;
                 const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : P.num_kb + (P.lora_k16 ? 1 : 0);
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!tc::mbar_wait(tc::smem_u32(&empty_bar[stage]), phase ^ 1)) {
+                    if (!tc::mbar_wait(tc::smem_u32(&empty_bar[stage]), phase ^ 1, lim)) {
                         set_timeout(g, s_abort);
                         break;
                     }
@@ -374,7 +387,11 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                                 tc::tma_load_3d_pair(sb, &P.tm_b, fb, kb * BK, nt * BN + (int)rank * (BN / 2), e);
                             }
                         } else {
-                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * (a2_bytes + 2 * P.b2_box_bytes));
+                            if (rank == 0) {
+                                tc::mbar_arrive_expect_tx(fb_local, 2 * (a2_bytes + 2 * P.b2_box_bytes));
+                                // FP8: the LoRA step needs no conversion; the producer makes both arrivals
+                                if (Q8) tc::mbar_arrive(fb_local);
+                            }
                             tc::tma_load_2d_pair(sa, tma2, fb, 0, m0);
 #pragma unroll
                             for (int jj = 0; jj < 2; ++jj)
@@ -420,6 +437,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                             }
                         } else {
                             tc::mbar_arrive_expect_tx(fb, P.a2_bytes + 4 * P.b2_box_bytes);
+                            if (Q8) tc::mbar_arrive(fb);     // FP8: no conversion, both arrivals here
                             tc::tma_load_2d(sa, &P.tm_a2, fb, 0, m0);
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
@@ -427,12 +445,14 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                                                 0, e);
                         }
                     }
+                    ++fills;
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
+            s_issued[0] = fills;
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader only for pairs)
@@ -448,7 +468,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             for (int t = tile0; t < total_tiles && !*s_abort; t += tile_step, ++it) {
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
-                if (!tc::mbar_wait(tc::smem_u32(&tempty_bar[acc]), acc_phase ^ 1)) {
+                if (!tc::mbar_wait(tc::smem_u32(&tempty_bar[acc]), acc_phase ^ 1, lim)) {
                     set_timeout(g, s_abort);
                     break;
                 }
@@ -466,7 +486,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb) {
                     // FP8 pairs: the peer's converted half is published by a cluster-scope release
-                    if (!tc::mbar_wait<Q8 && PAIR>(tc::smem_u32(&full_bar[stage]), phase)) {
+                    if (!tc::mbar_wait<Q8 && PAIR>(tc::smem_u32(&full_bar[stage]), phase, lim)) {
                         set_timeout(g, s_abort);
                         ok = false;
                         break;
@@ -535,6 +555,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             const uint32_t sig_leader = PAIR ? tc::mapa(tc::smem_u32(sig_slot), 0) : 0u;
             int stage = 0;
             uint32_t sbits = 0;                                     // per-stage parity of staged_bar
+            int done = 0;                                           // stages this group has signalled
             bool ok = true;
             uint32_t fm[kBoxes][4];                                 // multipliers of this thread's chunks
             bool big[kBoxes];
@@ -567,7 +588,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                             ka = __ldg(reinterpret_cast<const float4*>(se + kb * BK + cc * 8));
                             kb4 = __ldg(reinterpret_cast<const float4*>(se + kb * BK + cc * 8) + 1);
                         }
-                        const bool got = tc::mbar_wait(tc::smem_u32(&staged_bar[stage]), (sbits >> stage) & 1u);
+                        const bool got = tc::mbar_wait(tc::smem_u32(&staged_bar[stage]), (sbits >> stage) & 1u, lim);
                         if (!tc::named_bar_and(1 + grp, kGT, got && !*s_abort)) {
                             if (gt == 0) set_timeout(g, s_abort);
                             ok = false;
@@ -600,21 +621,24 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                         }
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     }
-                    if (mine) {
-                        // one signal per group and stage, after every thread's writes and proxy fence:
-                        // a CTA-scope arrive on this CTA's full barrier, or from the peer of a pair an
-                        // asynchronous store that completes transaction bytes on the leader's (a
-                        // cluster-scope arrive would hold the thread for a microsecond)
+                    if (mine && kb < P.num_kb) {
+                        // one signal per group and converted stage, after every thread's writes and
+                        // proxy fence: a CTA-scope arrive on this CTA's full barrier, or from the peer
+                        // of a pair an asynchronous store that completes transaction bytes on the
+                        // leader's (a cluster-scope arrive would hold the thread for a microsecond).
+                        // The LoRA step is not converted: its producer makes both arrivals, after its
+                        // wait for the stage to be free, so no arrival can reach an earlier phase.
                         tc::named_bar_sync(1 + grp, kGT);
                         if (gt == 0) {
                             if (!PAIR || rank == 0) tc::mbar_arrive(tc::smem_u32(&full_bar[stage]));
-                            else if (kb < P.num_kb)
-                                tc::st_async_signal(sig_leader, 1u, full_leader0 + stage * (uint32_t)sizeof(uint64_t));
+                            else tc::st_async_signal(sig_leader, 1u, full_leader0 + stage * (uint32_t)sizeof(uint64_t));
                         }
+                        ++done;
                     }
                     if (++stage == kStages) stage = 0;
                 }
             }
+            if (gt == 0) s_issued[1 + grp] = done;
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -648,7 +672,9 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             const int up_off = htile ? BN / 4 : BN / 2;                 // gate/up pairs: up's TMEM column - gate's
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
-            const bool ok = tc::mbar_wait(tc::smem_u32(&tfull_bar[acc]), acc_phase);
+            // diagnostics: a launch chosen to fail first waits on a barrier nothing arrives on
+            const bool ok = (P.stall == 0 || tc::mbar_wait(tc::smem_u32(stall_bar), 0, lim)) &&
+                            tc::mbar_wait(tc::smem_u32(&tfull_bar[acc]), acc_phase, lim);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) set_timeout(g, s_abort);
                 break;
@@ -769,11 +795,91 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             }
         }
     }
-    // after an abort, a peer's last stage signal may still be in flight towards the leader
-    if (Q8 && PAIR && *s_abort) __nanosleep(20000);
     tc::fence_before_sync();
     __syncthreads();
-    if constexpr (PAIR) tc::cluster_sync();    // the leader's MMAs into the peer's TMEM are done
+    if constexpr (PAIR) tc::cluster_sync();    // normally: the leader's MMAs into the peer's TMEM are done
+    // ---- abort drain.  After a wait gave up, copies and MMAs may still be in flight: loads
+    // of stages nobody consumed, a pair's loads and stage signals towards the leader's full
+    // barriers, MMAs of tiles whose accumulators nobody read.  Every one of them has landed
+    // before the shared memory and TMEM are released: each producer waits for its own code
+    // stages (FP8), the leader completes on behalf of the side that issued nothing every
+    // full-barrier phase that received any copy and waits for it, and the MMA issuer waits
+    // for a last commit.  These waits use the full limit.  Both CTAs of a pair read both
+    // abort flags, so they take the branch together.
+    bool aborted = *s_abort != 0;
+    if constexpr (PAIR)
+        aborted = aborted || tc::ld_shared_cluster(tc::mapa(tc::smem_u32((const void*)s_abort), rank ^ 1u)) != 0;
+    if (aborted) {
+        if (warp == 0 && lane == 0) {
+            // stage fills issued by each producer, stages signalled by each converter group
+            const int own_f = s_issued[0];
+            int peer_f = 0, peer_done[kConvGroups] = {};
+            if constexpr (PAIR) {
+                const uint32_t pv = tc::mapa(tc::smem_u32((const void*)s_issued), rank ^ 1u);
+                peer_f = (int)tc::ld_shared_cluster(pv);
+                for (int i = 0; i < kConvGroups; ++i) peer_done[i] = (int)tc::ld_shared_cluster(pv + 4u * (1 + i));
+            }
+            const int f_lead = rank == 0 ? own_f : peer_f, f_peer = rank == 0 ? peer_f : own_f;
+            const int f_max = PAIR ? max(own_f, peer_f) : own_f;
+            // The producers run at most kStages fills apart (each waits for the MMA to have
+            // consumed the stage's previous fill), and every fill before f_max - kStages was
+            // consumed, so its phases are complete; the fills after it are the current
+            // phases of their stages.  Replay the fill sequence to find their sizes.
+            const int w0 = max(0, f_max - kStages);
+            int f = 0;
+            uint32_t sbits = 0;
+            int gcount[kConvGroups] = {};
+            for (int t = tile0; t < total_tiles && f < f_max; t += tile_step) {
+                int e, mt, nt;
+                decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
+                const bool half = PAIR && half_tile(s_off, e, mt);
+                const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : P.num_kb + (P.lora_k16 ? 1 : 0);
+                for (int kb = 0; kb < nkb && f < f_max; ++kb, ++f) {
+                    const int st = f % kStages;
+                    const bool main = G::KW > 1 || kb < P.num_kb;     // not the LoRA step
+                    const uint32_t spar = (sbits >> st) & 1u;
+                    int gi = 0;                                       // index among its group's code stages
+                    if (Q8 && main) {
+                        sbits ^= 1u << st;
+                        gi = gcount[st % kConvGroups]++;
+                    }
+                    if (f < w0) continue;
+                    if (Q8 && main && f < own_f) tc::mbar_wait(tc::smem_u32(&staged_bar[st]), spar);
+                    if (rank != 0) continue;
+                    // bytes that one CTA's copies of this fill complete on the full barrier
+                    uint32_t b;
+                    if (G::KW > 1) b = min(G::KW, P.num_kb - kb * G::KW) * (kABytes + BN * BK * 2);
+                    else if (main) b = (half ? kABytes / 2 : kABytes) + (Q8 ? 0 : G::kBBytes);
+                    else b = (half ? P.a2_bytes / 2 : P.a2_bytes) + (PAIR ? 2 : 4) * P.b2_box_bytes;
+                    const bool lp = f < f_lead, pp = PAIR && f < f_peer;
+                    if (!lp && !pp) continue;                         // no copy went towards this phase
+                    const int grp = st % kConvGroups;
+                    const bool lc = Q8 && main && gi < s_issued[1 + grp];
+                    const bool ps = Q8 && PAIR && main && gi < peer_done[grp];
+                    const uint32_t fb = tc::smem_u32(&full_bar[st]);
+                    if (!lp) {
+                        // only the peer issued this fill: the leader's arrivals, expecting what came
+                        tc::mbar_arrive_expect_tx(fb, (pp ? b : 0u) + (ps ? (uint32_t)kSignalBytes : 0u));
+                        if (Q8) tc::mbar_arrive(fb);
+                    } else {
+                        const uint32_t missing =
+                            (PAIR && !pp ? b : 0u) + (Q8 && PAIR && main && !ps ? (uint32_t)kSignalBytes : 0u);
+                        if (missing) tc::mbar_complete_tx(fb, missing);
+                        if (Q8 && main && !lc) tc::mbar_arrive(fb);
+                    }
+                    tc::mbar_wait(tc::smem_u32(&full_bar[st]), (uint32_t)(f / kStages) & 1u);
+                }
+            }
+        } else if (warp == 1 && lane == 0 && rank == 0) {
+            // completes when every MMA this thread issued has completed
+            if constexpr (PAIR) tc::mma_commit_pair(tc::smem_u32(drain_bar), 0x1);
+            else tc::mma_commit(tc::smem_u32(drain_bar));
+            tc::mbar_wait(tc::smem_u32(drain_bar), 0);
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        if constexpr (PAIR) tc::cluster_sync();
+    }
     if (warp == 1) {
         tc::fence_after_sync();
         if constexpr (PAIR) tc::tmem_dealloc_pair(tmem_base, kTmemCols);
@@ -889,6 +995,7 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
     memset(&P, 0, sizeof(P));
     P.g = g;
     P.num_kb = g.K / BK;
+    P.wait_ns = tc::kWaitTimeoutNs;
     const bool paired = g.epi == EPI_SWIGLU;
     const bool q8 = g.b_scale != nullptr;
     // FP8 weights always run on SM pairs: each CTA dequantises half of the B tile
@@ -944,6 +1051,14 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
     }
     const int64_t tm = pair ? 2 * BM : BM;
     const int64_t max_tiles = ((g.N + tm - 1) / tm + g.E) * (int64_t)P.n_tiles;
+    if (!pair) {
+        // diagnostics: a single-CTA launch the caller chose to fail (moe_diag_force_timeout)
+        const DiagWait dw = diag_next_single_cta_launch();
+        if (dw.stall) {
+            P.stall = 1;
+            P.wait_ns = dw.limit_ns;
+        }
+    }
     const size_t offs_bytes = (size_t)2 * (g.E + 1) * sizeof(int32_t);
     const bool mn = g.b_mn_major;
     if (proj) {

@@ -43,6 +43,8 @@ struct WgradParams {
     int E, r, rp;
     uint32_t b_sbo, b_swz;
     int32_t* dev_status;
+    uint64_t wait_ns;    // limit of the ordinary bounded waits
+    int stall;           // diagnostics: the epilogue first waits on a barrier nothing arrives on
 };
 
 // tile t -> (problem, expert, 128-column tile)
@@ -67,9 +69,12 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
     uint64_t* empty_bar = full_bar + kWStages;
     uint64_t* tfull_bar = empty_bar + kWStages;
     uint64_t* tempty_bar = tfull_bar + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty_bar + 2);
+    uint64_t* drain_bar = tempty_bar + 2;            // after an abort: the MMA issuer's last commit
+    uint64_t* stall_bar = drain_bar + 1;             // diagnostics: nothing ever arrives on it
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stall_bar + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int32_t* s_off = reinterpret_cast<int32_t*>(tmem_slot + 4);
+    static_assert((2 * kWStages + 6) * 8 + 16 <= 256, "barriers and flags fit the 256-byte tail");
     const int E = P.E;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -83,6 +88,8 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
             tc::mbar_init(tc::smem_u32(&tfull_bar[a]), 1);
             tc::mbar_init(tc::smem_u32(&tempty_bar[a]), 4);
         }
+        tc::mbar_init(tc::smem_u32(drain_bar), 1);
+        tc::mbar_init(tc::smem_u32(stall_bar), 1);
         *s_abort = 0;
         tc::fence_mbar_init();
     }
@@ -101,6 +108,8 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     const int total = E * (P.m_tiles[0] + (P.nprob > 1 ? P.m_tiles[1] : 0));
+    const uint64_t lim = P.wait_ns;
+    int fills = 0;                                   // the producer's stage fills (lane 0 of warp 0)
 
     if (warp == 0) {
         if (lane == 0) {
@@ -111,7 +120,7 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
                 wg_decode(P, t, prob, e, mt);
                 const int beg = s_off[e], end = s_off[e + 1];
                 for (int p0 = beg; p0 < end; p0 += WK) {
-                    if (!tc::mbar_wait(tc::smem_u32(&empty_bar[stage]), phase ^ 1)) {
+                    if (!tc::mbar_wait(tc::smem_u32(&empty_bar[stage]), phase ^ 1, lim)) {
                         *s_abort = 1;
                         atomicOr(P.dev_status, MOE_DEV_TIMEOUT);
                         break;
@@ -122,6 +131,7 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
                     tc::tma_load_2d(sa, &P.tm_big[prob], fb, mt * WM, p0);
                     tc::tma_load_2d(sa + kWABytes / 2, &P.tm_big[prob], fb, mt * WM + 64, p0);
                     tc::tma_load_2d(sa + kWABytes, &P.tm_small[prob], fb, 0, p0);
+                    ++fills;
                     if (++stage == kWStages) {
                         stage = 0;
                         phase ^= 1;
@@ -142,7 +152,7 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             ++it;
-            bool ok = tc::mbar_wait(tc::smem_u32(&tempty_bar[acc]), acc_phase ^ 1);
+            bool ok = tc::mbar_wait(tc::smem_u32(&tempty_bar[acc]), acc_phase ^ 1, lim);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) {
                     *s_abort = 1;
@@ -153,7 +163,7 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
             tc::fence_after_sync();
             const uint32_t d = tmem_base + acc * kAcc;
             for (int p0 = beg; p0 < end; p0 += WK) {
-                ok = tc::mbar_wait(tc::smem_u32(&full_bar[stage]), phase);
+                ok = tc::mbar_wait(tc::smem_u32(&full_bar[stage]), phase, lim);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     if (lane == 0) {
@@ -213,7 +223,9 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             ++it;
-            const bool ok = tc::mbar_wait(tc::smem_u32(&tfull_bar[acc]), acc_phase);
+            // diagnostics: a launch chosen to fail first waits on a barrier nothing arrives on
+            const bool ok = (P.stall == 0 || tc::mbar_wait(tc::smem_u32(stall_bar), 0, lim)) &&
+                            tc::mbar_wait(tc::smem_u32(&tfull_bar[acc]), acc_phase, lim);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) {
                     *s_abort = 1;
@@ -241,6 +253,21 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
     }
     tc::fence_before_sync();
     __syncthreads();
+    // ---- abort drain: the loads of the last stages may be unconsumed and the last MMAs
+    // unread; every one has landed before the shared memory and TMEM are released (full limit)
+    if (*s_abort) {
+        if (warp == 0 && lane == 0) {
+            // every fill before fills - kWStages was consumed by the MMA warp; the later ones
+            // are the current phases of their stages, each completed by its loads alone
+            for (int f = max(0, fills - kWStages); f < fills; ++f)
+                tc::mbar_wait(tc::smem_u32(&full_bar[f % kWStages]), (uint32_t)(f / kWStages) & 1u);
+        } else if (warp == 1 && lane == 0) {
+            tc::mma_commit(tc::smem_u32(drain_bar));
+            tc::mbar_wait(tc::smem_u32(drain_bar), 0);
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+    }
     if (warp == 1) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem_base, kTmemCols);
@@ -310,6 +337,7 @@ cudaError_t launch_lora_wgrad_tc(const WgradProblem* probs, int nprob, int rp, i
     P.nprob = nprob;
     P.E = E; P.r = r; P.rp = rp;
     P.dev_status = dev_status;
+    P.wait_ns = tc::kWaitTimeoutNs;
     P.b_sbo = 8 * rp * 2;
     P.b_swz = rp >= 64 ? tc::kSw128 : (rp >= 32 ? tc::kSw64 : tc::kSw32);
     const CUtensorMapSwizzle bsw = rp >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B
@@ -324,6 +352,12 @@ cudaError_t launch_lora_wgrad_tc(const WgradProblem* probs, int nprob, int rp, i
         if (!encode2d(&P.tm_big[i], q.Big, (uint64_t)q.M, rows, 64, WK, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         if (!encode2d(&P.tm_small[i], q.Small, (uint64_t)rp, rows, (uint32_t)rp, WK, bsw)) return cudaErrorInvalidValue;
+    }
+    // diagnostics: a launch the caller chose to fail (moe_diag_force_timeout)
+    const DiagWait dw = diag_next_single_cta_launch();
+    if (dw.stall) {
+        P.stall = 1;
+        P.wait_ns = dw.limit_ns;
     }
     switch (rp) {
         case 16: return launch_wg<16>(P, s);

@@ -8,6 +8,16 @@
 
 namespace moe {
 
+// ---- diagnostics (api.cu)
+// Wait limit and forced stall of the next single-CTA tensor-core launch (a grouped GEMM on
+// single-CTA tiles, a rank-r projection or a LoRA reduction): the library's full limit and
+// no stall, unless moe_diag_force_timeout chose this launch.  Counts the launch.
+struct DiagWait {
+    uint64_t limit_ns;
+    bool stall;
+};
+DiagWait diag_next_single_cta_launch();
+
 // ---- routing (route.cu)
 size_t route_workspace_bytes(int64_t N, int E);
 cudaError_t launch_route(const void* idx, int idx_bytes, const float* topk_w, int64_t N, int E,

@@ -10,7 +10,9 @@ namespace moe {
 namespace tc {
 
 // Bounded waits: a wait that does not complete within this many nanoseconds
-// gives up, and the caller reports MOE_DEV_TIMEOUT.
+// gives up, and the caller reports MOE_DEV_TIMEOUT.  The kernels take the limit of
+// their ordinary waits as a launch parameter (this value unless a diagnostic launch
+// shortens it); the waits that drain in-flight copies after an abort always use it.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -65,17 +67,23 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false on timeout.
+// Wait for the phase with the given parity to complete; false after `limit_ns`.
 template <bool CLUSTER = false>
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitTimeoutNs) {
     auto poll = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
     if (poll()) return true;
     const uint64_t t0 = globaltimer();
     uint32_t n = 0;
     while (!poll()) {
-        if ((++n & 255u) == 0 && globaltimer() - t0 > kWaitTimeoutNs) return false;
+        if ((++n & 255u) == 0 && globaltimer() - t0 > limit_ns) return false;
     }
     return true;
+}
+
+// Count `bytes` transaction bytes as arrived on a local mbarrier without moving data
+// (the abort drain balances a phase whose other side issued no copy).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
 // named barrier `id` (1..15) over `n` threads (a multiple of 32)
@@ -218,6 +226,13 @@ __device__ __forceinline__ uint32_t mapa(uint32_t a, uint32_t rank) {
 
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 32-bit load from shared memory of a CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ uint32_t ld_shared_cluster(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
 }
 
 // Arrive on an mbarrier given by its shared::cluster address (possibly the peer CTA's).

@@ -59,6 +59,18 @@ def errors(got: np.ndarray, ref: np.ndarray):
     return rel, mx
 
 
+def assert_elementwise(name: str, got: np.ndarray, ref: np.ndarray):
+    """The per-element half of the bound alone: |got - ref| <= 2e-2 * max|ref| everywhere."""
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    if ref.size == 0:
+        return
+    if np.abs(ref).max() == 0:
+        assert np.abs(got).max() == 0, f"{name}: expected exact zeros"
+        return
+    _, mx = errors(got, ref)
+    assert mx <= MAX_ABS, f"{name}: max-abs/max {mx:.3e} (<= {MAX_ABS})"
+
+
 def assert_close(name: str, got: np.ndarray, ref: np.ndarray):
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
     if ref.size == 0:

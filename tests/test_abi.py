@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.moe_abi_version() == 4
+    assert lib.moe_abi_version() == 5
     for code in range(0, 7):
         assert lib.moe_status_string(code)
 
@@ -209,3 +209,13 @@ def test_binding_argtypes_match_header_arity(lib):
             assert n == 0, f"{name}: no argtypes set but the header declares {n} parameters"
         else:
             assert len(argtypes) == n, f"{name}: binding declares {len(argtypes)} arguments, header {n}"
+
+
+def test_forced_timeout_hook_checks_its_limit(lib):
+    """The failure-path hook takes a wait limit in [1 us, 2 s] and disarms on a negative index;
+    checked on the host, nothing is launched."""
+    assert lib.moe_diag_force_timeout(0, 999) == 2
+    assert lib.moe_diag_force_timeout(0, 2_000_000_001) == 2
+    assert lib.moe_diag_force_timeout(-1, 0) == 0
+    assert lib.moe_diag_force_timeout(3, 1_000_000) == 0
+    assert lib.moe_diag_force_timeout(-1, 0) == 0
