@@ -103,8 +103,9 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
 # DRAM bytes (read + write) per launch from ncu captures of the current kernels
 # (profiles/), keyed by (workload, kernel); None where no capture of the current code exists.
 MEASURED_TRAFFIC = {
-    ("gptoss20b", "gemm_gate_up_fwd"): 1.181e9 + 0.263e9,
-    ("gptoss20b", "gemm_gate_up_bwd"): 1.322e9 + 0.178e9,
+    ("gptoss20b", "gemm_gate_up_fwd"): 1.1775e9 + 0.2623e9,
+    ("gptoss20b", "gemm_down_fwd"): 0.6337e9 + 0.0798e9,
+    ("gptoss20b", "gemm_gate_up_bwd"): 1.3219e9 + 0.1743e9,
 }
 
 

@@ -73,7 +73,12 @@ enum {
 
 enum {
     MOE_DEV_BAD_EXPERT_ID = 1,
-    MOE_DEV_TIMEOUT = 2
+    MOE_DEV_TIMEOUT = 2,
+    /* Debug build of the library only (libmoe_lora_gb300_debug.so, compiled with
+     * MOE_DEBUG=1): an index read from a routing buffer (perm, inv_perm, offsets,
+     * tile_offsets) was out of range; the access was skipped.  The release build
+     * does not check these indices: they must come from moe_route. */
+    MOE_DEV_BAD_INDEX = 4
 };
 
 /* Row tile of the grouped GEMMs; tile_offsets counts tiles of this many rows. */

@@ -8,6 +8,7 @@ the shared library is missing or fails to load, every call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from dataclasses import dataclass
@@ -16,10 +17,13 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe_lora_gb300.so")
+# the debug build: indices read from routing buffers are checked (MOE_DEV_BAD_INDEX)
+LIB_DEBUG_PATH = os.path.join(_PKG, "libmoe_lora_gb300_debug.so")
 
 MOE_OK = 0
 MOE_DEV_BAD_EXPERT_ID = 1
 MOE_DEV_TIMEOUT = 2
+MOE_DEV_BAD_INDEX = 4
 TILE_M = 128
 
 
@@ -45,14 +49,16 @@ EXPORTED = ("moe_abi_version", "moe_status_string", "moe_launch_count", "moe_rou
             "moe_packed_metadata", "moe_packed_causal_mask", "moe_diag_force_timeout")
 ABI_VERSION = 5
 
-_lib = None
+_libs: dict = {}
+_default_path = LIB_PATH
 
 
-def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load the CUDA library (raises if it has not been built)."""
-    global _lib
-    if _lib is not None:
-        return _lib
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built).  Without `path`: the library
+    the binding's calls currently go to (the release build unless `using_library` says so)."""
+    path = path or _default_path
+    if path in _libs:
+        return _libs[path]
     if not os.path.exists(path):
         raise MoEError(f"MoE-LoRA CUDA library not built: {path} is missing "
                        "(run moe_expert_dispatch_stable_gb300.build.build())")
@@ -85,8 +91,22 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         getattr(lib, name).restype = i32
     if lib.moe_abi_version() != ABI_VERSION:
         raise MoEError("MoE-LoRA library ABI version mismatch")
-    _lib = lib
+    _libs[path] = lib
     return lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Send the binding's calls to the library at `path` (e.g. LIB_DEBUG_PATH, the build
+    that checks routing indices) inside the block; process-wide."""
+    global _default_path
+    old = _default_path
+    lib = load_library(path)
+    _default_path = path
+    try:
+        yield lib
+    finally:
+        _default_path = old
 
 
 def _check(status: int):

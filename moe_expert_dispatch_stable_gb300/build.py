@@ -18,6 +18,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_lora_gb300.so")
+# the debug build: every index read from a caller's routing buffer is checked before use
+# (MOE_DEBUG=1; out-of-range indices set MOE_DEV_BAD_INDEX and are skipped)
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libmoe_lora_gb300_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["route.cu", "router.cu", "rowops.cu", "quant.cu", "packed.cu", "gemm_tc.cu", "gemm_wgrad.cu", "api.cu"]
 
@@ -43,14 +47,18 @@ def _stale(obj: str, src: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, extra_flags=()) -> str:
-    """Compile (if stale) and link the library; returns its path."""
+def build(verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile (if stale) and link the library (the debug build with debug=True);
+    returns its path."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    bdir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    if debug:
+        extra_flags = (*extra_flags, "-DMOE_DEBUG=1")
+    os.makedirs(bdir, exist_ok=True)
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(bdir, src.replace(".cu", ".o"))
         if _stale(o, s):
             jobs.append([nvcc, *_flags(extra_flags), "-c", s, "-o", o])
     def run(cmd):
@@ -64,13 +72,13 @@ def build(verbose: bool = False, extra_flags=()) -> str:
         for msg in ex.map(run, jobs):
             if verbose and msg:
                 print(msg, file=sys.stderr)
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
-    if jobs or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        tmp = LIB + ".tmp"
+    objs = [os.path.join(bdir, s.replace(".cu", ".o")) for s in SOURCES]
+    if jobs or not os.path.exists(lib) or any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs):
+        tmp = lib + ".tmp"
         run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv))
+    print(build(verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -277,7 +277,7 @@ moe_status moe_lora_saved_regather(const moe_dims* d, const moe_routing* rt, con
     cudaStream_t s = (cudaStream_t)stream;
     void* x_perm = static_cast<uint8_t*>(saved) + L.x_perm;
     MOE_TRY(timed("gather_x", s, [&] {
-        return launch_gather_rows(x, d->H, rt->perm, nullptr, N, d->k, x_perm, nullptr, nullptr, s);
+        return launch_gather_rows(x, d->H, rt->perm, nullptr, N, d->k, x_perm, nullptr, nullptr, nullptr, s);
     }));
     return MOE_OK;
 }
@@ -325,7 +325,7 @@ static moe_status fwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     void* O = sv + L.o;
     const int H = d->H, I = d->I, E = d->E, r = d->r;
 
-    MOE_TRY(timed("gather_x", s, [&] { return launch_gather_rows(x, H, rt->perm, nullptr, N, d->k, x_perm, nullptr, nullptr, s); }));
+    MOE_TRY(timed("gather_x", s, [&] { return launch_gather_rows(x, H, rt->perm, nullptr, N, d->k, x_perm, nullptr, nullptr, dev_status, s); }));
     MOE_TRY(timed("proj_xa", s, [&] { return project(x_perm, H, A_gu, r, L.rp, d->scale, rt, E, N, XA, dev_status, s); }));
 
     GroupedGemm g{};
@@ -347,7 +347,7 @@ static moe_status fwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     g2.out0 = O; g2.ldo = H; g2.epi = EPI_BF16;
     MOE_TRY(timed("gemm_down_fwd", s, [&] { return launch_grouped_gemm(g2, s); }));
 
-    MOE_TRY(timed("combine_y", s, [&] { return launch_combine(O, false, rt->w_sorted, rt->inv_perm, d->T, d->k, H, y, s); }));
+    MOE_TRY(timed("combine_y", s, [&] { return launch_combine(O, false, rt->w_sorted, rt->inv_perm, d->T, d->k, H, y, dev_status, s); }));
     return MOE_OK;
 }
 
@@ -398,7 +398,7 @@ static moe_status bwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     void* dXp = ws + W.dx_perm;
 
     // dO = w * dy[token]  (and d_topk_w[slot] = <dy[token], O[p]> when requested)
-    MOE_TRY(timed("gather_dy", s, [&] { return launch_gather_rows(dy, H, rt->perm, rt->w_sorted, N, d->k, dO, Os, d_topk_w, s); }));
+    MOE_TRY(timed("gather_dy", s, [&] { return launch_gather_rows(dy, H, rt->perm, rt->w_sorted, N, d->k, dO, Os, d_topk_w, dev_status, s); }));
     // G_s = s * dO B_d^T
     MOE_TRY(timed("proj_g", s, [&] { return project(dO, H, B_d, r, L.rp, d->scale, rt, E, N, G, dev_status, s); }));
     // dh = dO W_d[e]^T + G_s A_d[e]  ->  dGU = SwiGLU'(GU) dh
@@ -424,7 +424,7 @@ static moe_status bwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     g2.A2 = Gg; g2.rp = L.rp; g2.r = r; g2.B2 = A_gu; g2.ldb2 = H; g2.b2_expert_stride = (int64_t)r * H;
     g2.out0 = dXp; g2.ldo = H; g2.epi = EPI_PLAIN_F32;
     MOE_TRY(timed("gemm_gate_up_bwd", s, [&] { return launch_grouped_gemm(g2, s); }));
-    MOE_TRY(timed("combine_dx", s, [&] { return launch_combine(dXp, true, nullptr, rt->inv_perm, d->T, d->k, H, dx, s); }));
+    MOE_TRY(timed("combine_dx", s, [&] { return launch_combine(dXp, true, nullptr, rt->inv_perm, d->T, d->k, H, dx, dev_status, s); }));
     // dA_gu = Gg_s^T x_perm ; dB_gu = XA_s^T dGU
     {
         const WgradProblem wp[2] = {{Gg, x_perm, H, dA_gu}, {XA, dGU, 2 * I, dB_gu}};

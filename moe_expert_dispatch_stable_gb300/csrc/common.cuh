@@ -47,6 +47,35 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// ---- debug build
+// With MOE_DEBUG=1 (a separate build of the library) every index read from a caller's
+// routing buffer is checked before it is used: an index outside [0, n) sets
+// MOE_DEV_BAD_INDEX in the status word (when the call has one) and the access is skipped.
+// No trap, no assert.  The release build (MOE_DEBUG=0) compiles the checks away.
+#ifndef MOE_DEBUG
+#define MOE_DEBUG 0
+#endif
+
+__device__ __forceinline__ bool dbg_index_ok(int64_t i, int64_t n, int32_t* status) {
+    if (!MOE_DEBUG || (i >= 0 && i < n)) return true;
+    if (status != nullptr) atomicOr(status, MOE_DEV_BAD_INDEX);
+    return false;
+}
+
+// Debug build: offsets [E+1] must start at 0, never decrease and end at N; tile offsets
+// (when given) must count ceil(rows / tile_m) tiles per expert.  Checked by one thread.
+__device__ __forceinline__ bool dbg_offsets_ok(const int32_t* offs, const int32_t* toffs, int E, int64_t N, int tile_m,
+                                               int32_t* status) {
+    if (!MOE_DEBUG) return true;
+    bool ok = offs[0] == 0 && offs[E] == N && (toffs == nullptr || toffs[0] == 0);
+    for (int e = 0; e < E && ok; ++e) {
+        ok = offs[e + 1] >= offs[e];
+        if (ok && toffs != nullptr) ok = toffs[e + 1] - toffs[e] == (offs[e + 1] - offs[e] + tile_m - 1) / tile_m;
+    }
+    if (!ok && status != nullptr) atomicOr(status, MOE_DEV_BAD_INDEX);
+    return ok;
+}
+
 // Rounded-up padded LoRA rank used for the [N, RP] rank-r activations.
 inline int lora_rp(int r) { return r <= 16 ? 16 : (r <= 32 ? 32 : 64); }
 

@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
     volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     uint32_t* sig_slot = tmem_slot + 2;             // FP8 pairs: target of the peer's stage signals
     // what the roles issued, read by the abort drain: [0] the producer's stage fills,
-    // [1 + g] the stages converter group g signalled (FP8)
+    // [1 + g] the stages converter group g signalled (FP8); [3] debug build: bad offsets
     volatile int* s_issued = reinterpret_cast<volatile int*>(tmem_slot + 4);
     int32_t* s_off = reinterpret_cast<int32_t*>(tmem_slot + 8);
     static_assert((3 * kStages + 6) * 8 + 32 <= 256, "barriers and flags fit the 256-byte tail");
@@ -331,7 +331,13 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
     if constexpr (PAIR) tc::cluster_sync();    // the peer's barriers exist before anyone signals them
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    const int total_tiles = s_toff[E] * P.n_tiles;
+    if constexpr (MOE_DEBUG) {
+        // debug build: offsets that do not describe N rows schedule no tile
+        if (threadIdx.x == 0)
+            s_issued[3] = dbg_offsets_ok(s_off, PAIR ? nullptr : s_toff, E, g.N, BM, g.dev_status) ? 0 : 1;
+        __syncthreads();
+    }
+    const int total_tiles = (MOE_DEBUG && s_issued[3]) ? 0 : s_toff[E] * P.n_tiles;
     const uint64_t lim = P.wait_ns;
     int fills = 0;                                  // the producer's stage fills (lane 0 of warp 0)
 

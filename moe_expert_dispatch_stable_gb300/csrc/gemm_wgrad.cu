@@ -43,6 +43,7 @@ struct WgradParams {
     int E, r, rp;
     uint32_t b_sbo, b_swz;
     int32_t* dev_status;
+    int64_t N;           // sorted rows (the debug build checks the offsets against it)
     uint64_t wait_ns;    // limit of the ordinary bounded waits
     int stall;           // diagnostics: the epilogue first waits on a barrier nothing arrives on
 };
@@ -107,7 +108,13 @@ __global__ void __launch_bounds__(kWThreads, 1) lora_wgrad_tc_kernel(const __gri
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = E * (P.m_tiles[0] + (P.nprob > 1 ? P.m_tiles[1] : 0));
+    volatile int* s_bad = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    if constexpr (MOE_DEBUG) {
+        // debug build: offsets that do not describe the N rows schedule no tile
+        if (threadIdx.x == 0) *s_bad = dbg_offsets_ok(s_off, nullptr, E, P.N, 1, P.dev_status) ? 0 : 1;
+        __syncthreads();
+    }
+    const int total = (MOE_DEBUG && *s_bad) ? 0 : E * (P.m_tiles[0] + (P.nprob > 1 ? P.m_tiles[1] : 0));
     const uint64_t lim = P.wait_ns;
     int fills = 0;                                   // the producer's stage fills (lane 0 of warp 0)
 
@@ -337,6 +344,7 @@ cudaError_t launch_lora_wgrad_tc(const WgradProblem* probs, int nprob, int rp, i
     P.nprob = nprob;
     P.E = E; P.r = r; P.rp = rp;
     P.dev_status = dev_status;
+    P.N = N;
     P.wait_ns = tc::kWaitTimeoutNs;
     P.b_sbo = 8 * rp * 2;
     P.b_swz = rp >= 64 ? tc::kSw128 : (rp >= 32 ? tc::kSw64 : tc::kSw32);

@@ -28,12 +28,14 @@ cudaError_t route_static_scratch(void** ptr);
 // ---- row kernels (rowops.cu)
 // dst[p, :] = src[perm[p] / k, :]   (optionally scaled by w_sorted[p], rounded to bf16).
 // With O and d_w given: d_w[perm[p]] = <src[perm[p] / k, :], O[p, :]> (fp32), in the same pass.
+// `status` (may be null): the debug build's MOE_DEV_BAD_INDEX for a perm entry outside [0, N).
 cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, const float* w_sorted,
-                               int64_t N, int k, void* dst, const void* O, float* d_w, cudaStream_t s);
+                               int64_t N, int k, void* dst, const void* O, float* d_w, int32_t* status,
+                               cudaStream_t s);
 // out[t, :] = bf16( sum_{j<k} w * src[inv_perm[t*k+j], :] ), w = w_sorted[inv_perm[t*k+j]] (or 1 when
 // w_sorted is null); bf16 or fp32 src, fp32 sum in the fixed order j = 0..k-1
 cudaError_t launch_combine(const void* src, bool src_f32, const float* w_sorted, const int32_t* inv_perm, int64_t T,
-                           int k, int H, void* out, cudaStream_t s);
+                           int k, int H, void* out, int32_t* status, cudaStream_t s);
 
 // ---- FP8 expert weights (quant.cu)
 // scale[m, c] = 2^ceil(log2(amax_r |W[m, r, c]| / 448)), Wq[m, r, c] = e4m3_rn(W[m, r, c] / scale[m, c])

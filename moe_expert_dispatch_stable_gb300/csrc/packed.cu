@@ -125,7 +125,8 @@ packed_mask_kernel(const int32_t* __restrict__ cu_seqlens, const int32_t* __rest
         const int64_t f0 = q * 16;
         int64_t i = f0 / T;
         int64_t j = f0 - i * T;
-        int64_t lo = cu_seqlens[seq_id[i]];
+        // debug build: a sample id outside [0, T] gives the row no ones
+        int64_t lo = dbg_index_ok(seq_id[i], T + 1, nullptr) ? cu_seqlens[seq_id[i]] : i + 1;
         uint32_t w[4] = {0u, 0u, 0u, 0u};                  // byte u of the chunk in w[u / 4]
         const int nb = (int)min((int64_t)16, nbytes - f0);
 #pragma unroll
@@ -134,7 +135,7 @@ packed_mask_kernel(const int32_t* __restrict__ cu_seqlens, const int32_t* __rest
             if (++j == T && u + 1 < nb) {
                 j = 0;
                 ++i;
-                lo = cu_seqlens[seq_id[i]];
+                lo = dbg_index_ok(seq_id[i], T + 1, nullptr) ? cu_seqlens[seq_id[i]] : i + 1;
             }
         }
         if (nb == 16) {
@@ -157,7 +158,7 @@ packed_mask_rows_kernel(const int32_t* __restrict__ cu_seqlens, const int32_t* _
     pdl_trigger();
     const int chunks = T >> 4;
     for (int i = blockIdx.x; i < T; i += gridDim.x) {
-        const int lo = cu_seqlens[seq_id[i]];
+        const int lo = dbg_index_ok(seq_id[i], (int64_t)T + 1, nullptr) ? cu_seqlens[seq_id[i]] : i + 1;
         uint4* row = reinterpret_cast<uint4*>(mask + (int64_t)i * T);
         for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
             const int j0 = c << 4;

@@ -115,7 +115,10 @@ router_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ 
         const float inv = 1.0f / s;
         // c = sum_j dw_j * p_{idx_j}
         float c = 0.f;
-        for (int j = lane; j < k; j += 32) c += d_topk_w[t * k + j] * expf(row[topk_idx[t * k + j]] - m) * inv;
+        for (int j = lane; j < k; j += 32) {
+            const int ix = topk_idx[t * k + j];
+            if (dbg_index_ok(ix, E, nullptr)) c += d_topk_w[t * k + j] * expf(row[ix] - m) * inv;
+        }
         c = warp_sum(c);
         for (int e = lane; e < E; e += 32) {
             float g = 0.f;

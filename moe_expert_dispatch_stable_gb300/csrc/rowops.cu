@@ -54,13 +54,15 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 // gather takes the chunked kernel below.
 __global__ void gather_rows_kernel(const uint4* __restrict__ src, int vpr, const int32_t* __restrict__ perm,
                                    const float* __restrict__ w_sorted, int64_t N, int k,
-                                   uint4* __restrict__ dst, const uint4* __restrict__ O, float* __restrict__ d_w) {
+                                   uint4* __restrict__ dst, const uint4* __restrict__ O, float* __restrict__ d_w,
+                                   int32_t* status) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t p = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < N; p += nwarps) {
         const int slot = perm[p];
+        if (!dbg_index_ok(slot, N, status)) continue;
         const int64_t t = slot / k;
         const uint4* s = src + t * vpr;
         uint4* d = dst + p * vpr;
@@ -100,7 +102,7 @@ constexpr int kUpl = 4;
 
 __global__ void gather_rows32_kernel(const uint8_t* __restrict__ src, int units, const int32_t* __restrict__ perm,
                                      const float* __restrict__ w_sorted, int64_t N, int k,
-                                     uint8_t* __restrict__ dst) {
+                                     uint8_t* __restrict__ dst, int32_t* status) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
@@ -111,7 +113,9 @@ __global__ void gather_rows32_kernel(const uint8_t* __restrict__ src, int units,
     for (int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < tasks; task += nwarps) {
         const int64_t p = task / cpr;
         const int c = (int)(task - p * cpr);
-        const int64_t t = perm[p] / k;
+        const int64_t slot = perm[p];
+        if (!dbg_index_ok(slot, N, status)) continue;
+        const int64_t t = slot / k;
         const float w = w_sorted != nullptr ? w_sorted[p] : 1.0f;
         const uint8_t* s = src + t * row_bytes;
         uint8_t* d = dst + p * row_bytes;
@@ -141,7 +145,8 @@ __global__ void gather_rows32_kernel(const uint8_t* __restrict__ src, int units,
 }
 
 cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, const float* w_sorted,
-                               int64_t N, int k, void* dst, const void* O, float* d_w, cudaStream_t s) {
+                               int64_t N, int k, void* dst, const void* O, float* d_w, int32_t* status,
+                               cudaStream_t s) {
     if (N == 0) return cudaSuccess;
     const int threads = 256;
     if (d_w == nullptr && H % 16 == 0) {
@@ -149,11 +154,11 @@ cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, cons
         const int64_t tasks = N * ((units + 32 * kUpl - 1) / (32 * kUpl));
         const int64_t blocks = std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms() * 16);
         return launch_pdl(gather_rows32_kernel, dim3((unsigned)blocks), dim3(threads), 0, s, (const uint8_t*)src,
-                          units, perm, w_sorted, N, k, (uint8_t*)dst);
+                          units, perm, w_sorted, N, k, (uint8_t*)dst, status);
     }
     const int64_t blocks = std::min<int64_t>((N + 7) / 8, (int64_t)num_sms() * 16);
     return launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(threads), 0, s, (const uint4*)src, H / 8, perm,
-                      w_sorted, N, k, (uint4*)dst, (const uint4*)O, d_w);
+                      w_sorted, N, k, (uint4*)dst, (const uint4*)O, d_w, status);
 }
 
 // ---------------------------------------------------------------- combine
@@ -187,7 +192,7 @@ __host__ __device__ constexpr int combine_upl() { return 1; }
 template <typename SrcT>
 __global__ void combine_kernel(const SrcT* __restrict__ src, const float* __restrict__ w_sorted,
                                const int32_t* __restrict__ inv_perm, int64_t T, int k, int H,
-                               bf16* __restrict__ out) {
+                               bf16* __restrict__ out, int32_t* status) {
     pdl_wait();
     pdl_trigger();
     constexpr int kC = combine_upl<SrcT>();
@@ -207,8 +212,10 @@ __global__ void combine_kernel(const SrcT* __restrict__ src, const float* __rest
         // the slots' rows and weights, 32 at a time one per lane, broadcast in slot order
         for (int j0 = 0; j0 < k; j0 += 32) {
             const int kj = min(32, k - j0);
-            const int64_t my_row = lane < kj ? inv_perm[t * k + j0 + lane] : 0;
-            const float my_w = (lane < kj && w_sorted != nullptr) ? w_sorted[my_row] : 1.0f;
+            int64_t my_row = lane < kj ? inv_perm[t * k + j0 + lane] : 0;
+            const bool my_ok = lane >= kj || dbg_index_ok(my_row, T * k, status);
+            if (!my_ok) my_row = 0;                         // debug build: a bad row adds nothing
+            const float my_w = !my_ok ? 0.0f : ((lane < kj && w_sorted != nullptr) ? w_sorted[my_row] : 1.0f);
 #pragma unroll 4
             for (int j = 0; j < kj; ++j) {
                 const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
@@ -234,7 +241,7 @@ __global__ void combine_kernel(const SrcT* __restrict__ src, const float* __rest
 }
 
 cudaError_t launch_combine(const void* src, bool src_f32, const float* w_sorted, const int32_t* inv_perm, int64_t T,
-                           int k, int H, void* out, cudaStream_t s) {
+                           int k, int H, void* out, int32_t* status, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (H % 16 != 0) return cudaErrorInvalidValue;
     const int threads = 256;
@@ -244,9 +251,9 @@ cudaError_t launch_combine(const void* src, bool src_f32, const float* w_sorted,
     const int64_t blocks = std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms() * 16);
     if (src_f32)
         return launch_pdl(combine_kernel<float>, dim3((unsigned)blocks), dim3(threads), 0, s, (const float*)src,
-                          w_sorted, inv_perm, T, k, H, (bf16*)out);
+                          w_sorted, inv_perm, T, k, H, (bf16*)out, status);
     return launch_pdl(combine_kernel<bf16>, dim3((unsigned)blocks), dim3(threads), 0, s, (const bf16*)src, w_sorted,
-                      inv_perm, T, k, H, (bf16*)out);
+                      inv_perm, T, k, H, (bf16*)out, status);
 }
 
 }  // namespace moe

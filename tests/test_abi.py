@@ -178,13 +178,26 @@ def test_packed_metadata_host_checks(lib):
 
 def test_binding_fails_loudly_without_library(tmp_path):
     from moe_expert_dispatch_stable_gb300 import binding as b
-    saved = b._lib
-    try:
-        b._lib = None
-        with pytest.raises(b.MoEError):
-            b.load_library(str(tmp_path / "missing.so"))
-    finally:
-        b._lib = saved
+    with pytest.raises(b.MoEError):
+        b.load_library(str(tmp_path / "missing.so"))
+    with pytest.raises(b.MoEError):
+        with b.using_library(str(tmp_path / "missing.so")):
+            pass
+
+
+def test_debug_build_loads_and_exports_the_same_symbols():
+    """The debug build (MOE_DEBUG=1: routing indices checked, MOE_DEV_BAD_INDEX) builds,
+    loads and exports every declared symbol, with the same ABI version."""
+    from moe_expert_dispatch_stable_gb300 import binding as b, build
+    path = build.build(debug=True)
+    assert path == b.LIB_DEBUG_PATH
+    dbg = b.load_library(path)
+    assert dbg.moe_abi_version() == b.ABI_VERSION
+    for name in sorted(_declared_symbols()):
+        assert hasattr(dbg, name), f"{name} missing from the debug build"
+    with b.using_library(path) as lib:
+        assert lib is dbg and b.load_library() is dbg
+    assert b.load_library() is not dbg
 
 
 def _header_arity():
