@@ -103,9 +103,10 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
 # DRAM bytes (read + write) per launch from ncu captures of the current kernels
 # (profiles/), keyed by (workload, kernel); None where no capture of the current code exists.
 MEASURED_TRAFFIC = {
-    ("gptoss20b", "gemm_gate_up_fwd"): 1.1775e9 + 0.2623e9,
-    ("gptoss20b", "gemm_down_fwd"): 0.6337e9 + 0.0798e9,
-    ("gptoss20b", "gemm_gate_up_bwd"): 1.3219e9 + 0.1743e9,
+    ("gptoss20b", "gemm_gate_up_fwd"): 1.1739e9 + 0.2629e9,
+    ("gptoss20b", "gemm_down_fwd"): 0.6334e9 + 0.0801e9,
+    ("gptoss20b", "gemm_down_bwd"): 0.8349e9 + 0.1645e9,
+    ("gptoss20b", "gemm_gate_up_bwd"): 1.3212e9 + 0.1741e9,
 }
 
 
