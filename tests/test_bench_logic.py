@@ -61,3 +61,28 @@ def test_routing_summary_shows_the_skew():
     flat = mi.CONFIGS["gptoss20b"]
     r2 = bench.routing_summary(mi.make_routing(flat, 0)[0], flat.E)
     assert r2["zero_experts"] == 0 and r2["above_10x_mean"] == 0
+
+
+def test_tensor_peak_is_the_burst_figure_at_full_clock():
+    """Kernels timed inside a few-millisecond step at the maximum SM clock are held against the
+    burst bf16 peak; a run whose median clock fell more than 5 % below the maximum (a power cap
+    that bit, or a clock lock) against the sustained one; no clock record: sustained."""
+    peaks = dict(hbm_gbs=6690.0, bf16_tflops=1924.2, bf16_tflops_sustained=1735.4, source="measured")
+    p, src = bench.tensor_peak(peaks, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})
+    assert p == 1924.2 and "burst" in src and "2070" in src
+    p, _ = bench.tensor_peak(peaks, {"sm_mhz": 1976.0, "sm_max_mhz": 2070.0})
+    assert p == 1924.2
+    p, src = bench.tensor_peak(peaks, {"sm_mhz": 1900.0, "sm_max_mhz": 2070.0})
+    assert p == 1735.4 and "sustained" in src
+    p, _ = bench.tensor_peak(peaks, {"sm_mhz": None, "sm_max_mhz": None})
+    assert p == 1735.4
+
+
+def test_routing_summary_shows_the_skewed_histogram():
+    """The skewed workload's routing: many experts without rows and a few above ten times
+    the mean, as the bench line reports them."""
+    cfg = mi.CONFIGS["gptoss120b_skew"]
+    idx, _ = mi.make_routing(cfg, 0)
+    s = bench.routing_summary(idx, cfg.E)
+    assert s["zero_experts"] >= 10 and s["above_10x_mean"] >= 1
+    assert sum(s["counts"]) == cfg.T * cfg.k and s["max"] == max(s["counts"])
