@@ -39,6 +39,9 @@ CASES = {
     "ragged_single": mi.MoEConfig("ragged", T=700, H=256, E=6, k=2, I=320, r=16, alpha=32),
     "pairs_ragged": mi.MoEConfig("pairs", T=1000, H=256, E=4, k=2, I=320, r=16, alpha=32),
     "tiny_r8": mi.CONFIGS["tiny"],
+    # ~3 tiles per SM pair: the converters carry their stage parity across tiles and
+    # LoRA steps
+    "multi_tile": mi.MoEConfig("multitile", T=8192, H=512, E=8, k=2, I=512, r=16, alpha=32),
 }
 
 
