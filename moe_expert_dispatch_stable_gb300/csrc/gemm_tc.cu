@@ -65,8 +65,14 @@ struct Geo {
     // FP8 weights: the TMA lands the e4m3 codes in the upper half of the B slot and the
     // converter warps expand them in place, so a stage is as large as with bf16 weights
     static constexpr int kQBytes = Q8 ? kBBytes / 2 : 0;
-    static constexpr int kStageBytes = kABytes * KW + ((kBBytes + 1023) / 1024) * 1024;
-    static constexpr int kStages = PAIR ? 6 : (BN >= 256 ? 4 : (216 * 1024) / kStageBytes);
+    // bf16 SM pairs take two 64-deep k-blocks per ring stage: one barrier wait, 8 MMAs
+    // and one commit per stage.  Each wait-and-commit cycle costs the tensor pipe a fixed
+    // ~0.13 us, a third of a 64-deep stage of 256 x 256 MMAs (measured: 16-18 % faster
+    // GEMMs than six 64-deep stages).
+    static constexpr int KB2 = (PAIR && !Q8) ? 2 : 1;
+    static constexpr int kSubBytes = kABytes * KW + ((kBBytes + 1023) / 1024) * 1024;   // one k-block
+    static constexpr int kStageBytes = KB2 * kSubBytes;
+    static constexpr int kStages = PAIR ? 6 / KB2 : (BN >= 256 ? 4 : (216 * 1024) / kStageBytes);
     static constexpr int kAccCols = BN;
     static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
@@ -340,6 +346,8 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
     const int total_tiles = (MOE_DEBUG && s_issued[3]) ? 0 : s_toff[E] * P.n_tiles;
     const uint64_t lim = P.wait_ns;
     int fills = 0;                                  // the producer's stage fills (lane 0 of warp 0)
+    constexpr int KB2 = G::KB2;                     // 64-deep k-blocks per ring stage
+    const int nmain = (P.num_kb + KB2 - 1) / KB2;   // main-product stages per tile (then the LoRA step)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -355,7 +363,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 const CUtensorMap* tma2 = half ? &P.tm_a2_64 : &P.tm_a2;
                 const int a_bytes = half ? kABytes / 2 : kABytes;
                 const int a2_bytes = half ? P.a2_bytes / 2 : P.a2_bytes;
-                const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : P.num_kb + (P.lora_k16 ? 1 : 0);
+                const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : nmain + (P.lora_k16 ? 1 : 0);
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!tc::mbar_wait(tc::smem_u32(&empty_bar[stage]), phase ^ 1, lim)) {
                         set_timeout(g, s_abort);
@@ -367,7 +375,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                     if constexpr (PAIR) {
                         // both CTAs' loads complete on the leader's full barrier
                         const uint32_t fb = tc::mapa(fb_local, 0);
-                        if (kb < P.num_kb && Q8) {
+                        if (kb < nmain && Q8) {
                             if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * a_bytes + kSignalBytes);
                             tc::tma_load_2d_pair(sa, tma, fb, kb * BK, m0);
                             const uint32_t sq = sb + G::kQBytes;
@@ -381,16 +389,22 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                             } else {
                                 tc::tma_load_3d(sq, &P.tm_b, qb, kb * BK, nt * BN + (int)rank * (BN / 2), e);
                             }
-                        } else if (kb < P.num_kb) {
-                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * (a_bytes + G::kBBytes));
-                            tc::tma_load_2d_pair(sa, tma, fb, kb * BK, m0);
-                            if (B_MN) {
+                        } else if (kb < nmain) {
+                            // k-blocks kb * KB2 .. of this stage, each in its own A + B sub-block
+                            const int nsub = min(KB2, P.num_kb - kb * KB2);
+                            if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * nsub * (a_bytes + G::kBBytes));
+                            for (int j = 0; j < nsub; ++j) {
+                                const uint32_t saj = sa + j * G::kSubBytes, sbj = saj + kABytes;
+                                const int kx = (kb * KB2 + j) * BK;
+                                tc::tma_load_2d_pair(saj, tma, fb, kx, m0);
+                                if (B_MN) {
 #pragma unroll
-                                for (int jj = 0; jj < 2; ++jj)
-                                    tc::tma_load_3d_pair(sb + jj * kBoxMN, &P.tm_b, fb,
-                                                         b_col_pair<PAIRED, BN>(half, (int)rank, jj, nt, g.Ncols), kb * BK, e);
-                            } else {
-                                tc::tma_load_3d_pair(sb, &P.tm_b, fb, kb * BK, nt * BN + (int)rank * (BN / 2), e);
+                                    for (int jj = 0; jj < 2; ++jj)
+                                        tc::tma_load_3d_pair(sbj + jj * kBoxMN, &P.tm_b, fb,
+                                                             b_col_pair<PAIRED, BN>(half, (int)rank, jj, nt, g.Ncols), kx, e);
+                                } else {
+                                    tc::tma_load_3d_pair(sbj, &P.tm_b, fb, kx, nt * BN + (int)rank * (BN / 2), e);
+                                }
                             }
                         } else {
                             if (rank == 0) {
@@ -416,7 +430,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                         }
                     } else {
                         const uint32_t fb = fb_local;
-                        if (kb < P.num_kb && Q8) {
+                        if (kb < nmain && Q8) {
                             tc::mbar_arrive_expect_tx(fb, kABytes);
                             tc::tma_load_2d(sa, &P.tm_a, fb, kb * BK, m0);
                             const uint32_t sq = sb + G::kQBytes;
@@ -430,7 +444,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                             } else {
                                 tc::tma_load_3d(sq, &P.tm_b, qb, kb * BK, nt * BN, e);
                             }
-                        } else if (kb < P.num_kb) {
+                        } else if (kb < nmain) {
                             tc::mbar_arrive_expect_tx(fb, kABytes + G::kBBytes);
                             tc::tma_load_2d(sa, &P.tm_a, fb, kb * BK, m0);
                             if (B_MN) {
@@ -488,7 +502,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 }
                 const uint32_t idesc = half ? idesc_half : idesc_full;
                 const uint32_t idesc2 = half ? idesc2_half : idesc2_full;
-                const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : P.num_kb + (P.lora_k16 ? 1 : 0);
+                const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : nmain + (P.lora_k16 ? 1 : 0);
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb) {
                     // FP8 pairs: the peer's converted half is published by a cluster-scope release
@@ -511,14 +525,21 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                                 tc::mma_bf16(d, ad, bd, idesc, (kb > 0 || j > 0 || kk > 0) ? 1u : 0u);
                             }
                         }
-                    } else if (kb < P.num_kb) {
+                    } else if (kb < nmain) {
+                        const int nsub = min(KB2, P.num_kb - kb * KB2);
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk) {
-                            const uint64_t ad = tc::smem_desc(sa + kk * 32, 16, 1024, tc::kSw128);
-                            const uint64_t bd = B_MN ? tc::smem_desc(sb + kk * 2048, kBoxMN, 1024, tc::kSw128)
-                                                     : tc::smem_desc(sb + kk * 32, 16, 1024, tc::kSw128);
-                            if constexpr (PAIR) tc::mma_bf16_pair(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                            else tc::mma_bf16(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        for (int j = 0; j < KB2; ++j) {
+                            if (j >= nsub) break;
+                            const uint32_t saj = sa + j * G::kSubBytes, sbj = saj + kABytes;
+#pragma unroll
+                            for (int kk = 0; kk < BK / 16; ++kk) {
+                                const uint64_t ad = tc::smem_desc(saj + kk * 32, 16, 1024, tc::kSw128);
+                                const uint64_t bd = B_MN ? tc::smem_desc(sbj + kk * 2048, kBoxMN, 1024, tc::kSw128)
+                                                         : tc::smem_desc(sbj + kk * 32, 16, 1024, tc::kSw128);
+                                const uint32_t acc_in = (kb > 0 || j > 0 || kk > 0) ? 1u : 0u;
+                                if constexpr (PAIR) tc::mma_bf16_pair(d, ad, bd, idesc, acc_in);
+                                else tc::mma_bf16(d, ad, bd, idesc, acc_in);
+                            }
                         }
                     } else {
                         for (int kk = 0; kk < P.lora_k16; ++kk) {
@@ -839,10 +860,10 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 int e, mt, nt;
                 decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
                 const bool half = PAIR && half_tile(s_off, e, mt);
-                const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : P.num_kb + (P.lora_k16 ? 1 : 0);
+                const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : nmain + (P.lora_k16 ? 1 : 0);
                 for (int kb = 0; kb < nkb && f < f_max; ++kb, ++f) {
                     const int st = f % kStages;
-                    const bool main = G::KW > 1 || kb < P.num_kb;     // not the LoRA step
+                    const bool main = G::KW > 1 || kb < nmain;        // not the LoRA step
                     const uint32_t spar = (sbits >> st) & 1u;
                     int gi = 0;                                       // index among its group's code stages
                     if (Q8 && main) {
@@ -855,7 +876,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                     // bytes that one CTA's copies of this fill complete on the full barrier
                     uint32_t b;
                     if (G::KW > 1) b = min(G::KW, P.num_kb - kb * G::KW) * (kABytes + BN * BK * 2);
-                    else if (main) b = (half ? kABytes / 2 : kABytes) + (Q8 ? 0 : G::kBBytes);
+                    else if (main) b = ((half ? kABytes / 2 : kABytes) + (Q8 ? 0 : G::kBBytes)) * min(KB2, P.num_kb - kb * KB2);
                     else b = (half ? P.a2_bytes / 2 : P.a2_bytes) + (PAIR ? 2 : 4) * P.b2_box_bytes;
                     const bool lp = f < f_lead, pp = PAIR && f < f_peer;
                     if (!lp && !pp) continue;                         // no copy went towards this phase
