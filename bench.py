@@ -103,10 +103,10 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
 # DRAM bytes (read + write) per launch from ncu captures of the current kernels
 # (profiles/), keyed by (workload, kernel); None where no capture of the current code exists.
 MEASURED_TRAFFIC = {
-    ("gptoss20b", "gemm_gate_up_fwd"): 1.1739e9 + 0.2629e9,
-    ("gptoss20b", "gemm_down_fwd"): 0.6334e9 + 0.0801e9,
-    ("gptoss20b", "gemm_down_bwd"): 0.8349e9 + 0.1645e9,
-    ("gptoss20b", "gemm_gate_up_bwd"): 1.3212e9 + 0.1741e9,
+    ("gptoss20b", "gemm_gate_up_fwd"): 1.1687e9 + 0.2635e9,
+    ("gptoss20b", "gemm_down_fwd"): 0.6341e9 + 0.0807e9,
+    ("gptoss20b", "gemm_down_bwd"): 0.8410e9 + 0.1647e9,
+    ("gptoss20b", "gemm_gate_up_bwd"): 1.3230e9 + 0.1761e9,
 }
 
 
