@@ -12,6 +12,7 @@
 // CTA = 10 warps, one CTA per SM, grid = #SMs:
 //   warp 0      TMA producer (one lane): A [128 x 64] and B [256 x 64] per stage,
 //               4 stages of 48 KB, 128-byte swizzle; the LoRA step loads A2 / B2
+//               (SM pairs: 3 stages of two 32 KB k-blocks, see Geo)
 //   warp 1      TMEM allocator + MMA issuer (one lane): 4 x tcgen05.mma
 //               M=128 N=256 K=16 per stage into one of two 256-column fp32
 //               accumulators (double buffer: the epilogue of tile i overlaps
@@ -67,8 +68,9 @@ struct Geo {
     static constexpr int kQBytes = Q8 ? kBBytes / 2 : 0;
     // bf16 SM pairs take two 64-deep k-blocks per ring stage: one barrier wait, 8 MMAs
     // and one commit per stage.  Each wait-and-commit cycle costs the tensor pipe a fixed
-    // ~0.13 us, a third of a 64-deep stage of 256 x 256 MMAs (measured: 16-18 % faster
-    // GEMMs than six 64-deep stages).
+    // ~0.13 us, a third of a 64-deep stage of 256 x 256 MMAs (measured without loads or
+    // epilogue: gate_up forward 0.327 vs 0.373 ms with six 64-deep stages; with them the
+    // step is 1-2 % faster).
     static constexpr int KB2 = (PAIR && !Q8) ? 2 : 1;
     static constexpr int kSubBytes = kABytes * KW + ((kBBytes + 1023) / 1024) * 1024;   // one k-block
     static constexpr int kStageBytes = KB2 * kSubBytes;
