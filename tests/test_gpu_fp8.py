@@ -35,8 +35,10 @@ def test_quantizer_bit_exact_against_oracle():
             assert np.array_equal(sc[e].cpu().numpy(), scales)
 
 
+# Every FP8 launch runs on SM pairs.  The bf16 reference runs on single-CTA tiles for the
+# first case (about 233 rows per expert) and on SM pairs for the others.
 CASES = {
-    "ragged_single": mi.MoEConfig("ragged", T=700, H=256, E=6, k=2, I=320, r=16, alpha=32),
+    "ragged_bf16_single_cta": mi.MoEConfig("ragged", T=700, H=256, E=6, k=2, I=320, r=16, alpha=32),
     "pairs_ragged": mi.MoEConfig("pairs", T=1000, H=256, E=4, k=2, I=320, r=16, alpha=32),
     "tiny_r8": mi.CONFIGS["tiny"],
     # ~3 tiles per SM pair: the converters carry their stage parity across tiles and
@@ -78,7 +80,7 @@ def test_fp8_layer_is_bit_identical_to_bf16_on_dequantized_weights(name):
 
 
 
-@pytest.mark.parametrize("name", ["ragged_single", "pairs_ragged"])
+@pytest.mark.parametrize("name", ["ragged_bf16_single_cta", "pairs_ragged"])
 def test_fp8_extreme_column_scales_bit_identical(name):
     """Columns whose power-of-two scale is far from 1: above 2^7 (the dequantising
     multiply is split in two), below fp32's normal range (a subnormal scale), and tiny
