@@ -245,7 +245,9 @@ MOE_API moe_status moe_quantize_fp8(const uint16_t* W, int64_t n_mat, int64_t ro
  * The GEMMs stream the codes (half the bytes of bf16) and dequantise them to bf16 in
  * shared memory before the tensor cores read them, so the results are bit-identical to
  * moe_lora_fwd / moe_lora_bwd called with the dequantised bf16 weights.  The LoRA
- * factors and activations stay bf16.  Same saved / workspace sizes. */
+ * factors and activations stay bf16.  Same saved / workspace sizes.  The expert GEMMs
+ * run on SM pairs (2-CTA clusters, each CTA dequantising half of a B tile); on a device
+ * where no such cluster fits, the calls return MOE_ERR_CUDA. */
 MOE_API moe_status moe_lora_fwd_fp8(const moe_dims* d, const moe_routing* rt, const uint16_t* x,
                                     const uint8_t* Wq_gu, const float* s_gu,
                                     const uint16_t* A_gu, const uint16_t* B_gu,

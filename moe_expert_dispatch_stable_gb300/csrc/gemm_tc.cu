@@ -239,6 +239,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
     constexpr bool PAIRED = (EPI == EPI_SWIGLU);
     using G = Geo<BN, PAIR, Q8>;
     static_assert(!Q8 || BN == 256, "FP8 weights are for the expert GEMMs");
+    static_assert(!Q8 || PAIR, "FP8 weights run on SM pairs (each CTA dequantises half of the B tile)");
     constexpr int kStages = G::kStages;
     constexpr int kStageBytes = G::kStageBytes;
     constexpr int kAccCols = G::kAccCols;
@@ -431,22 +432,9 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                             tc::tma_load_3d(sa + G::KW * kABytes + j * (BN * BK * 2), &P.tm_b, fb, kx, nt * BN, e);
                         }
                     } else {
+                        // single-CTA tile (bf16 weights only)
                         const uint32_t fb = fb_local;
-                        if (kb < nmain && Q8) {
-                            tc::mbar_arrive_expect_tx(fb, kABytes);
-                            tc::tma_load_2d(sa, &P.tm_a, fb, kb * BK, m0);
-                            const uint32_t sq = sb + G::kQBytes;
-                            const uint32_t qb = tc::smem_u32(&staged_bar[stage]);
-                            tc::mbar_arrive_expect_tx(qb, G::kQBytes);
-                            if (B_MN) {
-#pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    tc::tma_load_3d(sq + j * (kBoxMN / 2), &P.tm_b, qb, b_col<PAIRED, BN>(j, nt, g.Ncols),
-                                                    kb * BK, e);
-                            } else {
-                                tc::tma_load_3d(sq, &P.tm_b, qb, kb * BK, nt * BN, e);
-                            }
-                        } else if (kb < nmain) {
+                        if (kb < nmain) {
                             tc::mbar_arrive_expect_tx(fb, kABytes + G::kBBytes);
                             tc::tma_load_2d(sa, &P.tm_a, fb, kb * BK, m0);
                             if (B_MN) {
@@ -459,7 +447,6 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                             }
                         } else {
                             tc::mbar_arrive_expect_tx(fb, P.a2_bytes + 4 * P.b2_box_bytes);
-                            if (Q8) tc::mbar_arrive(fb);     // FP8: no conversion, both arrivals here
                             tc::tma_load_2d(sa, &P.tm_a2, fb, 0, m0);
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
@@ -573,15 +560,15 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             constexpr int kGT = 32 * (kConvWarps / kConvGroups);    // threads of one group
             constexpr int kUnits = G::kQBytes / 8;                  // 8 codes per unit
             constexpr int kIters = kUnits / kGT;
-            constexpr int kBoxes = B_MN ? (PAIR ? 2 : 4) : 1;
+            constexpr int kBoxes = B_MN ? 2 : 1;                   // 64-column code boxes per CTA (SM pairs)
             static_assert(kUnits % kGT == 0 && 512 % kGT == 0, "units per stage must split evenly");
             static_assert(kStages % kConvGroups == 0, "every group owns whole stages");
             const int ct = threadIdx.x - 32 * (2 + kEpiWarps);
             const int grp = ct / kGT;
             const int gt = ct % kGT;
             const int cc = gt & 7;                                  // the thread's 16-byte chunk of a row
-            const uint32_t full_leader0 = PAIR ? tc::mapa(tc::smem_u32(&full_bar[0]), 0) : 0u;
-            const uint32_t sig_leader = PAIR ? tc::mapa(tc::smem_u32(sig_slot), 0) : 0u;
+            const uint32_t full_leader0 = tc::mapa(tc::smem_u32(&full_bar[0]), 0);
+            const uint32_t sig_leader = tc::mapa(tc::smem_u32(sig_slot), 0);
             int stage = 0;
             uint32_t sbits = 0;                                     // per-stage parity of staged_bar
             int done = 0;                                           // stages this group has signalled
@@ -598,8 +585,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                     // MN-major: a chunk's scales depend on its columns only, fixed for the tile
 #pragma unroll
                     for (int j = 0; j < kBoxes; ++j) {
-                        const int col = (PAIR ? b_col_pair<PAIRED, BN>(half_tile(s_off, e, mt), (int)rank, j, nt, g.Ncols)
-                                              : b_col<PAIRED, BN>(j, nt, g.Ncols)) + cc * 8;
+                        const int col = b_col_pair<PAIRED, BN>(half_tile(s_off, e, mt), (int)rank, j, nt, g.Ncols) + cc * 8;
                         const bool in = col < g.ldb;
                         const float4 a = in ? __ldg(reinterpret_cast<const float4*>(se + col)) : make_float4(0, 0, 0, 0);
                         const float4 b = in ? __ldg(reinterpret_cast<const float4*>(se + col) + 1) : make_float4(0, 0, 0, 0);
@@ -659,7 +645,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                         // wait for the stage to be free, so no arrival can reach an earlier phase.
                         tc::named_bar_sync(1 + grp, kGT);
                         if (gt == 0) {
-                            if (!PAIR || rank == 0) tc::mbar_arrive(tc::smem_u32(&full_bar[stage]));
+                            if (rank == 0) tc::mbar_arrive(tc::smem_u32(&full_bar[stage]));
                             else tc::st_async_signal(sig_leader, 1u, full_leader0 + stage * (uint32_t)sizeof(uint64_t));
                         }
                         ++done;
@@ -1110,13 +1096,9 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
             }
             return e;
         }
-        const size_t smem = Geo<256, false, true>::kSmem + offs_bytes;
-        switch (g.epi) {
-            case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256, false, true>(P, max_tiles, smem, s);
-            case EPI_BF16: return launch_tc<EPI_BF16, true, 256, false, true>(P, max_tiles, smem, s);
-            case EPI_DSWIGLU: return launch_tc<EPI_DSWIGLU, false, 256, false, true>(P, max_tiles, smem, s);
-            default: return launch_tc<EPI_PLAIN_F32, false, 256, false, true>(P, max_tiles, smem, s);
-        }
+        // FP8 weights run on SM pairs only: a device on which no 2-CTA cluster fits
+        // cannot run them
+        return cudaErrorNotSupported;
     }
     if (pair) {
         const size_t smem = Geo<256, true>::kSmem + offs_bytes;
