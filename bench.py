@@ -80,7 +80,7 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
         "gemm_down_bwd": dict(flops=2 * N * H * I + 2 * N * r * I,
                               bytes=b * (N * H + E * I * H + E * r * I + N * rp + N * 2 * I + N * 2 * I)),
         "gemm_gate_up_bwd": dict(flops=2 * N * 2 * I * H + 2 * N * r * H,
-                                 bytes=b * (N * 2 * I + E * H * 2 * I + E * r * H + N * rp) + 4 * N * H),
+                                 bytes=b * (N * 2 * I + E * H * 2 * I + E * r * H + N * rp + N * H)),
         "gather_x": dict(flops=0, bytes=b * (T * H + N * H) + 4 * N),
         "gather_dy": dict(flops=N * H, bytes=b * (T * H + N * H) + 8 * N),
         "proj_xa": dict(flops=2 * N * H * r, bytes=b * (N * H + E * r * H + N * rp)),
@@ -88,7 +88,7 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
         "proj_g": dict(flops=2 * N * H * r, bytes=b * (N * H + E * r * H + N * rp)),
         "proj_gg": dict(flops=2 * N * 2 * I * r, bytes=b * (N * 2 * I + E * r * 2 * I + N * rp)),
         "combine_y": dict(flops=N * H, bytes=b * N * H + b * T * H + 4 * N),
-        "combine_dx": dict(flops=N * H, bytes=4 * N * H + b * T * H + 4 * N),
+        "combine_dx": dict(flops=N * H, bytes=b * N * H + b * T * H + 4 * N),
         "wgrad_down": dict(flops=2 * N * r * I + 2 * N * r * H,
                            bytes=b * (2 * N * rp + N * I + N * H + E * r * I + E * r * H)),
         "wgrad_gate_up": dict(flops=2 * N * r * H + 2 * N * r * 2 * I,
@@ -103,10 +103,10 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
 # DRAM bytes (read + write) per launch from ncu captures of the current kernels
 # (profiles/), keyed by (workload, kernel); None where no capture of the current code exists.
 MEASURED_TRAFFIC = {
-    ("gptoss20b", "gemm_gate_up_fwd"): 1.1687e9 + 0.2635e9,
-    ("gptoss20b", "gemm_down_fwd"): 0.6341e9 + 0.0807e9,
-    ("gptoss20b", "gemm_down_bwd"): 0.8410e9 + 0.1647e9,
-    ("gptoss20b", "gemm_gate_up_bwd"): 1.3230e9 + 0.1761e9,
+    ("gptoss20b", "gemm_gate_up_fwd"): 1.1666e9 + 0.2620e9,
+    ("gptoss20b", "gemm_down_fwd"): 0.6311e9 + 0.0796e9,
+    ("gptoss20b", "gemm_down_bwd"): 0.8360e9 + 0.1637e9,
+    ("gptoss20b", "gemm_gate_up_bwd"): 1.3162e9 + 0.0861e9,
 }
 
 

@@ -147,7 +147,7 @@ BwdWs bwd_ws(const moe_dims* d) {
     W.g_s = o;     o = align_up(o + N * rp * 2, kAlign);
     W.dgu = o;     o = align_up(o + N * 2 * d->I * 2, kAlign);
     W.gg_s = o;    o = align_up(o + N * rp * 2, kAlign);
-    W.dx_perm = o; o = align_up(o + N * d->H * 4, kAlign);
+    W.dx_perm = o; o = align_up(o + N * d->H * 2, kAlign);
     W.total = o;
     return W;
 }
@@ -416,15 +416,16 @@ static moe_status bwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     }
     // Gg_s = s * dGU B_gu^T
     MOE_TRY(timed("proj_gg", s, [&] { return project(dGU, 2 * I, B_gu, r, L.rp, d->scale, rt, E, N, Gg, dev_status, s); }));
-    // dX_perm = dGU W_gu[e]^T + Gg_s A_gu[e]
+    // dX_perm = dGU W_gu[e]^T + Gg_s A_gu[e], one bf16 row per routed slot (like the forward's
+    // O rows); the combine sums a token's k slots in fp32
     GroupedGemm g2{};
     g2.N = N; g2.E = E; g2.offsets = rt->offsets; g2.tile_offsets = rt->tile_offsets; g2.dev_status = dev_status;
     g2.K = 2 * I; g2.Ncols = H; g2.A = dGU;
     g2.B = W_gu; g2.b_scale = s_gu; g2.b_mn_major = false; g2.ldb = 2 * I; g2.b_expert_stride = (int64_t)H * 2 * I;
     g2.A2 = Gg; g2.rp = L.rp; g2.r = r; g2.B2 = A_gu; g2.ldb2 = H; g2.b2_expert_stride = (int64_t)r * H;
-    g2.out0 = dXp; g2.ldo = H; g2.epi = EPI_PLAIN_F32;
+    g2.out0 = dXp; g2.ldo = H; g2.epi = EPI_BF16;
     MOE_TRY(timed("gemm_gate_up_bwd", s, [&] { return launch_grouped_gemm(g2, s); }));
-    MOE_TRY(timed("combine_dx", s, [&] { return launch_combine(dXp, true, nullptr, rt->inv_perm, d->T, d->k, H, dx, dev_status, s); }));
+    MOE_TRY(timed("combine_dx", s, [&] { return launch_combine(dXp, false, nullptr, rt->inv_perm, d->T, d->k, H, dx, dev_status, s); }));
     // dA_gu = Gg_s^T x_perm ; dB_gu = XA_s^T dGU
     {
         const WgradProblem wp[2] = {{Gg, x_perm, H, dA_gu}, {XA, dGU, 2 * I, dB_gu}};

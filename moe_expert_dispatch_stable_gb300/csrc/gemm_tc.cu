@@ -681,7 +681,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             // queued (the MMAs are busy with it, and this accumulator is not needed before the
             // tile after that) the plain-store epilogues spread their chunks 0.5 us apart
             // (measured: 2-10 % faster gate_up backward and down forward).
-            const bool pace = (EPI == EPI_BF16 || EPI == EPI_PLAIN_F32) && t + tile_step < total_tiles;
+            const bool pace = EPI == EPI_BF16 && t + tile_step < total_tiles;
             const int cb0 = htile ? hw * span : c0;
             const int nbase = htile ? (q >> 1) * (PAIRED ? BN / 4 : BN / 2) : 0;   // output column offset
             const int up_off = htile ? BN / 4 : BN / 2;                 // gate/up pairs: up's TMEM column - gate's
@@ -782,23 +782,6 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                     if (valid && n < g.Ncols) {
                         // read once by the combine and once by the backward: evict-first
                         tc::st32_cs(out + (int64_t)p * g.ldo + n, pack8_bf16(v), pack8_bf16(v + 8));
-                    }
-                }
-            } else {
-                float* out = (float*)g.out0;
-#pragma unroll 1
-                for (int c = cb0; c < cb0 + span; c += 16) {
-                    if (pace && c != cb0) __nanosleep(kPaceNs);
-                    float v[16];
-                    tc::tmem_ld16(tb + c, v);
-                    tc::tmem_ld_wait();
-                    const int n = nt * BN + nbase + c;
-                    if (valid && n < g.Ncols) {
-                        float* o = out + (int64_t)p * g.ldo + n;
-                        const uint4* u = reinterpret_cast<const uint4*>(v);
-                        // read once by the combine: evict-first
-                        tc::st32_cs(o, u[0], u[1]);
-                        tc::st32_cs(o + 8, u[2], u[3]);
                     }
                 }
             }
@@ -1016,8 +999,9 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
     // FP8 weights always run on SM pairs: each CTA dequantises half of the B tile
     const bool pair = allow_pairs && !proj && (q8 || use_sm_pairs(g));
     if (q8 && (proj || g.ldb % 64 != 0)) return cudaErrorInvalidValue;
-    // FP8 kernels exist for the layer's four GEMMs: MN-major B forward, K-major B backward
-    if (q8 && g.b_mn_major != (g.epi == EPI_SWIGLU || g.epi == EPI_BF16)) return cudaErrorInvalidValue;
+    // kernels exist for the layer's four expert GEMMs (below) and the projections
+    if (!proj && g.epi != EPI_SWIGLU && g.epi != EPI_BF16 && g.epi != EPI_DSWIGLU) return cudaErrorInvalidValue;
+    if (g.epi == EPI_DSWIGLU && g.b_mn_major) return cudaErrorInvalidValue;   // built for a K-major B only
     P.n_tiles = proj ? 1 : (paired ? (g.Ncols + 127) / 128 : (g.Ncols + 255) / 256);
     // A: [N, K]
     {
@@ -1083,41 +1067,29 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
             default: return launch_tc<EPI_PROJ, false, 64, false>(P, max_tiles, Geo<64>::kSmem + offs_bytes, s);
         }
     }
+    // The layer's expert GEMMs: gate_up forward (SwiGLU, MN-major B), down forward (bf16,
+    // MN-major B), down backward (SwiGLU backward, K-major B: W_d read transposed) and
+    // gate_up backward (bf16, K-major B: W_gu read transposed).
     if (q8) {
-        // FP8 weights: the forward GEMMs take an MN-major B, the backward ones a K-major B
-        cudaError_t e;
-        if (pair) {
-            const size_t smem = Geo<256, true, true>::kSmem + offs_bytes;
-            switch (g.epi) {
-                case EPI_SWIGLU: e = launch_tc<EPI_SWIGLU, true, 256, true, true>(P, max_tiles, smem, s); break;
-                case EPI_BF16: e = launch_tc<EPI_BF16, true, 256, true, true>(P, max_tiles, smem, s); break;
-                case EPI_DSWIGLU: e = launch_tc<EPI_DSWIGLU, false, 256, true, true>(P, max_tiles, smem, s); break;
-                default: e = launch_tc<EPI_PLAIN_F32, false, 256, true, true>(P, max_tiles, smem, s);
-            }
-            return e;
+        if (!pair) return cudaErrorNotSupported;   // FP8 weights run on SM pairs only
+        const size_t smem = Geo<256, true, true>::kSmem + offs_bytes;
+        switch (g.epi) {
+            case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256, true, true>(P, max_tiles, smem, s);
+            case EPI_BF16:
+                return mn ? launch_tc<EPI_BF16, true, 256, true, true>(P, max_tiles, smem, s)
+                          : launch_tc<EPI_BF16, false, 256, true, true>(P, max_tiles, smem, s);
+            default: return launch_tc<EPI_DSWIGLU, false, 256, true, true>(P, max_tiles, smem, s);
         }
-        // FP8 weights run on SM pairs only: a device on which no 2-CTA cluster fits
-        // cannot run them
-        return cudaErrorNotSupported;
     }
     if (pair) {
         const size_t smem = Geo<256, true>::kSmem + offs_bytes;
-        cudaError_t e;
         switch (g.epi) {
-            case EPI_SWIGLU: e = launch_tc<EPI_SWIGLU, true, 256, true>(P, max_tiles, smem, s); break;
+            case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256, true>(P, max_tiles, smem, s);
             case EPI_BF16:
-                e = mn ? launch_tc<EPI_BF16, true, 256, true>(P, max_tiles, smem, s)
-                       : launch_tc<EPI_BF16, false, 256, true>(P, max_tiles, smem, s);
-                break;
-            case EPI_DSWIGLU:
-                e = mn ? launch_tc<EPI_DSWIGLU, true, 256, true>(P, max_tiles, smem, s)
-                       : launch_tc<EPI_DSWIGLU, false, 256, true>(P, max_tiles, smem, s);
-                break;
-            default:
-                e = mn ? launch_tc<EPI_PLAIN_F32, true, 256, true>(P, max_tiles, smem, s)
-                       : launch_tc<EPI_PLAIN_F32, false, 256, true>(P, max_tiles, smem, s);
+                return mn ? launch_tc<EPI_BF16, true, 256, true>(P, max_tiles, smem, s)
+                          : launch_tc<EPI_BF16, false, 256, true>(P, max_tiles, smem, s);
+            default: return launch_tc<EPI_DSWIGLU, false, 256, true>(P, max_tiles, smem, s);
         }
-        return e;
     }
     const size_t smem = Geo<256>::kSmem + offs_bytes;
     switch (g.epi) {
@@ -1125,12 +1097,7 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
         case EPI_BF16:
             return mn ? launch_tc<EPI_BF16, true, 256, false>(P, max_tiles, smem, s)
                       : launch_tc<EPI_BF16, false, 256, false>(P, max_tiles, smem, s);
-        case EPI_DSWIGLU:
-            return mn ? launch_tc<EPI_DSWIGLU, true, 256, false>(P, max_tiles, smem, s)
-                      : launch_tc<EPI_DSWIGLU, false, 256, false>(P, max_tiles, smem, s);
-        default:
-            return mn ? launch_tc<EPI_PLAIN_F32, true, 256, false>(P, max_tiles, smem, s)
-                      : launch_tc<EPI_PLAIN_F32, false, 256, false>(P, max_tiles, smem, s);
+        default: return launch_tc<EPI_DSWIGLU, false, 256, false>(P, max_tiles, smem, s);
     }
 }
 

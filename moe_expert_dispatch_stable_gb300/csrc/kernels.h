@@ -76,7 +76,6 @@ enum GemmEpi : int {
     EPI_SWIGLU = 0,     // paired gate/up accumulators -> GU (bf16, [N,2I]) and h (bf16, [N,I])
     EPI_BF16 = 1,       // out_bf16[p, n] = acc
     EPI_DSWIGLU = 2,    // acc = dh; reads GU, writes dGU (bf16 [N,2I])
-    EPI_PLAIN_F32 = 3,  // out_f32[p, n] = acc
     EPI_PROJ = 4        // out_bf16[p, 0:Ncols] = scale * acc  (rank-r projection, Ncols = RP)
 };
 
@@ -103,9 +102,9 @@ struct GroupedGemm {
     const int32_t* offsets;      // [E+1]
     const int32_t* tile_offsets; // [E+1], 128-row tiles
     const void* gu_in;           // EPI_DSWIGLU: GU [N, 2*Ncols]
-    void* out0;                  // EPI_SWIGLU: GU; EPI_DSWIGLU: dGU; BF16: bf16 out; PLAIN_F32: fp32 out
+    void* out0;                  // EPI_SWIGLU: GU; EPI_DSWIGLU: dGU; BF16: bf16 out
     void* out1;                  // EPI_SWIGLU: h
-    int ldo;                     // row length of the BF16 / PLAIN_F32 output
+    int ldo;                     // row length of the BF16 output
     float scale;                 // EPI_PROJ
     int epi;
     int32_t* dev_status;

@@ -57,7 +57,9 @@ def test_size_queries_and_dim_checks(lib):
     assert saved >= N * 2880 * 2 + N * 5760 * 2 + N * 2880 * 2 + 2 * N * 16 * 2
     assert ws == 0                                          # the forward keeps everything in `saved`
     assert saved >= N * (2880 * 2 + 5760 * 2 + 2880 * 2 + 2 * 16 * 2 + 2880 * 2)
-    assert b.moe_lora_bwd_workspace_size(ok) >= N * (2880 * 2 + 5760 * 2 + 2880 * 4)
+    # dO, G_s, dGU, Gg_s and the bf16 dX rows of the routed slots
+    bws = b.moe_lora_bwd_workspace_size(ok)
+    assert N * (2880 * 2 + 16 * 2 + 5760 * 2 + 16 * 2 + 2880 * 2) <= bws <= N * (2880 * 2 + 16 * 2 + 5760 * 2 + 16 * 2 + 2880 * 2) + 5 * 256
     offs, rp = b.moe_lora_saved_layout(ok)
     assert rp == 16 and offs[0] == 0 and all(o % 256 == 0 for o in offs) and offs == sorted(offs)
     assert b.moe_lora_saved_layout(b.Dims(64, 128, 256, 8, 2, 8, 2.0))[1] == 16
