@@ -21,6 +21,17 @@ def test_kernel_flops_add_up_to_layer_flops(name):
             assert w[k]["bound"] == "hbm"
 
 
+def test_slot_rows_are_bf16_in_the_byte_model():
+    # the forward's O rows and the backward's dX rows are both one bf16 row per routed slot,
+    # so the two combines move the same bytes, and the gate_up backward writes N*H*2 bytes
+    cfg = mi.CONFIGS["gptoss20b"]
+    w = bench.kernel_work(cfg)
+    assert w["combine_dx"]["bytes"] == w["combine_y"]["bytes"]
+    N, H, I, E, r = cfg.T * cfg.k, cfg.H, cfg.I, cfg.E, cfg.r
+    assert w["gemm_gate_up_bwd"]["bytes"] == 2 * (N * 2 * I + E * H * 2 * I + E * r * H + N * 16 + N * H)
+    assert abs(w["gemm_gate_up_bwd"]["bytes"] / 1e9 - 1.348) < 1e-3
+
+
 def test_step_flops_matches_closed_form_for_gptoss20b():
     cfg = mi.CONFIGS["gptoss20b"]
     N = cfg.T * cfg.k
