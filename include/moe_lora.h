@@ -184,6 +184,15 @@ MOE_API moe_status moe_lora_saved_layout(const moe_dims* d, size_t offsets[6], i
 MOE_API moe_status moe_lora_saved_regather(const moe_dims* d, const moe_routing* rt, const uint16_t* x, void* saved,
                                            size_t saved_bytes, void* stream);
 
+/* Re-create the h section of `saved` from its GU section: h = silu(g) * u row by row,
+ * with g, u the stored bf16 values, fp32 arithmetic and round to nearest bf16.  That is
+ * how moe_lora_fwd_h_from_gu forms h, so after that forward the result is bit-identical
+ * to what it wrote (after moe_lora_fwd, whose h comes from the unrounded accumulators,
+ * it is close but not identical).  For a caller that moves GU, XA_s and HA_s between
+ * forward and backward but not h.  `saved` as for moe_lora_fwd; only h is written.
+ * Asynchronous on `stream`. */
+MOE_API moe_status moe_lora_saved_rebuild_h(const moe_dims* d, void* saved, size_t saved_bytes, void* stream);
+
 /* Forward of the MoE-LoRA expert layer (Split-LoRA, SwiGLU, weighted combine).
  *  x     [T, H]                  W_gu [E, H, 2I] (gate = cols [0,I), up = [I,2I))
  *  A_gu  [E, r, H] (A^T, the PEFT lora_A layout)   B_gu [E, r, 2I]
@@ -191,6 +200,7 @@ MOE_API moe_status moe_lora_saved_regather(const moe_dims* d, const moe_routing*
  *  y     [T, H] output, bf16
  * For every slot (t, j) with e = topk_idx[t, j]:
  *   GU = x[t] W_gu[e] + s (x[t] A_gu[e]^T) B_gu[e];  h = silu(GU[:I]) * GU[I:]
+ *   (h from the fp32 accumulators; GU and h are then stored in bf16)
  *   o  = h W_d[e] + s (h A_d[e]^T) B_d[e];           y[t] = sum_j w[t,j] o_j
  * with bf16 operands, fp32 accumulation, and the k slots of a token summed in
  * the fixed order j = 0..k-1 (bitwise reproducible).  The forward needs no
@@ -203,6 +213,16 @@ MOE_API moe_status moe_lora_fwd(const moe_dims* d, const moe_routing* rt,
                         void* saved, size_t saved_bytes,
                         void* workspace, size_t workspace_bytes,
                         int32_t* dev_status, void* stream);
+
+/* moe_lora_fwd, except that h is formed from the gate and up values as stored (rounded
+ * to bf16) instead of from the fp32 accumulators, so that moe_lora_saved_rebuild_h can
+ * re-create h bit for bit from GU alone.  For a caller that offloads the saved
+ * activations and moves h neither way; same arguments and sizes as moe_lora_fwd. */
+MOE_API moe_status moe_lora_fwd_h_from_gu(const moe_dims* d, const moe_routing* rt, const uint16_t* x,
+                                          const uint16_t* W_gu, const uint16_t* A_gu, const uint16_t* B_gu,
+                                          const uint16_t* W_d, const uint16_t* A_d, const uint16_t* B_d, uint16_t* y,
+                                          void* saved, size_t saved_bytes, void* workspace, size_t workspace_bytes,
+                                          int32_t* dev_status, void* stream);
 
 /* ---------------------------------------------------------------- backward */
 MOE_API moe_status moe_lora_bwd_workspace_size(const moe_dims* d, size_t* bytes);

@@ -43,11 +43,11 @@ class moe_routing(ctypes.Structure):
 
 
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_launch_count", "moe_route_workspace_size", "moe_route",
-            "moe_lora_fwd_sizes", "moe_lora_saved_layout", "moe_lora_saved_regather", "moe_lora_fwd",
+            "moe_lora_fwd_sizes", "moe_lora_saved_layout", "moe_lora_saved_regather", "moe_lora_saved_rebuild_h", "moe_lora_fwd", "moe_lora_fwd_h_from_gu",
             "moe_lora_bwd_workspace_size", "moe_lora_bwd", "moe_timing_enable", "moe_timing_read",
             "moe_router_topk", "moe_router_bwd", "moe_quantize_fp8", "moe_lora_fwd_fp8", "moe_lora_bwd_fp8",
             "moe_packed_metadata", "moe_packed_causal_mask", "moe_diag_force_timeout")
-ABI_VERSION = 5
+ABI_VERSION = 6
 
 _libs: dict = {}
 _default_path = LIB_PATH
@@ -73,7 +73,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.moe_lora_fwd_sizes.argtypes = [P(moe_dims), P(sz), P(sz)]
     lib.moe_lora_saved_layout.argtypes = [P(moe_dims), P(sz), P(i32)]
     lib.moe_lora_saved_regather.argtypes = [P(moe_dims), P(moe_routing), vp, vp, sz, vp]
+    lib.moe_lora_saved_rebuild_h.argtypes = [P(moe_dims), vp, sz, vp]
     lib.moe_lora_fwd.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 8 + [vp, sz, vp, sz, vp, vp]
+    lib.moe_lora_fwd_h_from_gu.argtypes = lib.moe_lora_fwd.argtypes
     lib.moe_lora_bwd_workspace_size.argtypes = [P(moe_dims), P(sz)]
     lib.moe_lora_bwd.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 7 + [vp, sz] + [vp] * 6 + [vp, sz, vp, vp]
     lib.moe_router_topk.argtypes = [vp, i64, i32, i32, vp, vp, vp]
@@ -225,6 +227,13 @@ def moe_lora_saved_regather(d: Dims, rt: "Routing", x, saved, stream=None):
                                                   saved.numel() * saved.element_size(), _stream(stream)))
 
 
+def moe_lora_saved_rebuild_h(d: Dims, saved, stream=None):
+    """Re-create the h section of `saved` from its GU section (bit-identical to the forward's h)."""
+    dd = d.c_struct()
+    _check(load_library().moe_lora_saved_rebuild_h(ctypes.byref(dd), _ptr(saved), saved.numel() * saved.element_size(),
+                                                   _stream(stream)))
+
+
 def moe_lora_bwd_workspace_size(d: Dims) -> int:
     n = ctypes.c_size_t()
     _check(load_library().moe_lora_bwd_workspace_size(ctypes.byref(d.c_struct()), ctypes.byref(n)))
@@ -242,8 +251,9 @@ def _check_weights(d: Dims, W_gu, A_gu, B_gu, W_d, A_d, B_d):
 
 
 def moe_lora_fwd(d: Dims, rt: Routing, x, W_gu, A_gu, B_gu, W_d, A_d, B_d, y=None, saved=None,
-                 workspace=None, dev_status=None, stream=None):
-    """Forward of the layer; returns (y, saved)."""
+                 workspace=None, dev_status=None, stream=None, h_from_gu=False):
+    """Forward of the layer; returns (y, saved).  h_from_gu: form h from the stored bf16
+    GU (moe_lora_fwd_h_from_gu), so that moe_lora_saved_rebuild_h can re-create it."""
     lib = load_library()
     _need(x, "x", torch.bfloat16, (d.T, d.H))
     _check_weights(d, W_gu, A_gu, B_gu, W_d, A_d, B_d)
@@ -259,9 +269,10 @@ def moe_lora_fwd(d: Dims, rt: Routing, x, W_gu, A_gu, B_gu, W_d, A_d, B_d, y=Non
         dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
     _need(y, "y", torch.bfloat16, (d.T, d.H))
     dd, rr = d.c_struct(), rt.c_struct()
-    _check(lib.moe_lora_fwd(ctypes.byref(dd), ctypes.byref(rr), _ptr(x), _ptr(W_gu), _ptr(A_gu), _ptr(B_gu),
-                            _ptr(W_d), _ptr(A_d), _ptr(B_d), _ptr(y), _ptr(saved), saved.numel(),
-                            _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream)))
+    fn = lib.moe_lora_fwd_h_from_gu if h_from_gu else lib.moe_lora_fwd
+    _check(fn(ctypes.byref(dd), ctypes.byref(rr), _ptr(x), _ptr(W_gu), _ptr(A_gu), _ptr(B_gu),
+              _ptr(W_d), _ptr(A_d), _ptr(B_d), _ptr(y), _ptr(saved), saved.numel(),
+              _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream)))
     return y, saved
 
 
@@ -496,11 +507,14 @@ def moe_timing_read() -> dict:
 
 class MoELoRALayer:
     """Preallocated buffers for repeated route + forward + backward calls on one
-    stream (no allocation inside a step, so a step can be graph-captured)."""
+    stream (no allocation inside a step, so a step can be graph-captured).
+    h_from_gu: bf16 weights only; the forward forms h from the stored bf16 GU
+    (moe_lora_fwd_h_from_gu), as the offloaded stack does."""
 
-    def __init__(self, d: Dims, weights: dict, device="cuda"):
+    def __init__(self, d: Dims, weights: dict, device="cuda", h_from_gu=False):
         self.d = d
         self.w = weights
+        self.h_from_gu = h_from_gu
         self.fp8 = "Wq_gu" in weights          # FP8 base weights (quantize_expert_weights)
         dev = torch.device(device)
         self.rt = Routing.empty(d.T, d.k, d.E, dev)
@@ -528,7 +542,8 @@ class MoELoRALayer:
             return moe_lora_fwd_fp8(self.d, self.rt, x, self.w, self.y, self.saved, self.fwd_ws, self.dev_status,
                                     stream)
         return moe_lora_fwd(self.d, self.rt, x, *self._wts(), y=self.y, saved=self.saved,
-                            workspace=self.fwd_ws, dev_status=self.dev_status, stream=stream)[0]
+                            workspace=self.fwd_ws, dev_status=self.dev_status, stream=stream,
+                            h_from_gu=self.h_from_gu)[0]
 
     def backward(self, dy, stream=None, with_topk_grad=True):
         dtw = self.d_topk_w if with_topk_grad else None

@@ -183,7 +183,7 @@ DiagWait moe::diag_next_single_cta_launch() {
 
 extern "C" {
 
-int32_t moe_abi_version(void) { return 5; }
+int32_t moe_abi_version(void) { return 6; }
 
 const char* moe_status_string(moe_status s) {
     switch (s) {
@@ -282,6 +282,21 @@ moe_status moe_lora_saved_regather(const moe_dims* d, const moe_routing* rt, con
     return MOE_OK;
 }
 
+moe_status moe_lora_saved_rebuild_h(const moe_dims* d, void* saved, size_t saved_bytes, void* stream) {
+    moe_status st = check_dims(d);
+    if (st != MOE_OK) return st;
+    const int64_t N = d->T * (int64_t)d->k;
+    if (N > 0 && saved == nullptr) return MOE_ERR_NULL_ARG;
+    if (!aligned32(saved)) return MOE_ERR_MISALIGNED;
+    const SavedLayout L = saved_layout(d);
+    if (saved_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (N == 0) return MOE_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t* sv = static_cast<uint8_t*>(saved);
+    MOE_TRY(timed("rebuild_h", s, [&] { return launch_swiglu_rows(sv + L.gu, d->I, N, sv + L.h, s); }));
+    return MOE_OK;
+}
+
 moe_status moe_lora_bwd_workspace_size(const moe_dims* d, size_t* bytes) {
     moe_status st = check_dims(d);
     if (st != MOE_OK) return st;
@@ -296,7 +311,7 @@ static moe_status fwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
                            const float* s_gu, const uint16_t* A_gu, const uint16_t* B_gu, const void* W_d,
                            const float* s_d, const uint16_t* A_d, const uint16_t* B_d, uint16_t* y, void* saved,
                            size_t saved_bytes, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                           void* stream) {
+                           void* stream, bool h_from_gu = false) {
     if (!aligned16(s_gu) || !aligned16(s_d)) return MOE_ERR_MISALIGNED;
     moe_status st = check_dims(d);
     if (st != MOE_OK) return st;
@@ -334,7 +349,7 @@ static moe_status fwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     g.K = H; g.Ncols = I; g.A = x_perm;
     g.B = W_gu; g.b_scale = s_gu; g.b_mn_major = true; g.ldb = 2 * I; g.b_expert_stride = (int64_t)H * 2 * I;
     g.A2 = XA; g.rp = L.rp; g.r = r; g.B2 = B_gu; g.ldb2 = 2 * I; g.b2_expert_stride = (int64_t)r * 2 * I;
-    g.out0 = GU; g.out1 = h; g.epi = EPI_SWIGLU;
+    g.out0 = GU; g.out1 = h; g.epi = EPI_SWIGLU; g.h_from_gu = h_from_gu ? 1 : 0;
     MOE_TRY(timed("gemm_gate_up_fwd", s, [&] { return launch_grouped_gemm(g, s); }));
 
     MOE_TRY(timed("proj_ha", s, [&] { return project(h, I, A_d, r, L.rp, d->scale, rt, E, N, HA, dev_status, s); }));
@@ -440,6 +455,14 @@ moe_status moe_lora_fwd(const moe_dims* d, const moe_routing* rt, const uint16_t
                         size_t workspace_bytes, int32_t* dev_status, void* stream) {
     return fwd_impl(d, rt, x, W_gu, nullptr, A_gu, B_gu, W_d, nullptr, A_d, B_d, y, saved, saved_bytes, workspace,
                     workspace_bytes, dev_status, stream);
+}
+
+moe_status moe_lora_fwd_h_from_gu(const moe_dims* d, const moe_routing* rt, const uint16_t* x, const uint16_t* W_gu,
+                                  const uint16_t* A_gu, const uint16_t* B_gu, const uint16_t* W_d, const uint16_t* A_d,
+                                  const uint16_t* B_d, uint16_t* y, void* saved, size_t saved_bytes, void* workspace,
+                                  size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    return fwd_impl(d, rt, x, W_gu, nullptr, A_gu, B_gu, W_d, nullptr, A_d, B_d, y, saved, saved_bytes, workspace,
+                    workspace_bytes, dev_status, stream, true);
 }
 
 moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt, const uint16_t* dy, const uint16_t* W_gu,

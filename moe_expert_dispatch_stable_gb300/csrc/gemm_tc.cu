@@ -711,13 +711,23 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                     tc::tmem_ld_wait();
                     const int n = nt * (BN / 2) + nbase + c;
                     if (valid && n < I) {
+                        const uint4 g0 = pack8_bf16(gv), g1 = pack8_bf16(gv + 8);
+                        const uint4 u0 = pack8_bf16(uv), u1 = pack8_bf16(uv + 8);
+                        if (g.h_from_gu) {
+                            // h from the stored (bf16) gate and up values, so that
+                            // swiglu_rows rebuilds it bit for bit from GU alone
+                            unpack8_bf16(g0, gv);
+                            unpack8_bf16(g1, gv + 8);
+                            unpack8_bf16(u0, uv);
+                            unpack8_bf16(u1, uv + 8);
+                        }
                         float hv[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) hv[i] = swiglu_f(gv[i], uv[i]);
                         // one full 32-byte sector per thread and store; GU is only read again
                         // by the backward: stream it past L2 (evict-first)
-                        tc::st32_cs(GU + (int64_t)p * 2 * I + n, pack8_bf16(gv), pack8_bf16(gv + 8));
-                        tc::st32_cs(GU + (int64_t)p * 2 * I + I + n, pack8_bf16(uv), pack8_bf16(uv + 8));
+                        tc::st32_cs(GU + (int64_t)p * 2 * I + n, g0, g1);
+                        tc::st32_cs(GU + (int64_t)p * 2 * I + I + n, u0, u1);
                         tc::st32(Hh + (int64_t)p * I + n, pack8_bf16(hv), pack8_bf16(hv + 8));
                     }
                 }

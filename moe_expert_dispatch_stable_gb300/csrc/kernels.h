@@ -36,6 +36,8 @@ cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, cons
 // w_sorted is null); bf16 or fp32 src, fp32 sum in the fixed order j = 0..k-1
 cudaError_t launch_combine(const void* src, bool src_f32, const float* w_sorted, const int32_t* inv_perm, int64_t T,
                            int k, int H, void* out, int32_t* status, cudaStream_t s);
+// h [N, I] = SwiGLU of GU [N, 2I] row by row (bf16 in and out)
+cudaError_t launch_swiglu_rows(const void* gu, int I, int64_t N, void* h, cudaStream_t s);
 
 // ---- FP8 expert weights (quant.cu)
 // scale[m, c] = 2^ceil(log2(amax_r |W[m, r, c]| / 448)), Wq[m, r, c] = e4m3_rn(W[m, r, c] / scale[m, c])
@@ -106,6 +108,7 @@ struct GroupedGemm {
     void* out1;                  // EPI_SWIGLU: h
     int ldo;                     // row length of the BF16 output
     float scale;                 // EPI_PROJ
+    int h_from_gu;               // EPI_SWIGLU: h from the bf16-rounded gate / up values (as stored)
     int epi;
     int32_t* dev_status;
 };

@@ -3,6 +3,7 @@
 // the deterministic, routing-weighted per-token combine.  Both are HBM-bound,
 // with a couple of flops per element.
 #include "common.cuh"
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
 
@@ -238,6 +239,38 @@ __global__ void combine_kernel(const SrcT* __restrict__ src, const float* __rest
             if (u < units) tc::st32(out + t * H + (int64_t)u * 16, pack8(acc[i]), pack8(acc[i] + 8));
         }
     }
+}
+
+// ---------------------------------------------------------------- SwiGLU rows
+// h[p] = SwiGLU(GU[p]) for every sorted row, 8 columns per thread and step: the forward's
+// h rebuilt from the saved bf16 GU.  The gate_up epilogue forms h from the same bf16 gate
+// and up values with the same arithmetic (swiglu_f, round to nearest bf16), so the rows
+// are bit-identical to the ones it stored.
+__global__ void swiglu_rows_kernel(const uint4* __restrict__ gu, int i8, int64_t N, uint4* __restrict__ h) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t units = N * i8;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += step) {
+        const int64_t p = u / i8;
+        const int c = (int)(u - p * i8);
+        float g[8], v[8], o[8];
+        unpack8(__ldg(gu + p * 2 * i8 + c), g);
+        unpack8(__ldg(gu + p * 2 * i8 + i8 + c), v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = swiglu_f(g[j], v[j]);
+        h[p * i8 + c] = pack8(o);
+    }
+}
+
+cudaError_t launch_swiglu_rows(const void* gu, int I, int64_t N, void* h, cudaStream_t s) {
+    if (N == 0) return cudaSuccess;
+    if (I % 8 != 0) return cudaErrorInvalidValue;
+    const int threads = 256;
+    const int64_t units = N * (I / 8);
+    const int64_t blocks = std::min<int64_t>((units + threads - 1) / threads, (int64_t)num_sms() * 16);
+    return launch_pdl(swiglu_rows_kernel, dim3((unsigned)blocks), dim3(threads), 0, s, (const uint4*)gu, I / 8, N,
+                      (uint4*)h);
 }
 
 cudaError_t launch_combine(const void* src, bool src_f32, const float* w_sorted, const int32_t* inv_perm, int64_t T,

@@ -14,12 +14,15 @@ the backward walks the layers in reverse, reloading layer l-1's activations
 while layer l's backward runs.  Only stream-ordered copies and events are used:
 no host synchronisation inside forward() or backward().
 
-Only the sections the backward cannot rebuild exactly cross the host link: GU, h,
-XA_s and HA_s (contiguous in the saved layout).  x_perm is regathered on the device
-from the layer's input (moe_lora_saved_regather, bit-identical to the forward's
-gather), and O, which only the router's d topk_w reads, is not needed because the
-stack returns no router gradients.  That is 40 % fewer bytes for the
-GPT-OSS-20B-shaped layer, whose reload is bound by the ~200 GB/s host-to-device link.
+Only the sections the backward cannot rebuild exactly cross the host link: GU, XA_s
+and HA_s.  x_perm is regathered on the device from the layer's input
+(moe_lora_saved_regather, bit-identical to the forward's gather), h is rebuilt from GU
+(moe_lora_saved_rebuild_h: the stack's forward, moe_lora_fwd_h_from_gu, forms h from the
+stored bf16 GU with the same arithmetic, so the rebuild is bit-identical), and O, which
+only the router's d topk_w
+reads, is not needed because the stack returns no router gradients.  That is 60 % fewer
+bytes than the whole saved buffer for the GPT-OSS-20B-shaped layer, whose reload is
+bound by the ~200 GB/s host-to-device link.
 """
 from __future__ import annotations
 
@@ -81,9 +84,10 @@ class OffloadedMoEStack:
         saved_b, ws_b = B.moe_lora_fwd_sizes(d)
         self.saved_bytes = max(saved_b, 16)
         offs, _ = B.moe_lora_saved_layout(d)
-        # bytes [lo, hi) of `saved` cross the host link: GU, h, XA_s, HA_s
-        self.span = (offs[1], offs[5])
-        self.transfer_bytes = offs[5] - offs[1]
+        # the byte ranges [lo, hi) of `saved` that cross the host link: GU, then XA_s and
+        # HA_s (h, between them, is rebuilt on the device); packed back to back on the host
+        self.spans = [(offs[1], offs[2]), (offs[3], offs[5])]
+        self.transfer_bytes = sum(hi - lo for lo, hi in self.spans)
         if buffers == "auto":
             free, _ = torch.cuda.mem_get_info(dev)
             self.n_buf = choose_buffers(self.saved_bytes, free, reserve_bytes)
@@ -119,12 +123,14 @@ class OffloadedMoEStack:
             B.moe_route(routing[l][0], routing[l][1], self.d.E, out=self.rt[l], workspace=self.route_ws,
                         dev_status=self.dev_status)
             B.moe_lora_fwd(self.d, self.rt[l], x, *self._wts(l), y=self.y[l], saved=buf,
-                           workspace=self.fwd_ws, dev_status=self.dev_status)
+                           workspace=self.fwd_ws, dev_status=self.dev_status, h_from_gu=True)
             self._x_in[l] = x
-            lo, hi = self.span
             self.copy_stream.wait_stream(comp)
             with torch.cuda.stream(self.copy_stream):
-                self.host[l][:hi - lo].copy_(buf[lo:hi], non_blocking=True)
+                at = 0
+                for lo, hi in self.spans:
+                    self.host[l][at:at + hi - lo].copy_(buf[lo:hi], non_blocking=True)
+                    at += hi - lo
                 self._copied[l].record(self.copy_stream)
             x = self.y[l]
         return x
@@ -140,8 +146,10 @@ class OffloadedMoEStack:
                 self.copy_stream.wait_event(self._copied[step.layer])
                 if step.after >= 0:
                     self.copy_stream.wait_event(self._bwd_done[step.after])
-                lo, hi = self.span
-                self.bufs[step.buffer][lo:hi].copy_(self.host[step.layer][:hi - lo], non_blocking=True)
+                at = 0
+                for lo, hi in self.spans:
+                    self.bufs[step.buffer][lo:hi].copy_(self.host[step.layer][at:at + hi - lo], non_blocking=True)
+                    at += hi - lo
                 self._reloaded[step.layer].record(self.copy_stream)
 
         # prime the pipeline: as many reloads as there are buffers
@@ -152,6 +160,7 @@ class OffloadedMoEStack:
             step = by_layer[l]
             comp.wait_event(self._reloaded[l])
             B.moe_lora_saved_regather(self.d, self.rt[l], self._x_in[l], self.bufs[step.buffer])
+            B.moe_lora_saved_rebuild_h(self.d, self.bufs[step.buffer])
             B.moe_lora_bwd(self.d, self.rt[l], dy, *self._wts(l), self.bufs[step.buffer], dx=self.dx[l],
                            grads=self.grads[l], workspace=self.bwd_ws, dev_status=self.dev_status)
             self._bwd_done[l].record(comp)

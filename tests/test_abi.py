@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.moe_abi_version() == 5
+    assert lib.moe_abi_version() == 6
     for code in range(0, 7):
         assert lib.moe_status_string(code)
 
@@ -110,6 +110,10 @@ def test_null_and_misaligned_arguments_rejected_before_launch(lib):
     assert lib.moe_lora_saved_regather(ctypes.byref(d), ctypes.byref(rt), None, a32, 1 << 30, None) == 1
     assert lib.moe_lora_saved_regather(ctypes.byref(d), ctypes.byref(rt), a32, a16, 1 << 30, None) == 3
     assert lib.moe_lora_saved_regather(ctypes.byref(d), ctypes.byref(rt), a32, a32, 16, None) == 4
+    # rebuild of h: NULL / 16-byte aligned / too small saved buffer
+    assert lib.moe_lora_saved_rebuild_h(ctypes.byref(d), None, 1 << 30, None) == 1
+    assert lib.moe_lora_saved_rebuild_h(ctypes.byref(d), a16, 1 << 30, None) == 3
+    assert lib.moe_lora_saved_rebuild_h(ctypes.byref(d), a32, 16, None) == 4
     # misaligned d_topk_w
     assert lib.moe_lora_bwd(ctypes.byref(d), ctypes.byref(rt), a32, *wts, a32, 1 << 30,
                             a32, *[w16] * 4, ctypes.c_void_p(20), a32, 1 << 30, w16, None) == 3

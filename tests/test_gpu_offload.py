@@ -37,7 +37,7 @@ def test_offloaded_stack_is_bit_identical_to_resident(buffers, L):
     d = moe.Dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r, cfg.scale)
     weights, routing, x0, dy = _stack_inputs(cfg, L)
 
-    layers = [moe.MoELoRALayer(d, w) for w in weights]
+    layers = [moe.MoELoRALayer(d, w, h_from_gu=True) for w in weights]   # the stack's forward
     x = x0
     for l in range(L):
         layers[l].route(*routing[l])
@@ -83,6 +83,29 @@ def test_saved_regather_reproduces_x_perm_bit_for_bit():
     xp = layer.saved[offs[0]:offs[0] + N * cfg.H * 2].view(torch.bfloat16).view(N, cfg.H)
     perm = layer.rt.perm.long()
     assert torch.equal(xp, x0[perm // cfg.k])
+
+
+@pytest.mark.parametrize("name", ["small", "pairs", "gptoss20b"])
+def test_saved_rebuild_h_reproduces_h_bit_for_bit(name):
+    """moe_lora_fwd_h_from_gu forms h from the bf16 GU it stores; moe_lora_saved_rebuild_h
+    recomputes h from that GU alone, bit for bit (single-CTA and SM-pair tiles, and the
+    GPT-OSS-20B shape in full), and touches nothing else in `saved`."""
+    import moe_expert_dispatch_stable_gb300 as moe
+    cfg = {"small": mi.MoEConfig("regather", T=300, H=128, E=5, k=2, I=192, r=8, alpha=16),
+           "pairs": mi.MoEConfig("pairs", T=1000, H=256, E=4, k=2, I=320, r=16, alpha=32),
+           "gptoss20b": mi.CONFIGS["gptoss20b"]}[name]
+    d = moe.Dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r, cfg.scale)
+    weights, routing, x0, _ = _stack_inputs(cfg, 1)
+    layer = moe.MoELoRALayer(d, weights[0], h_from_gu=True)
+    layer.route(*routing[0])
+    layer.forward(x0)
+    offs, _ = moe.moe_lora_saved_layout(d)
+    N = cfg.T * cfg.k
+    ref = layer.saved.clone()
+    layer.saved[offs[2]:offs[2] + N * cfg.I * 2].fill_(0x5A)      # scribble over the h rows only
+    moe.moe_lora_saved_rebuild_h(d, layer.saved)
+    torch.cuda.synchronize()
+    assert torch.equal(layer.saved, ref)
 
 
 def test_offloaded_stack_matches_oracle():
