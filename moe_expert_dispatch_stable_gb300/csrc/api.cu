@@ -362,7 +362,7 @@ static moe_status fwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     g2.out0 = O; g2.ldo = H; g2.epi = EPI_BF16;
     MOE_TRY(timed("gemm_down_fwd", s, [&] { return launch_grouped_gemm(g2, s); }));
 
-    MOE_TRY(timed("combine_y", s, [&] { return launch_combine(O, false, rt->w_sorted, rt->inv_perm, d->T, d->k, H, y, dev_status, s); }));
+    MOE_TRY(timed("combine_y", s, [&] { return launch_combine(O, rt->w_sorted, rt->inv_perm, d->T, d->k, H, y, dev_status, s); }));
     return MOE_OK;
 }
 
@@ -440,7 +440,7 @@ static moe_status bwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     g2.A2 = Gg; g2.rp = L.rp; g2.r = r; g2.B2 = A_gu; g2.ldb2 = H; g2.b2_expert_stride = (int64_t)r * H;
     g2.out0 = dXp; g2.ldo = H; g2.epi = EPI_BF16;
     MOE_TRY(timed("gemm_gate_up_bwd", s, [&] { return launch_grouped_gemm(g2, s); }));
-    MOE_TRY(timed("combine_dx", s, [&] { return launch_combine(dXp, false, nullptr, rt->inv_perm, d->T, d->k, H, dx, dev_status, s); }));
+    MOE_TRY(timed("combine_dx", s, [&] { return launch_combine(dXp, nullptr, rt->inv_perm, d->T, d->k, H, dx, dev_status, s); }));
     // dA_gu = Gg_s^T x_perm ; dB_gu = XA_s^T dGU
     {
         const WgradProblem wp[2] = {{Gg, x_perm, H, dA_gu}, {XA, dGU, 2 * I, dB_gu}};

@@ -34,8 +34,9 @@ cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, cons
                                cudaStream_t s);
 // out[t, :] = bf16( sum_{j<k} w * src[inv_perm[t*k+j], :] ), w = w_sorted[inv_perm[t*k+j]] (or 1 when
 // w_sorted is null); bf16 or fp32 src, fp32 sum in the fixed order j = 0..k-1
-cudaError_t launch_combine(const void* src, bool src_f32, const float* w_sorted, const int32_t* inv_perm, int64_t T,
-                           int k, int H, void* out, int32_t* status, cudaStream_t s);
+// out[t] = sum_j w_j * src[inv_perm[t*k+j]] over bf16 slot rows (w_sorted NULL: weights 1)
+cudaError_t launch_combine(const void* src, const float* w_sorted, const int32_t* inv_perm, int64_t T, int k, int H,
+                           void* out, int32_t* status, cudaStream_t s);
 // h [N, I] = SwiGLU of GU [N, 2I] row by row (bf16 in and out)
 cudaError_t launch_swiglu_rows(const void* gu, int I, int64_t N, void* h, cudaStream_t s);
 

@@ -165,7 +165,8 @@ cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, cons
 // ---------------------------------------------------------------- combine
 // out[t] = sum_{j=0}^{k-1} w_j * src[inv_perm[t*k+j]] in that order, summed in fp32.
 // One warp per (token, chunk of 32 * combine_upl units of 16 columns); each lane loads the k
-// slots' 16 columns with 32-byte accesses (bf16 rows: one, fp32 rows: two per slot).
+// slots' 16 columns with one 32-byte access per slot (the slot rows are bf16: the forward's
+// expert outputs O and the backward's per-slot input gradients).
 template <typename SrcT>
 __device__ __forceinline__ void load16(const SrcT* row, int u, float* a);
 
@@ -175,15 +176,6 @@ __device__ __forceinline__ void load16<bf16>(const bf16* row, int u, float* a) {
     tc::ld32_cs(row + (int64_t)u * 16, x, y);
     unpack8(x, a);
     unpack8(y, a + 8);
-}
-
-template <>
-__device__ __forceinline__ void load16<float>(const float* row, int u, float* a) {
-    uint4 v[4];
-    tc::ld32_cs(row + (int64_t)u * 16, v[0], v[1]);
-    tc::ld32_cs(row + (int64_t)u * 16 + 8, v[2], v[3]);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) a[i] = __uint_as_float(reinterpret_cast<const uint32_t*>(v)[i]);
 }
 
 // units per lane and task (measured: one keeps the most warps resident)
@@ -273,18 +265,15 @@ cudaError_t launch_swiglu_rows(const void* gu, int I, int64_t N, void* h, cudaSt
                       (uint4*)h);
 }
 
-cudaError_t launch_combine(const void* src, bool src_f32, const float* w_sorted, const int32_t* inv_perm, int64_t T,
-                           int k, int H, void* out, int32_t* status, cudaStream_t s) {
+cudaError_t launch_combine(const void* src, const float* w_sorted, const int32_t* inv_perm, int64_t T, int k, int H,
+                           void* out, int32_t* status, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (H % 16 != 0) return cudaErrorInvalidValue;
     const int threads = 256;
     const int units = H / 16;
-    const int upl = src_f32 ? combine_upl<float>() : combine_upl<bf16>();
+    const int upl = combine_upl<bf16>();
     const int64_t tasks = T * ((units + 32 * upl - 1) / (32 * upl));
     const int64_t blocks = std::min<int64_t>((tasks + 7) / 8, (int64_t)num_sms() * 16);
-    if (src_f32)
-        return launch_pdl(combine_kernel<float>, dim3((unsigned)blocks), dim3(threads), 0, s, (const float*)src,
-                          w_sorted, inv_perm, T, k, H, (bf16*)out, status);
     return launch_pdl(combine_kernel<bf16>, dim3((unsigned)blocks), dim3(threads), 0, s, (const bf16*)src, w_sorted,
                       inv_perm, T, k, H, (bf16*)out, status);
 }
