@@ -37,11 +37,11 @@ def make_case(cfg: mi.MoEConfig, seed: int = 0, device="cuda", gen_device=None, 
     return idx, w, ts
 
 
-def run_layer(cfg, idx, w, ts, idx_dtype=torch.int64, with_topk_grad=True):
+def run_layer(cfg, idx, w, ts, idx_dtype=torch.int64, with_topk_grad=True, h_from_gu=False):
     import moe_expert_dispatch_stable_gb300 as moe
     dev = ts["x"].device
     d = moe.Dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r, cfg.scale)
-    layer = moe.MoELoRALayer(d, ts, dev)
+    layer = moe.MoELoRALayer(d, ts, dev, h_from_gu=h_from_gu)
     grads = layer.step(torch.from_numpy(idx).to(dev, idx_dtype), torch.from_numpy(w).to(dev), ts["x"], ts["dy"],
                        with_topk_grad=with_topk_grad)
     torch.cuda.synchronize()

@@ -293,8 +293,8 @@ FULL = ["gptoss20b", "qwen3_30b", "gptoss120b_skew", "dsv3"]
 PER_EXPERT_L2_ROWS = 32
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_parity(name):
+@pytest.mark.parametrize("name,h_from_gu", [(n, False) for n in FULL] + [("gptoss20b", True)])
+def test_full_size_parity(name, h_from_gu):
     """The four large workloads at full size, compared with the fp64 oracle element by
     element: y and dx on every token, and dA_gu, dB_gu, dA_d, dB_d whole and on every
     expert, so that an error confined to one expert -- a band or wave boundary of the tile
@@ -304,10 +304,11 @@ def test_full_size_parity(name):
     gradient summed over a handful of rows is a few bf16-rounded rank-r products, so its
     rel-L2 is a small-sample statistic of that rounding (one 1-row expert of the skewed
     workload measured 5.1e-3 while the whole tensor stayed far inside the bound).  Exact
-    zeros for empty experts."""
+    zeros for empty experts.  The GPT-OSS-20B shape also runs with the forward that forms
+    h from the stored bf16 GU (moe_lora_fwd_h_from_gu, the offloaded stack's forward)."""
     cfg = mi.CONFIGS[name]
     idx, w, ts = make_case(cfg, seed=0)
-    layer, grads = run_layer(cfg, idx, w, ts)
+    layer, grads = run_layer(cfg, idx, w, ts, h_from_gu=h_from_gu)
     assert int(layer.dev_status.item()) == 0
     counts, _ = _check_route(layer, idx, cfg.E)
     lazy = {n: LazyExperts(ts[n]) for n in WEIGHT_NAMES}
