@@ -147,12 +147,11 @@ MOE_API moe_status moe_route(const void* topk_idx, int32_t idx_bytes, const floa
  * slots at E = 1024, or T*k <= 523264 at E = 128).  Larger sizes return
  * MOE_ERR_WORKSPACE and launch nothing.
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current) and keeps it for the life of the process:
- * make that first call before any stream capture.  A device reset
- * (cudaDeviceReset, or destroying and re-creating the primary context) leaves
- * the kept address stale, so a process that resets a device must not call
- * moe_route_static on it again.  The call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * The first call on a device looks up the array's device address (with that
+ * device current) and keeps it together with the device's current context; a
+ * later call in a new context (after cudaDeviceReset, or a primary context
+ * destroyed and made again) looks it up afresh.  Make the first call in a
+ * context before any stream capture.  The call allocates nothing (no cudaMalloc, cudaFree or allocating
  * library routine) and clears the part of the array that must start at zero on
  * every call.  All calls share the array, so calls whose kernels overlap on the
  * GPU (several streams, or several host threads) race: serialise them. */

@@ -21,6 +21,7 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <cuda.h>
 #include <mutex>
 
 namespace moe {
@@ -227,22 +228,46 @@ cudaError_t launch_route(const void* idx, int idx_bytes, const float* topk_w, in
 // loads the library holds it until the process exits; every call shares it.
 static __device__ __align__(256) unsigned char g_route_scratch[MOE_ROUTE_STATIC_SCRATCH_BYTES];
 
-// Device address of g_route_scratch on the current device.  The host-side name of
-// the array is only a stand-in, so the address is looked up once per device (with
-// that device current) and cached.
+// The driver's cuCtxGetCurrent, looked up once through the runtime (no link to libcuda).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
+// Device address of g_route_scratch in the current context.  The host-side name of
+// the array is only a stand-in, so the address is looked up (with the device current)
+// and cached per device together with the context it belongs to; a new context on the
+// device (after cudaDeviceReset, or a primary context destroyed and made again) is
+// looked up afresh.
 cudaError_t route_static_scratch(void** ptr) {
     static std::mutex mu;
     static void* cached[64] = {nullptr};
+    static CUcontext cached_ctx[64] = {nullptr};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const CtxGetCurrentFn get = ctx_get_current();
+    if (get == nullptr) return cudaErrorInitializationError;
+    CUcontext ctx = nullptr;                  // NULL before the runtime made a context current
+    if (get(&ctx) != CUDA_SUCCESS) return cudaErrorInitializationError;
     std::lock_guard<std::mutex> g(mu);
-    if (cached[dev] == nullptr) {
+    if (ctx == nullptr || cached[dev] == nullptr || cached_ctx[dev] != ctx) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_route_scratch);
+        e = cudaGetSymbolAddress(&p, g_route_scratch);     // makes the primary context current if needed
         if (e != cudaSuccess) return e;
+        if (ctx == nullptr && (get(&ctx) != CUDA_SUCCESS || ctx == nullptr)) return cudaErrorInitializationError;
         cached[dev] = p;
+        cached_ctx[dev] = ctx;
     }
     *ptr = cached[dev];
     return cudaSuccess;
