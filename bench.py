@@ -25,7 +25,7 @@ unless --config says otherwise.  Prints ONE JSON line (rank 0).
   other_configs  the Qwen3-30B-A3B, skewed GPT-OSS-120B and DeepSeek-V3 shapes, a
                short run each (10 steps): ms/step, tokens/s, grouped-GEMM TFLOP/s,
                the dominant kernel against its roofline, the routing histogram, and
-               the FP8-base step of the DeepSeek-V3 shape
+               the FP8- and NF4-base steps of the DeepSeek-V3 shape
   cpu_baseline the CPU oracle timed on a bounded token sample (rank 0, N=1): route,
                forward and backward separately, the threads used, and the tiny layer
                on one thread
@@ -332,12 +332,16 @@ def routing_summary(idx, E: int) -> dict:
     return out
 
 
-# ----------------------------------------------------------------------------- fp8 base weights
-def fp8_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, steps: int, flush) -> dict:
-    """route + fwd + bwd with the expert base weights in FP8 (e4m3 codes + power-of-two
-    column scales), timed like the main loop."""
+# ----------------------------------------------------------------------------- quantised base weights
+QUANT_KEYS = {"fp8": ("Wq", "s_"), "nf4": ("W4", "m_")}
+
+
+def quant_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, steps: int, flush, fmt: str) -> dict:
+    """route + fwd + bwd with the expert base weights quantised (fmt "fp8": e4m3 codes +
+    power-of-two column scales; "nf4": 4-bit NormalFloat codes + 64-element absmax
+    scales), timed like the main loop."""
     import torch
-    wq = moe.quantize_expert_weights(layer.w)
+    wq = moe.quantize_expert_weights(layer.w, fmt=fmt)
     q8 = moe.MoELoRALayer(layer.d, wq, dev)
     for _ in range(3):
         q8.step(t_idx, t_w, ts["x"], ts["dy"], with_topk_grad=False)
@@ -357,7 +361,7 @@ def fp8_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, steps: int, flush) -> 
     assert int(q8.dev_status.item()) == 0
     gemm_ms = sum(kt[n][0] for n in GEMM_KERNELS if n in kt) / steps
     kernels = {n: round(v[0] / steps, 4) for n, v in kt.items() if n in GEMM_KERNELS}
-    wbytes = sum(t.numel() * t.element_size() for n, t in wq.items() if n.startswith(("Wq", "s_")))
+    wbytes = sum(t.numel() * t.element_size() for n, t in wq.items() if n.startswith(QUANT_KEYS[fmt]))
     del q8, wq
     return {"ms_per_step": ms / steps, "tokens_per_s": cfg.T * steps / (ms / 1e3), "gemm_ms_per_step": gemm_ms,
             "gemm_kernels_ms_per_step": kernels, "base_weight_bytes": wbytes, "steps": steps}
@@ -427,7 +431,7 @@ def workload_measurement(name: str, moe, dev, flush, steps: int, peaks: dict, se
     """A short run of another workload on the same line: route + fwd + bwd per step
     (CUDA events around each step, L2 flushed between steps), its grouped GEMMs against
     the dense bf16 peak, the dominant kernel against its roofline, and, with `fp8`, the
-    same step with FP8 base weights.  The clocks of the main run decide burst or
+    same step with FP8 and with NF4 base weights.  The clocks of the main run decide burst or
     sustained peak; this short run sits right after it."""
     import torch
     cfg = mi.CONFIGS[name]
@@ -476,15 +480,15 @@ def workload_measurement(name: str, moe, dev, flush, steps: int, peaks: dict, se
                                "frac_of_bf16_burst": work[dom]["flops"] / (d_ms / 1e3) / 1e12 / peaks["bf16_tflops"]},
            "kernels_ms_per_step": {n: round(v[0] / steps, 4) for n, v in sorted(kt.items(), key=lambda kv: -kv[1][0])},
            "routing": routing_summary(idx, cfg.E)}
-    if fp8:
-        wq = moe.quantize_expert_weights(layer.w)
-        q8 = moe.MoELoRALayer(layer.d, wq, dev)
-        f_ms, f_kt = run(q8, True)
-        out["fp8_base"] = {"ms_per_step": f_ms, "tokens_per_s": cfg.T / (f_ms / 1e3),
-                           "gemm_ms_per_step": sum(f_kt[n][0] for n in GEMM_KERNELS if n in f_kt) / steps,
-                           "gemm_kernels_ms_per_step": {n: round(f_kt[n][0] / steps, 4) for n in GEMM_KERNELS
-                                                        if n in f_kt}}
-        del q8, wq
+    for fmt in ("fp8", "nf4") if fp8 else ():
+        wq = moe.quantize_expert_weights(layer.w, fmt=fmt)
+        lq = moe.MoELoRALayer(layer.d, wq, dev)
+        f_ms, f_kt = run(lq, True)
+        out[fmt + "_base"] = {"ms_per_step": f_ms, "tokens_per_s": cfg.T / (f_ms / 1e3),
+                              "gemm_ms_per_step": sum(f_kt[n][0] for n in GEMM_KERNELS if n in f_kt) / steps,
+                              "gemm_kernels_ms_per_step": {n: round(f_kt[n][0] / steps, 4) for n in GEMM_KERNELS
+                                                           if n in f_kt}}
+        del lq, wq
     del layer, ts
     torch.cuda.empty_cache()
     return out
@@ -502,7 +506,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--breakdown", action="store_true", help="print per-kernel times to stderr")
     ap.add_argument("--no-offload", action="store_true", help="skip the offloaded-stack measurement")
-    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-base-weight measurement")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the quantised-base-weight (FP8, NF4) measurements")
     ap.add_argument("--offload-layers", type=int, default=4)
     ap.add_argument("--other-steps", type=int, default=10,
                     help="timed steps of each other workload on the line (0: none)")
@@ -765,9 +769,11 @@ def main():
                                "max_seqlen": int(meta.max_seqlen.item()),
                                "meta_us": line["router"].pop("packed_meta")["us_per_launch"],
                                **{"mask_" + k: v for k, v in line["router"].pop("packed_mask").items()}}
-    # ---- the same step with FP8 (e4m3) base weights, dequantised inside the GEMMs
+    # ---- the same step with FP8 (e4m3) and NF4 base weights, dequantised inside the GEMMs
     if not args.no_fp8:
-        line["fp8_base"] = fp8_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, max(10, args.steps // 4), flush)
+        for fmt in ("fp8", "nf4"):
+            line[fmt + "_base"] = quant_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, max(10, args.steps // 4),
+                                                    flush, fmt)
     # ---- stack of layers with saved activations offloaded to pinned host memory:
     # backward time with double-buffered reload vs single buffer vs resident
     if not args.no_offload:

@@ -25,7 +25,7 @@
  *  - All tensors are dense row-major; bf16 tensors are passed as uint16_t*.
  *  - Every pointer is a DEVICE pointer unless stated otherwise, 16-byte aligned,
  *    owned by the caller; the activation buffers x, y, dy, dx, saved and the
- *    workspaces of moe_lora_fwd / moe_lora_bwd (and their _fp8 forms) are 32-byte
+ *    workspaces of moe_lora_fwd / moe_lora_bwd (and their _fp8 / _nf4 forms) are 32-byte
  *    aligned (their rows are moved with 32-byte accesses).  Buffers whose size is a multiple of T (x, y, dy, dx,
  *    perm, inv_perm, w_sorted, saved, workspaces) may be NULL when T == 0.  The library allocates no device memory and keeps no
  *    state beyond a per-device cache of the SM count and of a driver entry point.
@@ -38,7 +38,7 @@
  *    expert id outside [0, E), MOE_DEV_TIMEOUT when a bounded wait inside a
  *    kernel gave up.  When a bit is set the outputs are unspecified.
  *  - No function blocks the host.  moe_route, moe_lora_fwd, moe_lora_bwd (and the
- *    _fp8 forms) can be captured in a CUDA graph.
+ *    _fp8 / _nf4 forms) can be captured in a CUDA graph.
  *
  * Sizes supported: 1 <= k <= E <= 1024, H and I multiples of 64, 1 <= r <= 64,
  * T >= 0 and T*k < 2^31.
@@ -279,6 +279,54 @@ MOE_API moe_status moe_lora_bwd_fp8(const moe_dims* d, const moe_routing* rt, co
                                     const uint8_t* Wq_gu, const float* s_gu,
                                     const uint16_t* A_gu, const uint16_t* B_gu,
                                     const uint8_t* Wq_d, const float* s_d,
+                                    const uint16_t* A_d, const uint16_t* B_d,
+                                    const void* saved, size_t saved_bytes,
+                                    uint16_t* dx, uint16_t* dA_gu, uint16_t* dB_gu,
+                                    uint16_t* dA_d, uint16_t* dB_d, float* d_topk_w,
+                                    void* workspace, size_t workspace_bytes,
+                                    int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------- NF4 expert base weights
+ * The pages' "QLoRA 4-bit" base (the Unsloth 2026 wiki page, section "supported models and
+ * 2026 changes", model table; the GPU MODE lecture 32 notes, open questions, name QLoRA's
+ * NF4), read as QLoRA's 4-bit NormalFloat data type.  Per matrix m, row r and block b of
+ * 64 consecutive columns of W [n_mat, rows, cols] (bf16, cols a multiple of 64):
+ *   absmax[m, r, b] = max |W[m, r, 64b .. 64b+63]|
+ *   code of W[m, r, c] = the i in 0..15 whose T[i] is nearest to W[m, r, c] / absmax (both in
+ *                        float32, the lower i on a tie; 7, the zero, when absmax is 0)
+ *   Wq[m, r, c / 2]    = code(c even) | code(c odd) << 4
+ * T = moe_nf4_codebook.  The dequantised weight is bf16(T[code] * absmax), the product in
+ * float32 rounded to nearest even.  Wq uint8 [n_mat, rows, cols / 2], absmax float32
+ * [n_mat, rows, cols / 64].  One kernel; weight preparation, not the hot path.
+ * MOE_ERR_BAD_DIMS when cols is not a multiple of 64. */
+MOE_API moe_status moe_quantize_nf4(const uint16_t* W, int64_t n_mat, int64_t rows, int32_t cols,
+                                    uint8_t* Wq, float* absmax, void* stream);
+
+/* The 16 NF4 code values T[0..15] (host memory, ascending): quantiles of the standard
+ * normal distribution at probabilities evenly spaced from delta = 1 - (1/32 + 1/30) / 2
+ * towards 1/2 (8 positive values; 7 negative ones, mirrored), an exact zero (T[7]), divided
+ * by the largest and rounded to float32, so T[0] = -1 and T[15] = 1.  Host only. */
+MOE_API moe_status moe_nf4_codebook(float* values);
+
+/* moe_lora_fwd / moe_lora_bwd with NF4 base weights: Wq_gu [E, H, I] bytes (2I codes per row)
+ * and Wq_d [E, I, H / 2] with block scales absmax_gu [E, H, 2I / 64] and absmax_d
+ * [E, I, H / 64] (moe_quantize_nf4).  The GEMMs stream the codes (a quarter of the bytes of
+ * bf16) and dequantise them to bf16 in shared memory before the tensor cores read them, so
+ * the results are bit-identical to moe_lora_fwd / moe_lora_bwd called with the dequantised
+ * bf16 weights.  LoRA factors and activations stay bf16; same saved / workspace sizes; SM
+ * pairs as for the FP8 forms (MOE_ERR_CUDA where no 2-CTA cluster fits). */
+MOE_API moe_status moe_lora_fwd_nf4(const moe_dims* d, const moe_routing* rt, const uint16_t* x,
+                                    const uint8_t* Wq_gu, const float* absmax_gu,
+                                    const uint16_t* A_gu, const uint16_t* B_gu,
+                                    const uint8_t* Wq_d, const float* absmax_d,
+                                    const uint16_t* A_d, const uint16_t* B_d, uint16_t* y,
+                                    void* saved, size_t saved_bytes,
+                                    void* workspace, size_t workspace_bytes,
+                                    int32_t* dev_status, void* stream);
+MOE_API moe_status moe_lora_bwd_nf4(const moe_dims* d, const moe_routing* rt, const uint16_t* dy,
+                                    const uint8_t* Wq_gu, const float* absmax_gu,
+                                    const uint16_t* A_gu, const uint16_t* B_gu,
+                                    const uint8_t* Wq_d, const float* absmax_d,
                                     const uint16_t* A_d, const uint16_t* B_d,
                                     const void* saved, size_t saved_bytes,
                                     uint16_t* dx, uint16_t* dA_gu, uint16_t* dB_gu,

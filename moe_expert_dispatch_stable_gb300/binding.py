@@ -46,8 +46,9 @@ EXPORTED = ("moe_abi_version", "moe_status_string", "moe_launch_count", "moe_rou
             "moe_lora_fwd_sizes", "moe_lora_saved_layout", "moe_lora_saved_regather", "moe_lora_saved_rebuild_h", "moe_lora_fwd", "moe_lora_fwd_h_from_gu",
             "moe_lora_bwd_workspace_size", "moe_lora_bwd", "moe_timing_enable", "moe_timing_read",
             "moe_router_topk", "moe_router_bwd", "moe_quantize_fp8", "moe_lora_fwd_fp8", "moe_lora_bwd_fp8",
+            "moe_quantize_nf4", "moe_nf4_codebook", "moe_lora_fwd_nf4", "moe_lora_bwd_nf4",
             "moe_packed_metadata", "moe_packed_causal_mask", "moe_diag_force_timeout")
-ABI_VERSION = 6
+ABI_VERSION = 7
 
 _libs: dict = {}
 _default_path = LIB_PATH
@@ -82,6 +83,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.moe_quantize_fp8.argtypes = [vp, i64, i64, i32, vp, vp, vp]
     lib.moe_lora_fwd_fp8.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 10 + [vp, sz, vp, sz, vp, vp]
     lib.moe_lora_bwd_fp8.argtypes = [P(moe_dims), P(moe_routing)] + [vp] * 10 + [sz] + [vp] * 6 + [vp, sz, vp, vp]
+    lib.moe_quantize_nf4.argtypes = lib.moe_quantize_fp8.argtypes
+    lib.moe_nf4_codebook.argtypes = [P(ctypes.c_float)]
+    lib.moe_lora_fwd_nf4.argtypes = lib.moe_lora_fwd_fp8.argtypes
+    lib.moe_lora_bwd_nf4.argtypes = lib.moe_lora_bwd_fp8.argtypes
     lib.moe_router_bwd.argtypes = [vp, vp, vp, i64, i32, i32, vp, vp]
     lib.moe_packed_metadata.argtypes = [vp, i32, i64, vp, vp, vp, vp, vp]
     lib.moe_packed_causal_mask.argtypes = [vp, vp, i64, vp, vp]
@@ -427,12 +432,50 @@ def moe_quantize_fp8(W: torch.Tensor, stream=None):
     return Wq, sc
 
 
-def quantize_expert_weights(weights: dict, stream=None) -> dict:
-    """Expert weights with the two base stacks replaced by FP8 codes + scales."""
+def moe_quantize_nf4(W: torch.Tensor, stream=None):
+    """NF4 codes (two per byte) and per-64-element absmax scales of a bf16 weight stack
+    [..., rows, cols], cols a multiple of 64; returns (Wq uint8 [..., rows, cols / 2],
+    absmax float32 [..., rows, cols / 64])."""
+    _need(W, "W", torch.bfloat16)
+    rows, cols = W.shape[-2], W.shape[-1]
+    if cols % 64:
+        raise MoEError("NF4 quantisation needs rows of a multiple of 64 elements")
+    n_mat = W.numel() // max(rows * cols, 1)
+    Wq = torch.empty(W.shape[:-1] + (cols // 2,), dtype=torch.uint8, device=W.device)
+    am = torch.empty(W.shape[:-1] + (cols // 64,), dtype=torch.float32, device=W.device)
+    _check(load_library().moe_quantize_nf4(_ptr(W), n_mat, rows, cols, _ptr(Wq), _ptr(am), _stream(stream)))
+    return Wq, am
+
+
+def moe_nf4_codebook() -> list:
+    """The 16 NF4 code values the library quantises and dequantises with (ascending)."""
+    buf = (ctypes.c_float * 16)()
+    _check(load_library().moe_nf4_codebook(buf))
+    return list(buf)
+
+
+def quantize_expert_weights(weights: dict, stream=None, fmt: str = "fp8") -> dict:
+    """Expert weights with the two base stacks replaced by codes + scales: fmt "fp8" (e4m3
+    codes, column scales: keys Wq_gu, s_gu, Wq_d, s_d) or "nf4" (4-bit NormalFloat codes,
+    64-element block scales: keys W4_gu, m_gu, W4_d, m_d)."""
     out = {k: v for k, v in weights.items() if k not in ("W_gu", "W_d")}
-    out["Wq_gu"], out["s_gu"] = moe_quantize_fp8(weights["W_gu"], stream)
-    out["Wq_d"], out["s_d"] = moe_quantize_fp8(weights["W_d"], stream)
+    if fmt == "fp8":
+        out["Wq_gu"], out["s_gu"] = moe_quantize_fp8(weights["W_gu"], stream)
+        out["Wq_d"], out["s_d"] = moe_quantize_fp8(weights["W_d"], stream)
+    elif fmt == "nf4":
+        out["W4_gu"], out["m_gu"] = moe_quantize_nf4(weights["W_gu"], stream)
+        out["W4_d"], out["m_d"] = moe_quantize_nf4(weights["W_d"], stream)
+    else:
+        raise MoEError(f"unknown weight format {fmt!r}")
     return out
+
+
+def _lora_factor_checks(d: Dims, w: dict):
+    bf = torch.bfloat16
+    _need(w["A_gu"], "A_gu", bf, (d.E, d.r, d.H))
+    _need(w["B_gu"], "B_gu", bf, (d.E, d.r, 2 * d.I))
+    _need(w["A_d"], "A_d", bf, (d.E, d.r, d.I))
+    _need(w["B_d"], "B_d", bf, (d.E, d.r, d.H))
 
 
 def _fp8_args(d: Dims, w: dict):
@@ -440,12 +483,17 @@ def _fp8_args(d: Dims, w: dict):
     _need(w["s_gu"], "s_gu", torch.float32, (d.E, 2 * d.I))
     _need(w["Wq_d"], "Wq_d", torch.uint8, (d.E, d.I, d.H))
     _need(w["s_d"], "s_d", torch.float32, (d.E, d.H))
-    bf = torch.bfloat16
-    _need(w["A_gu"], "A_gu", bf, (d.E, d.r, d.H))
-    _need(w["B_gu"], "B_gu", bf, (d.E, d.r, 2 * d.I))
-    _need(w["A_d"], "A_d", bf, (d.E, d.r, d.I))
-    _need(w["B_d"], "B_d", bf, (d.E, d.r, d.H))
+    _lora_factor_checks(d, w)
     return [_ptr(w[n]) for n in ("Wq_gu", "s_gu", "A_gu", "B_gu", "Wq_d", "s_d", "A_d", "B_d")]
+
+
+def _nf4_args(d: Dims, w: dict):
+    _need(w["W4_gu"], "W4_gu", torch.uint8, (d.E, d.H, d.I))
+    _need(w["m_gu"], "m_gu", torch.float32, (d.E, d.H, 2 * d.I // 64))
+    _need(w["W4_d"], "W4_d", torch.uint8, (d.E, d.I, d.H // 2))
+    _need(w["m_d"], "m_d", torch.float32, (d.E, d.I, d.H // 64))
+    _lora_factor_checks(d, w)
+    return [_ptr(w[n]) for n in ("W4_gu", "m_gu", "A_gu", "B_gu", "W4_d", "m_d", "A_d", "B_d")]
 
 
 def moe_lora_fwd_fp8(d: Dims, rt: Routing, x, w: dict, y, saved, workspace, dev_status, stream=None):
@@ -465,6 +513,29 @@ def moe_lora_bwd_fp8(d: Dims, rt: Routing, dy, w: dict, saved, dx, grads, worksp
     dA_gu, dB_gu, dA_d, dB_d = grads
     dd, rr = d.c_struct(), rt.c_struct()
     _check(load_library().moe_lora_bwd_fp8(ctypes.byref(dd), ctypes.byref(rr), _ptr(dy), *_fp8_args(d, w),
+                                           _ptr(saved), saved.numel(), _ptr(dx), _ptr(dA_gu), _ptr(dB_gu),
+                                           _ptr(dA_d), _ptr(dB_d), _ptr(d_topk_w), _ptr(workspace),
+                                           workspace.numel(), _ptr(dev_status), _stream(stream)))
+    return dx, dA_gu, dB_gu, dA_d, dB_d
+
+
+def moe_lora_fwd_nf4(d: Dims, rt: Routing, x, w: dict, y, saved, workspace, dev_status, stream=None):
+    """Forward with NF4 base weights (`w` from quantize_expert_weights(..., fmt="nf4"))."""
+    _need(x, "x", torch.bfloat16, (d.T, d.H))
+    dd, rr = d.c_struct(), rt.c_struct()
+    _check(load_library().moe_lora_fwd_nf4(ctypes.byref(dd), ctypes.byref(rr), _ptr(x), *_nf4_args(d, w), _ptr(y),
+                                           _ptr(saved), saved.numel(), _ptr(workspace), workspace.numel(),
+                                           _ptr(dev_status), _stream(stream)))
+    return y
+
+
+def moe_lora_bwd_nf4(d: Dims, rt: Routing, dy, w: dict, saved, dx, grads, workspace, dev_status, stream=None,
+                     d_topk_w=None):
+    """Backward with NF4 base weights; returns (dx, dA_gu, dB_gu, dA_d, dB_d)."""
+    _need(dy, "dy", torch.bfloat16, (d.T, d.H))
+    dA_gu, dB_gu, dA_d, dB_d = grads
+    dd, rr = d.c_struct(), rt.c_struct()
+    _check(load_library().moe_lora_bwd_nf4(ctypes.byref(dd), ctypes.byref(rr), _ptr(dy), *_nf4_args(d, w),
                                            _ptr(saved), saved.numel(), _ptr(dx), _ptr(dA_gu), _ptr(dB_gu),
                                            _ptr(dA_d), _ptr(dB_d), _ptr(d_topk_w), _ptr(workspace),
                                            workspace.numel(), _ptr(dev_status), _stream(stream)))
@@ -516,6 +587,7 @@ class MoELoRALayer:
         self.w = weights
         self.h_from_gu = h_from_gu
         self.fp8 = "Wq_gu" in weights          # FP8 base weights (quantize_expert_weights)
+        self.nf4 = "W4_gu" in weights          # NF4 base weights (quantize_expert_weights, fmt="nf4")
         dev = torch.device(device)
         self.rt = Routing.empty(d.T, d.k, d.E, dev)
         self.route_ws = torch.empty(moe_route_workspace_size(d.T, d.k, d.E), dtype=torch.uint8, device=dev)
@@ -541,6 +613,9 @@ class MoELoRALayer:
         if self.fp8:
             return moe_lora_fwd_fp8(self.d, self.rt, x, self.w, self.y, self.saved, self.fwd_ws, self.dev_status,
                                     stream)
+        if self.nf4:
+            return moe_lora_fwd_nf4(self.d, self.rt, x, self.w, self.y, self.saved, self.fwd_ws, self.dev_status,
+                                    stream)
         return moe_lora_fwd(self.d, self.rt, x, *self._wts(), y=self.y, saved=self.saved,
                             workspace=self.fwd_ws, dev_status=self.dev_status, stream=stream,
                             h_from_gu=self.h_from_gu)[0]
@@ -549,6 +624,9 @@ class MoELoRALayer:
         dtw = self.d_topk_w if with_topk_grad else None
         if self.fp8:
             return moe_lora_bwd_fp8(self.d, self.rt, dy, self.w, self.saved, self.dx, self.grads, self.bwd_ws,
+                                    self.dev_status, stream, d_topk_w=dtw)
+        if self.nf4:
+            return moe_lora_bwd_nf4(self.d, self.rt, dy, self.w, self.saved, self.dx, self.grads, self.bwd_ws,
                                     self.dev_status, stream, d_topk_w=dtw)
         return moe_lora_bwd(self.d, self.rt, dy, *self._wts(), self.saved, dx=self.dx, grads=self.grads,
                             workspace=self.bwd_ws, dev_status=self.dev_status, stream=stream, d_topk_w=dtw)

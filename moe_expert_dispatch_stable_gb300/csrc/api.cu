@@ -183,7 +183,7 @@ DiagWait moe::diag_next_single_cta_launch() {
 
 extern "C" {
 
-int32_t moe_abi_version(void) { return 6; }
+int32_t moe_abi_version(void) { return 7; }
 
 const char* moe_status_string(moe_status s) {
     switch (s) {
@@ -305,13 +305,14 @@ moe_status moe_lora_bwd_workspace_size(const moe_dims* d, size_t* bytes) {
     return MOE_OK;
 }
 
-// Forward / backward launch sequences; s_gu / s_d non-null: W_gu / W_d hold e4m3 codes
-// with per-column power-of-two scales (dequantised inside the GEMM pipeline).
+// Forward / backward launch sequences.  qbits 8: W_gu / W_d hold e4m3 codes with per-column
+// power-of-two scales s_gu / s_d; qbits 4: NF4 codes with one absmax per 64 elements of a row;
+// both dequantised inside the GEMM pipeline.  qbits 0: bf16 weights (s_gu, s_d unused).
 static moe_status fwd_impl(const moe_dims* d, const moe_routing* rt, const uint16_t* x, const void* W_gu,
                            const float* s_gu, const uint16_t* A_gu, const uint16_t* B_gu, const void* W_d,
                            const float* s_d, const uint16_t* A_d, const uint16_t* B_d, uint16_t* y, void* saved,
                            size_t saved_bytes, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                           void* stream, bool h_from_gu = false) {
+                           void* stream, int qbits = 0, bool h_from_gu = false) {
     if (!aligned16(s_gu) || !aligned16(s_d)) return MOE_ERR_MISALIGNED;
     moe_status st = check_dims(d);
     if (st != MOE_OK) return st;
@@ -347,7 +348,7 @@ static moe_status fwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     g.N = N; g.E = E; g.offsets = rt->offsets; g.tile_offsets = rt->tile_offsets; g.dev_status = dev_status;
     // gate_up: GU = x_perm W_gu[e] + XA_s B_gu[e]; h = silu(g) * u
     g.K = H; g.Ncols = I; g.A = x_perm;
-    g.B = W_gu; g.b_scale = s_gu; g.b_mn_major = true; g.ldb = 2 * I; g.b_expert_stride = (int64_t)H * 2 * I;
+    g.B = W_gu; g.b_quant = qbits; g.b_scale = s_gu; g.b_mn_major = true; g.ldb = 2 * I; g.b_expert_stride = (int64_t)H * 2 * I;
     g.A2 = XA; g.rp = L.rp; g.r = r; g.B2 = B_gu; g.ldb2 = 2 * I; g.b2_expert_stride = (int64_t)r * 2 * I;
     g.out0 = GU; g.out1 = h; g.epi = EPI_SWIGLU; g.h_from_gu = h_from_gu ? 1 : 0;
     MOE_TRY(timed("gemm_gate_up_fwd", s, [&] { return launch_grouped_gemm(g, s); }));
@@ -357,7 +358,7 @@ static moe_status fwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     GroupedGemm g2{};
     g2.N = N; g2.E = E; g2.offsets = rt->offsets; g2.tile_offsets = rt->tile_offsets; g2.dev_status = dev_status;
     g2.K = I; g2.Ncols = H; g2.A = h;
-    g2.B = W_d; g2.b_scale = s_d; g2.b_mn_major = true; g2.ldb = H; g2.b_expert_stride = (int64_t)I * H;
+    g2.B = W_d; g2.b_quant = qbits; g2.b_scale = s_d; g2.b_mn_major = true; g2.ldb = H; g2.b_expert_stride = (int64_t)I * H;
     g2.A2 = HA; g2.rp = L.rp; g2.r = r; g2.B2 = B_d; g2.ldb2 = H; g2.b2_expert_stride = (int64_t)r * H;
     g2.out0 = O; g2.ldo = H; g2.epi = EPI_BF16;
     MOE_TRY(timed("gemm_down_fwd", s, [&] { return launch_grouped_gemm(g2, s); }));
@@ -371,7 +372,7 @@ static moe_status bwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
                            const float* s_d, const uint16_t* A_d, const uint16_t* B_d, const void* saved,
                            size_t saved_bytes, uint16_t* dx, uint16_t* dA_gu, uint16_t* dB_gu, uint16_t* dA_d,
                            uint16_t* dB_d, float* d_topk_w, void* workspace, size_t workspace_bytes,
-                           int32_t* dev_status, void* stream) {
+                           int32_t* dev_status, void* stream, int qbits = 0) {
     if (!aligned16(s_gu) || !aligned16(s_d)) return MOE_ERR_MISALIGNED;
     moe_status st = check_dims(d);
     if (st != MOE_OK) return st;
@@ -420,7 +421,7 @@ static moe_status bwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     GroupedGemm g{};
     g.N = N; g.E = E; g.offsets = rt->offsets; g.tile_offsets = rt->tile_offsets; g.dev_status = dev_status;
     g.K = H; g.Ncols = I; g.A = dO;
-    g.B = W_d; g.b_scale = s_d; g.b_mn_major = false; g.ldb = H; g.b_expert_stride = (int64_t)I * H;
+    g.B = W_d; g.b_quant = qbits; g.b_scale = s_d; g.b_mn_major = false; g.ldb = H; g.b_expert_stride = (int64_t)I * H;
     g.A2 = G; g.rp = L.rp; g.r = r; g.B2 = A_d; g.ldb2 = I; g.b2_expert_stride = (int64_t)r * I;
     g.gu_in = GU; g.out0 = dGU; g.epi = EPI_DSWIGLU;
     MOE_TRY(timed("gemm_down_bwd", s, [&] { return launch_grouped_gemm(g, s); }));
@@ -436,7 +437,7 @@ static moe_status bwd_impl(const moe_dims* d, const moe_routing* rt, const uint1
     GroupedGemm g2{};
     g2.N = N; g2.E = E; g2.offsets = rt->offsets; g2.tile_offsets = rt->tile_offsets; g2.dev_status = dev_status;
     g2.K = 2 * I; g2.Ncols = H; g2.A = dGU;
-    g2.B = W_gu; g2.b_scale = s_gu; g2.b_mn_major = false; g2.ldb = 2 * I; g2.b_expert_stride = (int64_t)H * 2 * I;
+    g2.B = W_gu; g2.b_quant = qbits; g2.b_scale = s_gu; g2.b_mn_major = false; g2.ldb = 2 * I; g2.b_expert_stride = (int64_t)H * 2 * I;
     g2.A2 = Gg; g2.rp = L.rp; g2.r = r; g2.B2 = A_gu; g2.ldb2 = H; g2.b2_expert_stride = (int64_t)r * H;
     g2.out0 = dXp; g2.ldo = H; g2.epi = EPI_BF16;
     MOE_TRY(timed("gemm_gate_up_bwd", s, [&] { return launch_grouped_gemm(g2, s); }));
@@ -462,7 +463,7 @@ moe_status moe_lora_fwd_h_from_gu(const moe_dims* d, const moe_routing* rt, cons
                                   const uint16_t* B_d, uint16_t* y, void* saved, size_t saved_bytes, void* workspace,
                                   size_t workspace_bytes, int32_t* dev_status, void* stream) {
     return fwd_impl(d, rt, x, W_gu, nullptr, A_gu, B_gu, W_d, nullptr, A_d, B_d, y, saved, saved_bytes, workspace,
-                    workspace_bytes, dev_status, stream, true);
+                    workspace_bytes, dev_status, stream, 0, true);
 }
 
 moe_status moe_lora_bwd(const moe_dims* d, const moe_routing* rt, const uint16_t* dy, const uint16_t* W_gu,
@@ -481,7 +482,7 @@ moe_status moe_lora_fwd_fp8(const moe_dims* d, const moe_routing* rt, const uint
                             void* stream) {
     if (s_gu == nullptr || s_d == nullptr) return MOE_ERR_NULL_ARG;
     return fwd_impl(d, rt, x, Wq_gu, s_gu, A_gu, B_gu, Wq_d, s_d, A_d, B_d, y, saved, saved_bytes, workspace,
-                    workspace_bytes, dev_status, stream);
+                    workspace_bytes, dev_status, stream, 8);
 }
 
 moe_status moe_lora_bwd_fp8(const moe_dims* d, const moe_routing* rt, const uint16_t* dy, const uint8_t* Wq_gu,
@@ -492,7 +493,28 @@ moe_status moe_lora_bwd_fp8(const moe_dims* d, const moe_routing* rt, const uint
                             int32_t* dev_status, void* stream) {
     if (s_gu == nullptr || s_d == nullptr) return MOE_ERR_NULL_ARG;
     return bwd_impl(d, rt, dy, Wq_gu, s_gu, A_gu, B_gu, Wq_d, s_d, A_d, B_d, saved, saved_bytes, dx, dA_gu, dB_gu,
-                    dA_d, dB_d, d_topk_w, workspace, workspace_bytes, dev_status, stream);
+                    dA_d, dB_d, d_topk_w, workspace, workspace_bytes, dev_status, stream, 8);
+}
+
+moe_status moe_lora_fwd_nf4(const moe_dims* d, const moe_routing* rt, const uint16_t* x, const uint8_t* Wq_gu,
+                            const float* absmax_gu, const uint16_t* A_gu, const uint16_t* B_gu, const uint8_t* Wq_d,
+                            const float* absmax_d, const uint16_t* A_d, const uint16_t* B_d, uint16_t* y, void* saved,
+                            size_t saved_bytes, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            void* stream) {
+    if (absmax_gu == nullptr || absmax_d == nullptr) return MOE_ERR_NULL_ARG;
+    return fwd_impl(d, rt, x, Wq_gu, absmax_gu, A_gu, B_gu, Wq_d, absmax_d, A_d, B_d, y, saved, saved_bytes,
+                    workspace, workspace_bytes, dev_status, stream, 4);
+}
+
+moe_status moe_lora_bwd_nf4(const moe_dims* d, const moe_routing* rt, const uint16_t* dy, const uint8_t* Wq_gu,
+                            const float* absmax_gu, const uint16_t* A_gu, const uint16_t* B_gu, const uint8_t* Wq_d,
+                            const float* absmax_d, const uint16_t* A_d, const uint16_t* B_d, const void* saved,
+                            size_t saved_bytes, uint16_t* dx, uint16_t* dA_gu, uint16_t* dB_gu, uint16_t* dA_d,
+                            uint16_t* dB_d, float* d_topk_w, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, void* stream) {
+    if (absmax_gu == nullptr || absmax_d == nullptr) return MOE_ERR_NULL_ARG;
+    return bwd_impl(d, rt, dy, Wq_gu, absmax_gu, A_gu, B_gu, Wq_d, absmax_d, A_d, B_d, saved, saved_bytes, dx, dA_gu,
+                    dB_gu, dA_d, dB_d, d_topk_w, workspace, workspace_bytes, dev_status, stream, 4);
 }
 
 moe_status moe_quantize_fp8(const uint16_t* W, int64_t n_mat, int64_t rows, int32_t cols, uint8_t* Wq,
@@ -504,6 +526,23 @@ moe_status moe_quantize_fp8(const uint16_t* W, int64_t n_mat, int64_t rows, int3
     return cuda_status(timed("quantize_fp8", (cudaStream_t)stream, [&] {
         return launch_quantize_fp8(W, n_mat, rows, cols, Wq, scales, (cudaStream_t)stream);
     }));
+}
+
+moe_status moe_quantize_nf4(const uint16_t* W, int64_t n_mat, int64_t rows, int32_t cols, uint8_t* Wq,
+                            float* absmax, void* stream) {
+    if (n_mat < 0 || rows < 0 || cols < 0 || cols % 64 != 0) return MOE_ERR_BAD_DIMS;
+    if (n_mat * rows * (int64_t)cols > 0 && (W == nullptr || Wq == nullptr || absmax == nullptr))
+        return MOE_ERR_NULL_ARG;
+    if (!aligned16(W) || !aligned16(Wq) || !aligned16(absmax)) return MOE_ERR_MISALIGNED;
+    return cuda_status(timed("quantize_nf4", (cudaStream_t)stream, [&] {
+        return launch_quantize_nf4(W, n_mat, rows, cols, Wq, absmax, (cudaStream_t)stream);
+    }));
+}
+
+moe_status moe_nf4_codebook(float* values) {
+    if (values == nullptr) return MOE_ERR_NULL_ARG;
+    memcpy(values, nf4_table().v, sizeof(nf4_table().v));
+    return MOE_OK;
 }
 
 moe_status moe_router_topk(const float* logits, int64_t T, int32_t E, int32_t k, int32_t* topk_idx, float* topk_w,

@@ -57,21 +57,22 @@ constexpr int kBoxMN = 64 * BK * 2;          // one 64-column MN-major box of B:
 // Tile geometry for an output tile width BN (256 for the expert GEMMs; 16/32/64
 // for the rank-r projections).  PAIR: a 2-CTA cluster shares one 256 x 256 tile,
 // each CTA holding 128 rows of A and 128 columns of B per stage.
-template <int BN, bool PAIR = false, bool Q8 = false>
+template <int BN, bool PAIR = false, int QB = 0>
 struct Geo {
     // narrow tiles (the HBM-bound projections) load KW 64-column boxes of A per stage so
     // that every row is fetched in 256-512 byte runs
     static constexpr int KW = BN >= 256 ? 1 : (BN <= 16 ? 4 : 2);
     static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK * 2 * KW;
-    // FP8 weights: the TMA lands the e4m3 codes in the upper half of the B slot and the
-    // converter warps expand them in place, so a stage is as large as with bf16 weights
-    static constexpr int kQBytes = Q8 ? kBBytes / 2 : 0;
+    // quantised weights (QB-bit codes: 8 = e4m3, 4 = NF4): the TMA lands the codes at the
+    // top of the B slot and the converter warps expand them in place, so a stage is as
+    // large as with bf16 weights
+    static constexpr int kQBytes = QB ? kBBytes * QB / 16 : 0;
     // bf16 SM pairs take two 64-deep k-blocks per ring stage: one barrier wait, 8 MMAs
     // and one commit per stage.  Each wait-and-commit cycle costs the tensor pipe a fixed
     // ~0.13 us, a third of a 64-deep stage of 256 x 256 MMAs (measured without loads or
     // epilogue: gate_up forward 0.327 vs 0.373 ms with six 64-deep stages; with them the
     // step is 1-2 % faster).
-    static constexpr int KB2 = (PAIR && !Q8) ? 2 : 1;
+    static constexpr int KB2 = (PAIR && !QB) ? 2 : 1;
     static constexpr int kSubBytes = kABytes * KW + ((kBBytes + 1023) / 1024) * 1024;   // one k-block
     static constexpr int kStageBytes = KB2 * kSubBytes;
     static constexpr int kStages = PAIR ? 6 / KB2 : (BN >= 256 ? 4 : (216 * 1024) / kStageBytes);
@@ -92,6 +93,7 @@ struct TcParams {
     uint32_t a2_sbo, a2_swz;
     uint64_t wait_ns;   // limit of the ordinary bounded waits
     int stall;          // diagnostics: the epilogue first waits on a barrier nothing arrives on
+    float nf4[16];      // NF4 code values (quantised B with 4-bit codes)
 };
 
 // Tile order: expert by expert; inside an expert, bands of kRasterRows row tiles, and in a
@@ -233,13 +235,50 @@ __device__ __forceinline__ uint4 fp8x8_to_bf16(uint2 q, const uint32_t* m, bool 
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-template <int EPI, bool B_MN, int BN, bool PAIR, bool Q8>
-__global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams P) {
+// ---- NF4 -> bf16 by selection.  The 64 codes of a row share one scale, so the row's 16
+// possible values P[c] = bf16(T[c] * scale) are formed once and split into byte planes:
+// lo[q] holds the low bytes of P[4q .. 4q+3], hi[q] their high bytes.  A code's two bytes
+// are then picked with byte permutes: its low three bits choose one of the 8 bytes of a
+// pair of plane words, its high bit the pair.
+__device__ __forceinline__ void nf4_planes(const float* T, float s, uint32_t* lo, uint32_t* hi) {
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(__fmul_rn(T[2 * k], s), __fmul_rn(T[2 * k + 1], s));
+        w[k] = *reinterpret_cast<const uint32_t*>(&p);           // (P[2k], P[2k+1])
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        lo[q] = __byte_perm(w[2 * q], w[2 * q + 1], 0x6420);
+        hi[q] = __byte_perm(w[2 * q], w[2 * q + 1], 0x7531);
+    }
+}
+
+// 8 NF4 codes (one word, the first code in the low nibble) -> 8 bf16 values (four words)
+__device__ __forceinline__ uint4 nf4x8_to_bf16(uint32_t q, const uint32_t* lo, const uint32_t* hi) {
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t c = h ? q >> 16 : q;                       // codes 4h .. 4h+3 in the low nibbles
+        const uint32_t sel = c & 0x7777u;                         // byte within a pair of plane words
+        const uint32_t m = __byte_perm(0x0000FF00u, 0u, (c >> 3) & 0x1111u);   // 0xFF where code >= 8
+        const uint32_t l = (__byte_perm(lo[0], lo[1], sel) & ~m) | (__byte_perm(lo[2], lo[3], sel) & m);
+        const uint32_t u = (__byte_perm(hi[0], hi[1], sel) & ~m) | (__byte_perm(hi[2], hi[3], sel) & m);
+        o[2 * h] = __byte_perm(l, u, 0x5140);                     // (P[c0], P[c1])
+        o[2 * h + 1] = __byte_perm(l, u, 0x7362);                 // (P[c2], P[c3])
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <int EPI, bool B_MN, int BN, bool PAIR, int QB>
+__global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams P) {
     pdl_wait();      // no early trigger: dependents launch when this long kernel completes
     constexpr bool PAIRED = (EPI == EPI_SWIGLU);
-    using G = Geo<BN, PAIR, Q8>;
-    static_assert(!Q8 || BN == 256, "FP8 weights are for the expert GEMMs");
-    static_assert(!Q8 || PAIR, "FP8 weights run on SM pairs (each CTA dequantises half of the B tile)");
+    using G = Geo<BN, PAIR, QB>;
+    constexpr bool QW = QB != 0;                    // quantised weights (e4m3 or NF4 codes)
+    static_assert(QB == 0 || QB == 8 || QB == 4, "e4m3 or NF4 codes");
+    static_assert(!QW || BN == 256, "quantised weights are for the expert GEMMs");
+    static_assert(!QW || PAIR, "quantised weights run on SM pairs (each CTA dequantises half of the B tile)");
     constexpr int kStages = G::kStages;
     constexpr int kStageBytes = G::kStageBytes;
     constexpr int kAccCols = G::kAccCols;
@@ -282,7 +321,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
             // with FP8 weights the B half of a stage is complete when the converter group
             // that owns the stage has arrived (and, in a pair, the peer's group has completed
             // kSignalBytes transaction bytes on it)
-            tc::mbar_init(tc::smem_u32(&full_bar[s]), Q8 ? 2 : 1);
+            tc::mbar_init(tc::smem_u32(&full_bar[s]), QW ? 2 : 1);
             tc::mbar_init(tc::smem_u32(&empty_bar[s]), 1);
             tc::mbar_init(tc::smem_u32(&staged_bar[s]), 1);
         }
@@ -378,19 +417,23 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                     if constexpr (PAIR) {
                         // both CTAs' loads complete on the leader's full barrier
                         const uint32_t fb = tc::mapa(fb_local, 0);
-                        if (kb < nmain && Q8) {
+                        if (kb < nmain && QW) {
                             if (rank == 0) tc::mbar_arrive_expect_tx(fb_local, 2 * a_bytes + kSignalBytes);
                             tc::tma_load_2d_pair(sa, tma, fb, kb * BK, m0);
-                            const uint32_t sq = sb + G::kQBytes;
+                            // the codes land at the top of the B slot, plain rows of 64 codes
+                            // (64 bytes e4m3, 32 bytes NF4); a code row's byte coordinate is its
+                            // element coordinate * QB / 8
+                            const uint32_t sq = sb + G::kBBytes - G::kQBytes;
                             const uint32_t qb = tc::smem_u32(&staged_bar[stage]);
                             tc::mbar_arrive_expect_tx(qb, G::kQBytes);
                             if (B_MN) {
 #pragma unroll
                                 for (int jj = 0; jj < 2; ++jj)
-                                    tc::tma_load_3d(sq + jj * (kBoxMN / 2), &P.tm_b, qb,
-                                                    b_col_pair<PAIRED, BN>(half, (int)rank, jj, nt, g.Ncols), kb * BK, e);
+                                    tc::tma_load_3d(sq + jj * (kBoxMN * QB / 16), &P.tm_b, qb,
+                                                    b_col_pair<PAIRED, BN>(half, (int)rank, jj, nt, g.Ncols) * QB / 8,
+                                                    kb * BK, e);
                             } else {
-                                tc::tma_load_3d(sq, &P.tm_b, qb, kb * BK, nt * BN + (int)rank * (BN / 2), e);
+                                tc::tma_load_3d(sq, &P.tm_b, qb, kb * BK * QB / 8, nt * BN + (int)rank * (BN / 2), e);
                             }
                         } else if (kb < nmain) {
                             // k-blocks kb * KB2 .. of this stage, each in its own A + B sub-block
@@ -413,7 +456,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                             if (rank == 0) {
                                 tc::mbar_arrive_expect_tx(fb_local, 2 * (a2_bytes + 2 * P.b2_box_bytes));
                                 // FP8: the LoRA step needs no conversion; the producer makes both arrivals
-                                if (Q8) tc::mbar_arrive(fb_local);
+                                if (QW) tc::mbar_arrive(fb_local);
                             }
                             tc::tma_load_2d_pair(sa, tma2, fb, 0, m0);
 #pragma unroll
@@ -495,7 +538,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb) {
                     // FP8 pairs: the peer's converted half is published by a cluster-scope release
-                    if (!tc::mbar_wait<Q8 && PAIR>(tc::smem_u32(&full_bar[stage]), phase, lim)) {
+                    if (!tc::mbar_wait<QW && PAIR>(tc::smem_u32(&full_bar[stage]), phase, lim)) {
                         set_timeout(g, s_abort);
                         ok = false;
                         break;
@@ -550,13 +593,13 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                 else tc::mma_commit(tc::smem_u32(&tfull_bar[acc]));
             }
         }
-    } else if (Q8 && warp >= 2 + kEpiWarps) {
-        // ------------------------------------------------------------ FP8 dequantisers
-        // e4m3 codes (staging slot, plain row-major boxes of 64 bytes per row) -> bf16 in
-        // the 128-byte-swizzled layout TMA would have written: row r, 16-byte chunk cc of
-        // 8 elements at r * 128 + ((cc ^ (r & 7)) << 4); each value times its column's
+    } else if (QW && warp >= 2 + kEpiWarps) {
+        // ------------------------------------------------------------ dequantisers
+        // codes (staging slot, plain row-major boxes of 64 codes per row) -> bf16 in the
+        // 128-byte-swizzled layout TMA would have written: row r, 16-byte chunk cc of 8
+        // elements at r * 128 + ((cc ^ (r & 7)) << 4).  e4m3: each value times its column's
         // power-of-two scale (exact, fp8x8_to_bf16).
-        if constexpr (Q8) {
+        if constexpr (QB == 8) {
             constexpr int kGT = 32 * (kConvWarps / kConvGroups);    // threads of one group
             constexpr int kUnits = G::kQBytes / 8;                  // 8 codes per unit
             constexpr int kIters = kUnits / kGT;
@@ -615,7 +658,7 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                             fp8_multipliers(sc, fm[0], big[0]);
                         }
                         uint8_t* bt = smem + stage * kStageBytes + kABytes;
-                        const uint8_t* qt = bt + G::kQBytes;
+                        const uint8_t* qt = bt + G::kBBytes - G::kQBytes;
                         // all of the group's codes are read before any bf16 value overwrites them
                         uint2 q[kIters];
 #pragma unroll
@@ -643,6 +686,83 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                         // leader's (a cluster-scope arrive would hold the thread for a microsecond).
                         // The LoRA step is not converted: its producer makes both arrivals, after its
                         // wait for the stage to be free, so no arrival can reach an earlier phase.
+                        tc::named_bar_sync(1 + grp, kGT);
+                        if (gt == 0) {
+                            if (rank == 0) tc::mbar_arrive(tc::smem_u32(&full_bar[stage]));
+                            else tc::st_async_signal(sig_leader, 1u, full_leader0 + stage * (uint32_t)sizeof(uint64_t));
+                        }
+                        ++done;
+                    }
+                    if (++stage == kStages) stage = 0;
+                }
+            }
+            if (gt == 0) s_issued[1 + grp] = done;
+        } else if constexpr (QB == 4) {
+            // NF4: plain rows of 32 bytes (64 codes, two per byte, the even element in the
+            // low nibble) -> bf16(T[code] * absmax).  One thread per B row of the stage (64 k
+            // rows x 2 boxes of an MN-major B, 128 n rows of a K-major B); each such row is
+            // one 64-element block with one scale, so the thread forms its 16 possible values
+            // once and then only selects among them (nf4x8_to_bf16).  Stage ownership,
+            // barriers and the signal are those of the e4m3 converter.
+            constexpr int kGT = 32 * (kConvWarps / kConvGroups);    // threads of one group
+            static_assert(kGT == 128 && G::kQBytes == 128 * 32, "one 32-byte code row per converter thread");
+            static_assert(kStages % kConvGroups == 0, "every group owns whole stages");
+            const int ct = threadIdx.x - 32 * (2 + kEpiWarps);
+            const int grp = ct / kGT;
+            const int gt = ct % kGT;
+            const int jb = B_MN ? gt >> 6 : 0;                      // MN-major: the thread's 64-column box
+            const int r = B_MN ? gt & 63 : gt;                      // its row: k in the box, or n in the tile
+            const uint32_t full_leader0 = tc::mapa(tc::smem_u32(&full_bar[0]), 0);
+            const uint32_t sig_leader = tc::mapa(tc::smem_u32(sig_slot), 0);
+            const int64_t nblk = g.ldb / 64;                        // scale blocks per row of B[e]
+            const int64_t b_rows = g.b_expert_stride / g.ldb;
+            int stage = 0;
+            uint32_t sbits = 0;                                     // per-stage parity of staged_bar
+            int done = 0;                                           // stages this group has signalled
+            bool ok = true;
+            for (int t = tile0; t < total_tiles && ok; t += tile_step) {
+                int e, mt, nt;
+                decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
+                const float* se = g.b_scale + (int64_t)e * (g.b_expert_stride / 64);
+                // the thread's scale: MN-major, row kb * 64 + r of B[e] in the box's column
+                // block; K-major, row n of B[e] in the stage's k block (-1: outside B[e])
+                int64_t s_idx = -1, s_step;
+                if constexpr (B_MN) {
+                    const int col = b_col_pair<PAIRED, BN>(half_tile(s_off, e, mt), (int)rank, jb, nt, g.Ncols);
+                    if (col < g.ldb) s_idx = (int64_t)r * nblk + col / 64;
+                    s_step = 64 * nblk;
+                } else {
+                    const int64_t n = (int64_t)nt * BN + (int)rank * (BN / 2) + r;
+                    if (n < b_rows) s_idx = n * nblk;
+                    s_step = 1;
+                }
+                const int nkb = P.num_kb + (P.lora_k16 ? 1 : 0);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    const bool mine = (stage % kConvGroups) == grp;
+                    if (mine && kb < P.num_kb) {
+                        // loaded before the wait, used after it
+                        const float sc = s_idx < 0 ? 0.f : __ldg(se + s_idx + kb * s_step);
+                        const bool got = tc::mbar_wait(tc::smem_u32(&staged_bar[stage]), (sbits >> stage) & 1u, lim);
+                        if (!tc::named_bar_and(1 + grp, kGT, got && !*s_abort)) {
+                            if (gt == 0) set_timeout(g, s_abort);
+                            ok = false;
+                            break;
+                        }
+                        sbits ^= 1u << stage;
+                        uint8_t* bt = smem + stage * kStageBytes + kABytes;
+                        const uint4* qrow = reinterpret_cast<const uint4*>(bt + G::kBBytes - G::kQBytes + jb * 2048 + r * 32);
+                        const uint4 q0 = qrow[0], q1 = qrow[1];
+                        uint32_t lo[4], hi[4];
+                        nf4_planes(P.nf4, sc, lo, hi);
+                        // all of the group's codes are read before any bf16 value overwrites them
+                        tc::named_bar_sync(1 + grp, kGT);
+                        uint8_t* row = bt + jb * kBoxMN + r * 128;
+                        const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                        for (int cc = 0; cc < 8; ++cc)
+                            *reinterpret_cast<uint4*>(row + ((cc ^ (r & 7)) << 4)) = nf4x8_to_bf16(qw[cc], lo, hi);
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        // one signal per group and converted stage, as in the e4m3 converter
                         tc::named_bar_sync(1 + grp, kGT);
                         if (gt == 0) {
                             if (rank == 0) tc::mbar_arrive(tc::smem_u32(&full_bar[stage]));
@@ -847,33 +967,33 @@ __global__ void __launch_bounds__(threads_of(Q8), 1) grouped_gemm_tc_kernel(cons
                     const bool main = G::KW > 1 || kb < nmain;        // not the LoRA step
                     const uint32_t spar = (sbits >> st) & 1u;
                     int gi = 0;                                       // index among its group's code stages
-                    if (Q8 && main) {
+                    if (QW && main) {
                         sbits ^= 1u << st;
                         gi = gcount[st % kConvGroups]++;
                     }
                     if (f < w0) continue;
-                    if (Q8 && main && f < own_f) tc::mbar_wait(tc::smem_u32(&staged_bar[st]), spar);
+                    if (QW && main && f < own_f) tc::mbar_wait(tc::smem_u32(&staged_bar[st]), spar);
                     if (rank != 0) continue;
                     // bytes that one CTA's copies of this fill complete on the full barrier
                     uint32_t b;
                     if (G::KW > 1) b = min(G::KW, P.num_kb - kb * G::KW) * (kABytes + BN * BK * 2);
-                    else if (main) b = ((half ? kABytes / 2 : kABytes) + (Q8 ? 0 : G::kBBytes)) * min(KB2, P.num_kb - kb * KB2);
+                    else if (main) b = ((half ? kABytes / 2 : kABytes) + (QW ? 0 : G::kBBytes)) * min(KB2, P.num_kb - kb * KB2);
                     else b = (half ? P.a2_bytes / 2 : P.a2_bytes) + (PAIR ? 2 : 4) * P.b2_box_bytes;
                     const bool lp = f < f_lead, pp = PAIR && f < f_peer;
                     if (!lp && !pp) continue;                         // no copy went towards this phase
                     const int grp = st % kConvGroups;
-                    const bool lc = Q8 && main && gi < s_issued[1 + grp];
-                    const bool ps = Q8 && PAIR && main && gi < peer_done[grp];
+                    const bool lc = QW && main && gi < s_issued[1 + grp];
+                    const bool ps = QW && PAIR && main && gi < peer_done[grp];
                     const uint32_t fb = tc::smem_u32(&full_bar[st]);
                     if (!lp) {
                         // only the peer issued this fill: the leader's arrivals, expecting what came
                         tc::mbar_arrive_expect_tx(fb, (pp ? b : 0u) + (ps ? (uint32_t)kSignalBytes : 0u));
-                        if (Q8) tc::mbar_arrive(fb);
+                        if (QW) tc::mbar_arrive(fb);
                     } else {
                         const uint32_t missing =
-                            (PAIR && !pp ? b : 0u) + (Q8 && PAIR && main && !ps ? (uint32_t)kSignalBytes : 0u);
+                            (PAIR && !pp ? b : 0u) + (QW && PAIR && main && !ps ? (uint32_t)kSignalBytes : 0u);
                         if (missing) tc::mbar_complete_tx(fb, missing);
-                        if (Q8 && main && !lc) tc::mbar_arrive(fb);
+                        if (QW && main && !lc) tc::mbar_arrive(fb);
                     }
                     tc::mbar_wait(tc::smem_u32(&full_bar[st]), (uint32_t)(f / kStages) & 1u);
                 }
@@ -946,10 +1066,10 @@ int sm_count() {
 
 // One CTA per SM (grid = min(#SMs, tiles)); SM pairs: as many 2-CTA clusters as can be
 // resident at once (so that no pair waits for another to finish), at most one per tile.
-template <int EPI, bool B_MN, int BN, bool PAIR, bool Q8 = false>
+template <int EPI, bool B_MN, int BN, bool PAIR, int QB = 0>
 cudaError_t launch_tc(const TcParams& P, int64_t max_tiles, size_t smem, cudaStream_t s) {
-    auto k = grouped_gemm_tc_kernel<EPI, B_MN, BN, PAIR, Q8>;
-    constexpr int kThr = threads_of(Q8);
+    auto k = grouped_gemm_tc_kernel<EPI, B_MN, BN, PAIR, QB>;
+    constexpr int kThr = threads_of(QB != 0);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if constexpr (!PAIR) {
@@ -1005,10 +1125,13 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
     P.num_kb = g.K / BK;
     P.wait_ns = tc::kWaitTimeoutNs;
     const bool paired = g.epi == EPI_SWIGLU;
-    const bool q8 = g.b_scale != nullptr;
-    // FP8 weights always run on SM pairs: each CTA dequantises half of the B tile
-    const bool pair = allow_pairs && !proj && (q8 || use_sm_pairs(g));
-    if (q8 && (proj || g.ldb % 64 != 0)) return cudaErrorInvalidValue;
+    const int qb = g.b_quant;                       // bits per code of a quantised B (0: bf16)
+    if (qb != 0 && qb != 8 && qb != 4) return cudaErrorInvalidValue;
+    if (qb != 0 && g.b_scale == nullptr) return cudaErrorInvalidValue;
+    // quantised weights always run on SM pairs: each CTA dequantises half of the B tile
+    const bool pair = allow_pairs && !proj && (qb != 0 || use_sm_pairs(g));
+    if (qb != 0 && (proj || g.ldb % 64 != 0)) return cudaErrorInvalidValue;
+    if (qb == 4) memcpy(P.nf4, nf4_table().v, sizeof(P.nf4));
     // kernels exist for the layer's four expert GEMMs (below) and the projections
     if (!proj && g.epi != EPI_SWIGLU && g.epi != EPI_BF16 && g.epi != EPI_DSWIGLU) return cudaErrorInvalidValue;
     if (g.epi == EPI_DSWIGLU && g.b_mn_major) return cudaErrorInvalidValue;   // built for a K-major B only
@@ -1029,10 +1152,14 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
         const uint64_t st[2] = {(uint64_t)g.ldb * 2, (uint64_t)g.b_expert_stride * 2};
         const uint32_t box_mn[3] = {64, BK, 1};
         const uint32_t box_k[3] = {BK, (uint32_t)(pair ? BN / 2 : BN), 1};
-        if (q8) {
-            // e4m3 codes, one byte each, landed unswizzled in the staging slot
-            const uint64_t st8[2] = {(uint64_t)g.ldb, (uint64_t)g.b_expert_stride};
-            if (!encode(&P.tm_b, g.B, 3, dims, st8, g.b_mn_major ? box_mn : box_k, CU_TENSOR_MAP_SWIZZLE_NONE,
+        if (qb != 0) {
+            // codes landed unswizzled in the staging slot, addressed as bytes: e4m3 one per
+            // byte, NF4 two per byte (a 64-element row of a box is 32 bytes)
+            const uint64_t dims_q[3] = {(uint64_t)g.ldb * qb / 8, rows, (uint64_t)g.E};
+            const uint64_t st_q[2] = {(uint64_t)g.ldb * qb / 8, (uint64_t)g.b_expert_stride * qb / 8};
+            const uint32_t box_mn_q[3] = {(uint32_t)(64 * qb / 8), BK, 1};
+            const uint32_t box_k_q[3] = {(uint32_t)(BK * qb / 8), (uint32_t)(BN / 2), 1};
+            if (!encode(&P.tm_b, g.B, 3, dims_q, st_q, g.b_mn_major ? box_mn_q : box_k_q, CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_DATA_TYPE_UINT8))
                 return cudaErrorInvalidValue;
         } else if (!encode(&P.tm_b, g.B, 3, dims, st, g.b_mn_major ? box_mn : box_k, CU_TENSOR_MAP_SWIZZLE_128B)) {
@@ -1080,15 +1207,26 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
     // The layer's expert GEMMs: gate_up forward (SwiGLU, MN-major B), down forward (bf16,
     // MN-major B), down backward (SwiGLU backward, K-major B: W_d read transposed) and
     // gate_up backward (bf16, K-major B: W_gu read transposed).
-    if (q8) {
-        if (!pair) return cudaErrorNotSupported;   // FP8 weights run on SM pairs only
-        const size_t smem = Geo<256, true, true>::kSmem + offs_bytes;
+    if (qb == 8) {
+        if (!pair) return cudaErrorNotSupported;   // quantised weights run on SM pairs only
+        const size_t smem = Geo<256, true, 8>::kSmem + offs_bytes;
         switch (g.epi) {
-            case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256, true, true>(P, max_tiles, smem, s);
+            case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256, true, 8>(P, max_tiles, smem, s);
             case EPI_BF16:
-                return mn ? launch_tc<EPI_BF16, true, 256, true, true>(P, max_tiles, smem, s)
-                          : launch_tc<EPI_BF16, false, 256, true, true>(P, max_tiles, smem, s);
-            default: return launch_tc<EPI_DSWIGLU, false, 256, true, true>(P, max_tiles, smem, s);
+                return mn ? launch_tc<EPI_BF16, true, 256, true, 8>(P, max_tiles, smem, s)
+                          : launch_tc<EPI_BF16, false, 256, true, 8>(P, max_tiles, smem, s);
+            default: return launch_tc<EPI_DSWIGLU, false, 256, true, 8>(P, max_tiles, smem, s);
+        }
+    }
+    if (qb == 4) {
+        if (!pair) return cudaErrorNotSupported;
+        const size_t smem = Geo<256, true, 4>::kSmem + offs_bytes;
+        switch (g.epi) {
+            case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256, true, 4>(P, max_tiles, smem, s);
+            case EPI_BF16:
+                return mn ? launch_tc<EPI_BF16, true, 256, true, 4>(P, max_tiles, smem, s)
+                          : launch_tc<EPI_BF16, false, 256, true, 4>(P, max_tiles, smem, s);
+            default: return launch_tc<EPI_DSWIGLU, false, 256, true, 4>(P, max_tiles, smem, s);
         }
     }
     if (pair) {

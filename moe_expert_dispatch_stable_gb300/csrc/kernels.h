@@ -32,9 +32,8 @@ cudaError_t route_static_scratch(void** ptr);
 cudaError_t launch_gather_rows(const void* src, int H, const int32_t* perm, const float* w_sorted,
                                int64_t N, int k, void* dst, const void* O, float* d_w, int32_t* status,
                                cudaStream_t s);
-// out[t, :] = bf16( sum_{j<k} w * src[inv_perm[t*k+j], :] ), w = w_sorted[inv_perm[t*k+j]] (or 1 when
-// w_sorted is null); bf16 or fp32 src, fp32 sum in the fixed order j = 0..k-1
-// out[t] = sum_j w_j * src[inv_perm[t*k+j]] over bf16 slot rows (w_sorted NULL: weights 1)
+// out[t, :] = bf16( sum_{j<k} w * src[inv_perm[t*k+j], :] ) over bf16 slot rows, w = w_sorted[inv_perm[t*k+j]]
+// (or 1 when w_sorted is null), fp32 sum in the fixed order j = 0..k-1
 cudaError_t launch_combine(const void* src, const float* w_sorted, const int32_t* inv_perm, int64_t T, int k, int H,
                            void* out, int32_t* status, cudaStream_t s);
 // h [N, I] = SwiGLU of GU [N, 2I] row by row (bf16 in and out)
@@ -43,6 +42,20 @@ cudaError_t launch_swiglu_rows(const void* gu, int I, int64_t N, void* h, cudaSt
 // ---- FP8 expert weights (quant.cu)
 // scale[m, c] = 2^ceil(log2(amax_r |W[m, r, c]| / 448)), Wq[m, r, c] = e4m3_rn(W[m, r, c] / scale[m, c])
 cudaError_t launch_quantize_fp8(const void* W, int64_t n_mat, int64_t rows, int cols, void* Wq, float* scale,
+                                cudaStream_t s);
+
+// ---- NF4 (4-bit NormalFloat) expert weights (quant.cu)
+// The 16 NF4 code values, ascending, computed once on the host from their definition
+// (normal quantiles at evenly spaced probabilities, normalised to [-1, 1]).
+struct Nf4Table {
+    float v[16];
+};
+const Nf4Table& nf4_table();
+// Per 64 consecutive elements of a row: absmax[m, r, b] = max |W|; each element's code is
+// the nearest table value to W / absmax (float32, ties to the lower code; code 7 when the
+// block is all zero); Wq packs two codes per byte, the even column in the low nibble.
+// cols % 64 == 0.
+cudaError_t launch_quantize_nf4(const void* W, int64_t n_mat, int64_t rows, int cols, void* Wq, float* absmax,
                                 cudaStream_t s);
 
 // ---- router (router.cu)
@@ -93,7 +106,10 @@ struct GroupedGemm {
     const void* A;        // [N, K] bf16, K contiguous
     const void* B;        // bf16 expert stack
     bool b_mn_major;      // true: B_e(c, n) = B[e][c][n] (row length ldb); false: B[e][n][c]
-    const float* b_scale; // non-null: B holds e4m3 codes, value = code * b_scale[e * ldb + column of B[e]]
+    int b_quant;          // 0: bf16 B; 8: e4m3 codes, value = code * b_scale[e * ldb + column of B[e]];
+                          // 4: NF4 codes, two per byte, value = bf16(T[code] * b_scale[block]), one
+                          //    scale per 64 consecutive elements of a row of B[e]
+    const float* b_scale; // the scales of a quantised B
     int ldb;              // elements per row of B[e]
     int64_t b_expert_stride;  // elements between experts
     const void* A2;       // [N, RP] bf16 (LoRA rank activations, pre-scaled by s), or null

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.moe_abi_version() == 6
+    assert lib.moe_abi_version() == 7
     for code in range(0, 7):
         assert lib.moe_status_string(code)
 
@@ -149,6 +149,46 @@ def test_fp8_entry_points_host_checks(lib):
     for call in (fwd, bwd):
         assert call(None, w16) == 1 and call(w16, None) == 1
         assert call(v(20), w16) == 3 and call(w16, v(20)) == 3
+
+
+def test_nf4_entry_points_host_checks(lib):
+    from moe_expert_dispatch_stable_gb300 import binding as b
+    v = ctypes.c_void_p
+    # quantiser: rows of a multiple of 64 elements, NULL buffers with a non-empty tensor, misalignment
+    assert lib.moe_quantize_nf4(v(16), 2, 4, 96, v(16), v(16), None) == 2
+    assert lib.moe_quantize_nf4(v(16), -1, 4, 64, v(16), v(16), None) == 2
+    assert lib.moe_quantize_nf4(None, 2, 4, 64, v(16), v(16), None) == 1
+    assert lib.moe_quantize_nf4(v(16), 2, 4, 64, v(16), v(24), None) == 3
+    assert lib.moe_quantize_nf4(None, 0, 4, 64, None, None, None) == 0        # empty: nothing to do
+    assert lib.moe_nf4_codebook(None) == 1
+    rt = b.moe_routing(16, 16, 16, 16, 16, 16)
+    d = b.Dims(8, 64, 64, 4, 2, 4, 2.0).c_struct()
+    w16, a32 = v(16), v(32)
+
+    def fwd(m_gu, m_d):
+        return lib.moe_lora_fwd_nf4(ctypes.byref(d), ctypes.byref(rt), a32, w16, m_gu, w16, w16, w16, m_d, w16, w16,
+                                    a32, a32, 1 << 30, a32, 1 << 30, w16, None)
+
+    def bwd(m_gu, m_d):
+        return lib.moe_lora_bwd_nf4(ctypes.byref(d), ctypes.byref(rt), a32, w16, m_gu, w16, w16, w16, m_d, w16, w16,
+                                    a32, 1 << 30, a32, w16, w16, w16, w16, None, a32, 1 << 30, w16, None)
+
+    # the block scales are required and 16-byte aligned
+    for call in (fwd, bwd):
+        assert call(None, w16) == 1 and call(w16, None) == 1
+        assert call(v(20), w16) == 3 and call(w16, v(20)) == 3
+
+
+def test_nf4_codebook_equals_the_oracle_bit_for_bit(lib):
+    """The library computes its 16 NF4 values on the host from their definition (inverse
+    normal CDF by bisection on erfc); the oracle takes scipy's inverse CDF.  Both round to
+    float32, and the tables agree bit for bit."""
+    import numpy as np
+
+    from moe_expert_dispatch_stable_gb300 import binding as b
+    from oracle import nf4_oracle as nf
+    got = np.array(b.moe_nf4_codebook(), dtype=np.float32)
+    np.testing.assert_array_equal(got.view(np.uint32), nf.nf4_codebook().view(np.uint32))
 
 
 def test_timing_diagnostics_host_side(lib):
