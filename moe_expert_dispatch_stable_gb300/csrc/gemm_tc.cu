@@ -737,11 +737,15 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
                     s_step = 1;
                 }
                 const int nkb = P.num_kb + (P.lora_k16 ? 1 : 0);
+                auto scale_at = [&](int k) { return (s_idx < 0 || k >= P.num_kb) ? 0.f : __ldg(se + s_idx + k * s_step); };
+                // the scales run one owned stage ahead of the conversion, so that their load
+                // latency is not part of a stage's chain: first the group's first k block of
+                // the tile (stage indices advance by one per k block, kStages % kConvGroups == 0)
+                float sc = scale_at(((grp - stage) % kConvGroups + kConvGroups) % kConvGroups);
                 for (int kb = 0; kb < nkb; ++kb) {
                     const bool mine = (stage % kConvGroups) == grp;
                     if (mine && kb < P.num_kb) {
-                        // loaded before the wait, used after it
-                        const float sc = s_idx < 0 ? 0.f : __ldg(se + s_idx + kb * s_step);
+                        const float sc_next = scale_at(kb + kConvGroups);
                         const bool got = tc::mbar_wait(tc::smem_u32(&staged_bar[stage]), (sbits >> stage) & 1u, lim);
                         if (!tc::named_bar_and(1 + grp, kGT, got && !*s_abort)) {
                             if (gt == 0) set_timeout(g, s_abort);
@@ -769,6 +773,7 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
                             else tc::st_async_signal(sig_leader, 1u, full_leader0 + stage * (uint32_t)sizeof(uint64_t));
                         }
                         ++done;
+                        sc = sc_next;
                     }
                     if (++stage == kStages) stage = 0;
                 }
