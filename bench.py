@@ -347,7 +347,7 @@ def quant_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, steps: int, flush, f
         q8.step(t_idx, t_w, ts["x"], ts["dy"], with_topk_grad=False)
     torch.cuda.synchronize()
     moe.moe_timing_enable(True)
-    ms = 0.0
+    per_step = []
     for _ in range(steps):
         flush.zero_()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -355,7 +355,7 @@ def quant_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, steps: int, flush, f
         q8.step(t_idx, t_w, ts["x"], ts["dy"], with_topk_grad=False)
         e.record()
         torch.cuda.synchronize()
-        ms += s.elapsed_time(e)
+        per_step.append(s.elapsed_time(e))
     moe.moe_timing_enable(False)
     kt = moe.moe_timing_read()
     assert int(q8.dev_status.item()) == 0
@@ -363,7 +363,10 @@ def quant_measurement(cfg, layer, ts, t_idx, t_w, moe, dev, steps: int, flush, f
     kernels = {n: round(v[0] / steps, 4) for n, v in kt.items() if n in GEMM_KERNELS}
     wbytes = sum(t.numel() * t.element_size() for n, t in wq.items() if n.startswith(QUANT_KEYS[fmt]))
     del q8, wq
-    return {"ms_per_step": ms / steps, "tokens_per_s": cfg.T * steps / (ms / 1e3), "gemm_ms_per_step": gemm_ms,
+    ms = sum(per_step)
+    # the median beside the mean: a side line of few steps, where one slow step shows
+    return {"ms_per_step": ms / steps, "median_ms_per_step": sorted(per_step)[steps // 2],
+            "tokens_per_s": cfg.T * steps / (ms / 1e3), "gemm_ms_per_step": gemm_ms,
             "gemm_kernels_ms_per_step": kernels, "base_weight_bytes": wbytes, "steps": steps}
 
 
