@@ -238,8 +238,9 @@ __device__ __forceinline__ uint4 fp8x8_to_bf16(uint2 q, const uint32_t* m, bool 
 // ---- NF4 -> bf16 by selection.  The 64 codes of a row share one scale, so the row's 16
 // possible values P[c] = bf16(T[c] * scale) are formed once and split into byte planes:
 // lo[q] holds the low bytes of P[4q .. 4q+3], hi[q] their high bytes.  A code's two bytes
-// are then picked with byte permutes: its low three bits choose one of the 8 bytes of a
-// pair of plane words, its high bit the pair.
+// are then picked with byte permutes: its low three bits choose one of the 8 bytes of
+// each pair of plane words (codes 0-7, codes 8-15), and a third permute, steered by its
+// high bit, keeps the right one of the two.
 __device__ __forceinline__ void nf4_planes(const float* T, float s, uint32_t* lo, uint32_t* hi) {
     uint32_t w[8];
 #pragma unroll
@@ -254,18 +255,21 @@ __device__ __forceinline__ void nf4_planes(const float* T, float s, uint32_t* lo
     }
 }
 
-// 8 NF4 codes (one word, the first code in the low nibble) -> 8 bf16 values (four words)
+// 8 NF4 codes (one word, the first code in the low nibble) -> 8 bf16 values (four words);
+// 21 integer instructions
 __device__ __forceinline__ uint4 nf4x8_to_bf16(uint32_t q, const uint32_t* lo, const uint32_t* hi) {
+    const uint32_t sel = q & 0x77777777u;                          // byte within a pair of plane words
+    // result byte i of a two-word permute: byte i of the first word, or of the second
+    // (selector i + 4) where the code is >= 8
+    const uint32_t pick = ((q >> 1) & 0x44444444u) | 0x32103210u;
     uint32_t o[4];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const uint32_t c = h ? q >> 16 : q;                       // codes 4h .. 4h+3 in the low nibbles
-        const uint32_t sel = c & 0x7777u;                         // byte within a pair of plane words
-        const uint32_t m = __byte_perm(0x0000FF00u, 0u, (c >> 3) & 0x1111u);   // 0xFF where code >= 8
-        const uint32_t l = (__byte_perm(lo[0], lo[1], sel) & ~m) | (__byte_perm(lo[2], lo[3], sel) & m);
-        const uint32_t u = (__byte_perm(hi[0], hi[1], sel) & ~m) | (__byte_perm(hi[2], hi[3], sel) & m);
-        o[2 * h] = __byte_perm(l, u, 0x5140);                     // (P[c0], P[c1])
-        o[2 * h + 1] = __byte_perm(l, u, 0x7362);                 // (P[c2], P[c3])
+        const uint32_t s = h ? sel >> 16 : sel, p = h ? pick >> 16 : pick;   // codes 4h .. 4h+3
+        const uint32_t l = __byte_perm(__byte_perm(lo[0], lo[1], s), __byte_perm(lo[2], lo[3], s), p);
+        const uint32_t u = __byte_perm(__byte_perm(hi[0], hi[1], s), __byte_perm(hi[2], hi[3], s), p);
+        o[2 * h] = __byte_perm(l, u, 0x5140);                      // (P[c0], P[c1])
+        o[2 * h + 1] = __byte_perm(l, u, 0x7362);                  // (P[c2], P[c3])
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
