@@ -291,13 +291,15 @@ MOE_API moe_status moe_lora_bwd_fp8(const moe_dims* d, const moe_routing* rt, co
  * 2026 changes", model table; the GPU MODE lecture 32 notes, open questions, name QLoRA's
  * NF4), read as QLoRA's 4-bit NormalFloat data type.  Per matrix m, row r and block b of
  * 64 consecutive columns of W [n_mat, rows, cols] (bf16, cols a multiple of 64):
- *   absmax[m, r, b] = max |W[m, r, 64b .. 64b+63]|
+ *   absmax[m, b, r] = max |W[m, r, 64b .. 64b+63]|   (block-major: one column block's scales
+ *                     are contiguous over the rows, so a GEMM stage fetches its scales as one
+ *                     run with its codes)
  *   code of W[m, r, c] = the i in 0..15 whose T[i] is nearest to W[m, r, c] / absmax (both in
  *                        float32, the lower i on a tie; 7, the zero, when absmax is 0)
  *   Wq[m, r, c / 2]    = code(c even) | code(c odd) << 4
  * T = moe_nf4_codebook.  The dequantised weight is bf16(T[code] * absmax), the product in
  * float32 rounded to nearest even.  Wq uint8 [n_mat, rows, cols / 2], absmax float32
- * [n_mat, rows, cols / 64].  One kernel; weight preparation, not the hot path.
+ * [n_mat, cols / 64, rows].  One kernel; weight preparation, not the hot path.
  * MOE_ERR_BAD_DIMS when cols is not a multiple of 64. */
 MOE_API moe_status moe_quantize_nf4(const uint16_t* W, int64_t n_mat, int64_t rows, int32_t cols,
                                     uint8_t* Wq, float* absmax, void* stream);
@@ -309,8 +311,8 @@ MOE_API moe_status moe_quantize_nf4(const uint16_t* W, int64_t n_mat, int64_t ro
 MOE_API moe_status moe_nf4_codebook(float* values);
 
 /* moe_lora_fwd / moe_lora_bwd with NF4 base weights: Wq_gu [E, H, I] bytes (2I codes per row)
- * and Wq_d [E, I, H / 2] with block scales absmax_gu [E, H, 2I / 64] and absmax_d
- * [E, I, H / 64] (moe_quantize_nf4).  The GEMMs stream the codes (a quarter of the bytes of
+ * and Wq_d [E, I, H / 2] with block scales absmax_gu [E, 2I / 64, H] and absmax_d
+ * [E, H / 64, I] (moe_quantize_nf4).  The GEMMs stream the codes (a quarter of the bytes of
  * bf16) and dequantise them to bf16 in shared memory before the tensor cores read them, so
  * the results are bit-identical to moe_lora_fwd / moe_lora_bwd called with the dequantised
  * bf16 weights.  LoRA factors and activations stay bf16; same saved / workspace sizes; SM

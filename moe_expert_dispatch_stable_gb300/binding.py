@@ -435,14 +435,14 @@ def moe_quantize_fp8(W: torch.Tensor, stream=None):
 def moe_quantize_nf4(W: torch.Tensor, stream=None):
     """NF4 codes (two per byte) and per-64-element absmax scales of a bf16 weight stack
     [..., rows, cols], cols a multiple of 64; returns (Wq uint8 [..., rows, cols / 2],
-    absmax float32 [..., rows, cols / 64])."""
+    absmax float32 [..., cols / 64, rows], block-major)."""
     _need(W, "W", torch.bfloat16)
     rows, cols = W.shape[-2], W.shape[-1]
     if cols % 64:
         raise MoEError("NF4 quantisation needs rows of a multiple of 64 elements")
     n_mat = W.numel() // max(rows * cols, 1)
     Wq = torch.empty(W.shape[:-1] + (cols // 2,), dtype=torch.uint8, device=W.device)
-    am = torch.empty(W.shape[:-1] + (cols // 64,), dtype=torch.float32, device=W.device)
+    am = torch.empty(W.shape[:-2] + (cols // 64, rows), dtype=torch.float32, device=W.device)
     _check(load_library().moe_quantize_nf4(_ptr(W), n_mat, rows, cols, _ptr(Wq), _ptr(am), _stream(stream)))
     return Wq, am
 
@@ -489,9 +489,9 @@ def _fp8_args(d: Dims, w: dict):
 
 def _nf4_args(d: Dims, w: dict):
     _need(w["W4_gu"], "W4_gu", torch.uint8, (d.E, d.H, d.I))
-    _need(w["m_gu"], "m_gu", torch.float32, (d.E, d.H, 2 * d.I // 64))
+    _need(w["m_gu"], "m_gu", torch.float32, (d.E, 2 * d.I // 64, d.H))
     _need(w["W4_d"], "W4_d", torch.uint8, (d.E, d.I, d.H // 2))
-    _need(w["m_d"], "m_d", torch.float32, (d.E, d.I, d.H // 64))
+    _need(w["m_d"], "m_d", torch.float32, (d.E, d.H // 64, d.I))
     _lora_factor_checks(d, w)
     return [_ptr(w[n]) for n in ("W4_gu", "m_gu", "A_gu", "B_gu", "W4_d", "m_d", "A_d", "B_d")]
 

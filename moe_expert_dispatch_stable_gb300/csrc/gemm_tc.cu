@@ -78,12 +78,16 @@ struct Geo {
     static constexpr int kStages = PAIR ? 6 / KB2 : (BN >= 256 ? 4 : (216 * 1024) / kStageBytes);
     static constexpr int kAccCols = BN;
     static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
+    // NF4: the block scales of a stage's B half (128 rows of one 64-element block each) land
+    // by TMA with its codes, in a slot of their own after the ring
+    static constexpr int kScaleBytes = QB == 4 ? 128 * 4 : 0;
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * (kStageBytes + kScaleBytes) + 256;
 };
 
 struct TcParams {
     CUtensorMap tm_a, tm_b, tm_a2, tm_b2;
     CUtensorMap tm_a64, tm_a2_64;   // SM pairs: 64-row boxes of A / A2 for half tiles
+    CUtensorMap tm_bs;              // NF4: block scales [E][ldb / 64][rows of B[e]] (float32)
     GroupedGemm g;
     int num_kb;         // K / 64
     int lora_k16;       // RP / 16 (0: no LoRA step)
@@ -292,7 +296,8 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
     static_assert(!PAIR || BN == 256, "SM pairs run the 256-wide expert GEMMs only");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    float* s_scale = reinterpret_cast<float*>(smem + kStages * kStageBytes);   // NF4: kStages x 128 scales
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * (kStageBytes + G::kScaleBytes));
     uint64_t* empty_bar = full_bar + kStages;
     uint64_t* tfull_bar = empty_bar + kStages;
     uint64_t* tempty_bar = tfull_bar + 2;
@@ -363,6 +368,7 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
         tc::prefetch_tmap(&P.tm_a);
         tc::prefetch_tmap(&P.tm_b);
         if (PAIR) tc::prefetch_tmap(&P.tm_a64);
+        if (QB == 4) tc::prefetch_tmap(&P.tm_bs);
         if (P.lora_k16) {
             tc::prefetch_tmap(&P.tm_a2);
             tc::prefetch_tmap(&P.tm_b2);
@@ -429,15 +435,22 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
                             // element coordinate * QB / 8
                             const uint32_t sq = sb + G::kBBytes - G::kQBytes;
                             const uint32_t qb = tc::smem_u32(&staged_bar[stage]);
-                            tc::mbar_arrive_expect_tx(qb, G::kQBytes);
+                            // NF4: the stage's block scales come with its codes, on the same barrier
+                            const uint32_t ss = tc::smem_u32(s_scale + stage * 128);
+                            tc::mbar_arrive_expect_tx(qb, G::kQBytes + G::kScaleBytes);
                             if (B_MN) {
 #pragma unroll
-                                for (int jj = 0; jj < 2; ++jj)
-                                    tc::tma_load_3d(sq + jj * (kBoxMN * QB / 16), &P.tm_b, qb,
-                                                    b_col_pair<PAIRED, BN>(half, (int)rank, jj, nt, g.Ncols) * QB / 8,
-                                                    kb * BK, e);
+                                for (int jj = 0; jj < 2; ++jj) {
+                                    const int col = b_col_pair<PAIRED, BN>(half, (int)rank, jj, nt, g.Ncols);
+                                    tc::tma_load_3d(sq + jj * (kBoxMN * QB / 16), &P.tm_b, qb, col * QB / 8, kb * BK, e);
+                                    // 64 k rows of the box's column block (a block past B[e]'s columns reads zeros)
+                                    if (QB == 4) tc::tma_load_3d(ss + jj * 256, &P.tm_bs, qb, kb * BK, col / 64, e);
+                                }
                             } else {
-                                tc::tma_load_3d(sq, &P.tm_b, qb, kb * BK * QB / 8, nt * BN + (int)rank * (BN / 2), e);
+                                const int n0 = nt * BN + (int)rank * (BN / 2);
+                                tc::tma_load_3d(sq, &P.tm_b, qb, kb * BK * QB / 8, n0, e);
+                                // 128 n rows of the stage's k block (rows past B[e] read zeros)
+                                if (QB == 4) tc::tma_load_3d(ss, &P.tm_bs, qb, n0, kb, e);
                             }
                         } else if (kb < nmain) {
                             // k-blocks kb * KB2 .. of this stage, each in its own A + B sub-block
@@ -718,38 +731,15 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
             const int r = B_MN ? gt & 63 : gt;                      // its row: k in the box, or n in the tile
             const uint32_t full_leader0 = tc::mapa(tc::smem_u32(&full_bar[0]), 0);
             const uint32_t sig_leader = tc::mapa(tc::smem_u32(sig_slot), 0);
-            const int64_t nblk = g.ldb / 64;                        // scale blocks per row of B[e]
-            const int64_t b_rows = g.b_expert_stride / g.ldb;
             int stage = 0;
             uint32_t sbits = 0;                                     // per-stage parity of staged_bar
             int done = 0;                                           // stages this group has signalled
             bool ok = true;
             for (int t = tile0; t < total_tiles && ok; t += tile_step) {
-                int e, mt, nt;
-                decode_tile(t, P.n_tiles, s_toff, E, e, mt, nt);
-                const float* se = g.b_scale + (int64_t)e * (g.b_expert_stride / 64);
-                // the thread's scale: MN-major, row kb * 64 + r of B[e] in the box's column
-                // block; K-major, row n of B[e] in the stage's k block (-1: outside B[e])
-                int64_t s_idx = -1, s_step;
-                if constexpr (B_MN) {
-                    const int col = b_col_pair<PAIRED, BN>(half_tile(s_off, e, mt), (int)rank, jb, nt, g.Ncols);
-                    if (col < g.ldb) s_idx = (int64_t)r * nblk + col / 64;
-                    s_step = 64 * nblk;
-                } else {
-                    const int64_t n = (int64_t)nt * BN + (int)rank * (BN / 2) + r;
-                    if (n < b_rows) s_idx = n * nblk;
-                    s_step = 1;
-                }
                 const int nkb = P.num_kb + (P.lora_k16 ? 1 : 0);
-                auto scale_at = [&](int k) { return (s_idx < 0 || k >= P.num_kb) ? 0.f : __ldg(se + s_idx + k * s_step); };
-                // the scales run one owned stage ahead of the conversion, so that their load
-                // latency is not part of a stage's chain: first the group's first k block of
-                // the tile (stage indices advance by one per k block, kStages % kConvGroups == 0)
-                float sc = scale_at(((grp - stage) % kConvGroups + kConvGroups) % kConvGroups);
                 for (int kb = 0; kb < nkb; ++kb) {
                     const bool mine = (stage % kConvGroups) == grp;
                     if (mine && kb < P.num_kb) {
-                        const float sc_next = scale_at(kb + kConvGroups);
                         const bool got = tc::mbar_wait(tc::smem_u32(&staged_bar[stage]), (sbits >> stage) & 1u, lim);
                         if (!tc::named_bar_and(1 + grp, kGT, got && !*s_abort)) {
                             if (gt == 0) set_timeout(g, s_abort);
@@ -760,6 +750,9 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
                         uint8_t* bt = smem + stage * kStageBytes + kABytes;
                         const uint4* qrow = reinterpret_cast<const uint4*>(bt + G::kBBytes - G::kQBytes + jb * 2048 + r * 32);
                         const uint4 q0 = qrow[0], q1 = qrow[1];
+                        // the row's scale landed with the codes: MN-major, k row r of box jb's
+                        // column block; K-major, n row r in the stage's k block
+                        const float sc = s_scale[stage * 128 + jb * 64 + r];
                         uint32_t lo[4], hi[4];
                         nf4_planes(P.nf4, sc, lo, hi);
                         // all of the group's codes are read before any bf16 value overwrites them
@@ -777,7 +770,6 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
                             else tc::st_async_signal(sig_leader, 1u, full_leader0 + stage * (uint32_t)sizeof(uint64_t));
                         }
                         ++done;
-                        sc = sc_next;
                     }
                     if (++stage == kStages) stage = 0;
                 }
@@ -1171,6 +1163,17 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
             if (!encode(&P.tm_b, g.B, 3, dims_q, st_q, g.b_mn_major ? box_mn_q : box_k_q, CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_DATA_TYPE_UINT8))
                 return cudaErrorInvalidValue;
+            if (qb == 4) {
+                // block scales [E][ldb / 64][rows] float32: a stage takes 64 k rows of one column
+                // block (MN-major B) or 128 n rows of one k block (K-major B)
+                const uint64_t nblk = (uint64_t)g.ldb / 64;
+                const uint64_t dims_s[3] = {rows, nblk, (uint64_t)g.E};
+                const uint64_t st_s[2] = {rows * 4, rows * nblk * 4};
+                const uint32_t box_s[3] = {g.b_mn_major ? 64u : (uint32_t)(BN / 2), 1, 1};
+                if (!encode(&P.tm_bs, g.b_scale, 3, dims_s, st_s, box_s, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+                    return cudaErrorInvalidValue;
+            }
         } else if (!encode(&P.tm_b, g.B, 3, dims, st, g.b_mn_major ? box_mn : box_k, CU_TENSOR_MAP_SWIZZLE_128B)) {
             return cudaErrorInvalidValue;
         }

@@ -51,10 +51,11 @@ struct Nf4Table {
     float v[16];
 };
 const Nf4Table& nf4_table();
-// Per 64 consecutive elements of a row: absmax[m, r, b] = max |W|; each element's code is
-// the nearest table value to W / absmax (float32, ties to the lower code; code 7 when the
-// block is all zero); Wq packs two codes per byte, the even column in the low nibble.
-// cols % 64 == 0.
+// Per 64 consecutive elements of a row: absmax[m, b, r] = max |W[m, r, 64b .. 64b+63]|
+// (block-major: the scales of one column block are contiguous over the rows); each
+// element's code is the nearest table value to W / absmax (float32, ties to the lower code;
+// code 7 when the block is all zero); Wq packs two codes per byte, the even column in the
+// low nibble.  cols % 64 == 0.
 cudaError_t launch_quantize_nf4(const void* W, int64_t n_mat, int64_t rows, int cols, void* Wq, float* absmax,
                                 cudaStream_t s);
 
@@ -108,7 +109,8 @@ struct GroupedGemm {
     bool b_mn_major;      // true: B_e(c, n) = B[e][c][n] (row length ldb); false: B[e][n][c]
     int b_quant;          // 0: bf16 B; 8: e4m3 codes, value = code * b_scale[e * ldb + column of B[e]];
                           // 4: NF4 codes, two per byte, value = bf16(T[code] * b_scale[block]), one
-                          //    scale per 64 consecutive elements of a row of B[e]
+                          //    scale per 64 consecutive elements of a row of B[e], stored
+                          //    [E][ldb / 64][rows of B[e]]
     const float* b_scale; // the scales of a quantised B
     int ldb;              // elements per row of B[e]
     int64_t b_expert_stride;  // elements between experts

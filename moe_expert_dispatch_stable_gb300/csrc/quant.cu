@@ -8,8 +8,10 @@
 //
 // NF4 (4-bit NormalFloat) expert base weights: QLoRA's data type, the pages' "QLoRA
 // 4-bit" base.  16 code values (normal quantiles normalised to [-1, 1]), one float32
-// absmax per 64 consecutive elements of a row, nearest code, two codes per byte; the
-// dequantised weight is bf16(T[code] * absmax), formed inside the GEMM pipeline.
+// absmax per 64 consecutive elements of a row (stored block-major, [m][block][row], so
+// that the GEMM's TMA fetches a stage's scales as one contiguous run), nearest code, two
+// codes per byte; the dequantised weight is bf16(T[code] * absmax), formed inside the GEMM
+// pipeline.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -119,9 +121,10 @@ __device__ __forceinline__ uint32_t nf4_code(float w, float a, const Nf4Table& T
 
 // One warp per block of 64 elements (grid-stride); lane l holds elements 2l and 2l+1 and
 // writes their byte.  Rows are a whole number of blocks, so block b of the flat weight
-// array is row b / (cols / 64), and its codes and scale sit at the same flat index.
-__global__ void quantize_nf4_kernel(const bf16* __restrict__ W, int64_t n_blocks, uint8_t* __restrict__ Wq,
-                                    float* __restrict__ absmax, const Nf4Table T) {
+// array is (matrix m, row r, column block c) with b = (m * rows + r) * nblk + c, and its
+// codes sit at the same flat index; its scale goes to absmax[m][c][r].
+__global__ void quantize_nf4_kernel(const bf16* __restrict__ W, int64_t n_blocks, int64_t rows, int nblk,
+                                    uint8_t* __restrict__ Wq, float* __restrict__ absmax, const Nf4Table T) {
     const int lane = threadIdx.x & 31;
     const int64_t wpb = blockDim.x >> 5;
     const int64_t stride = (int64_t)gridDim.x * wpb;
@@ -131,7 +134,11 @@ __global__ void quantize_nf4_kernel(const bf16* __restrict__ W, int64_t n_blocks
 #pragma unroll
         for (int d = 16; d > 0; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
         Wq[b * 32 + lane] = (uint8_t)(nf4_code(w.x, a, T) | (nf4_code(w.y, a, T) << 4));
-        if (lane == 0) absmax[b] = a;
+        if (lane == 0) {
+            const int64_t c = b % nblk, mr = b / nblk;                 // mr = m * rows + r
+            const int64_t m = mr / rows, r = mr % rows;
+            absmax[(m * nblk + c) * rows + r] = a;
+        }
     }
 }
 
@@ -141,7 +148,8 @@ cudaError_t launch_quantize_nf4(const void* W, int64_t n_mat, int64_t rows, int 
     const int64_t n_blocks = n_mat * rows * (cols / 64);
     if (n_blocks == 0) return cudaSuccess;
     const int grid = (int)std::min<int64_t>((n_blocks + 7) / 8, 16384);
-    quantize_nf4_kernel<<<grid, 256, 0, s>>>((const bf16*)W, n_blocks, (uint8_t*)Wq, absmax, nf4_table());
+    quantize_nf4_kernel<<<grid, 256, 0, s>>>((const bf16*)W, n_blocks, rows, cols / 64, (uint8_t*)Wq, absmax,
+                                             nf4_table());
     return cudaGetLastError();
 }
 

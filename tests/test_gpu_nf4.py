@@ -35,7 +35,8 @@ def test_quantizer_bit_exact_against_oracle():
             for e in (0, W.shape[0] - 1):
                 codes, absmax = nf.quantize_nf4(W[e].cpu())
                 assert np.array_equal(Wq[e].cpu().numpy(), codes), (name, wname, e)
-                assert np.array_equal(am[e].cpu().numpy().view(np.uint32), absmax.view(np.uint32)), (name, wname, e)
+                # the device stores the scales block-major: [cols / 64, rows]
+                assert np.array_equal(am[e].t().cpu().numpy().view(np.uint32), absmax.view(np.uint32)), (name, wname, e)
 
 
 # Every NF4 launch runs on SM pairs.  The bf16 reference runs on single-CTA tiles for the
@@ -57,7 +58,7 @@ def _oracle_dequantized(ts, wq):
     for name_w, qn, sn in (("W_gu", "W4_gu", "m_gu"), ("W_d", "W4_d", "m_d")):
         codes, absmax = nf.quantize_nf4(ts[name_w].cpu())
         assert np.array_equal(wq[qn].cpu().numpy(), codes)
-        assert np.array_equal(wq[sn].cpu().numpy(), absmax)
+        assert np.array_equal(wq[sn].transpose(-1, -2).cpu().numpy(), absmax)
         deq[name_w] = torch.tensor(nf.dequantize_nf4(codes, absmax)).to(torch.bfloat16).cuda()
     return deq
 
@@ -111,7 +112,7 @@ def test_nf4_extreme_block_scales_bit_identical(name):
     ts["W_gu"], ts["W_d"] = W_gu, W_d
     wq = moe.quantize_expert_weights(ts, fmt="nf4")
     torch.cuda.synchronize()
-    assert float(wq["m_gu"][:, 8:16, cfg.I // 64].max()) < 2.0 ** -126
+    assert float(wq["m_gu"][:, cfg.I // 64, 8:16].max()) < 2.0 ** -126
     deq = _oracle_dequantized(ts, wq)
     ref, q4, g_ref, g_q4 = _run_both(cfg, idx, w, ts, deq, wq)
     assert bool(torch.isfinite(ref.y.float()).all())
@@ -127,7 +128,7 @@ def _torch_dequantize(Wq, am, T):
     for e in range(Wq.shape[0]):
         q = Wq[e].to(torch.int64)
         c = torch.stack([q & 15, q >> 4], dim=-1).reshape(q.shape[0], -1)
-        out[e] = (T[c] * am[e].repeat_interleave(64, dim=-1)).to(torch.bfloat16)
+        out[e] = (T[c] * am[e].t().repeat_interleave(64, dim=-1)).to(torch.bfloat16)
     return out
 
 
