@@ -516,6 +516,8 @@ def main():
     ap.add_argument("--steps-only", action="store_true",
                     help="run the warm-up and timed steps of the layer, print the line's step time and exit "
                          "(a short command for profilers)")
+    ap.add_argument("--base", default="bf16", choices=["bf16", "fp8", "nf4"],
+                    help="with --steps-only: the expert base weights' format")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = mi.CONFIGS[args.config]
@@ -546,7 +548,9 @@ def main():
     ts = mi.make_tensors(cfg, args.seed, dev, names=("W_gu", "A_gu", "B_gu", "W_d", "A_d", "B_d"))
     ts.update(mi.make_tensors(cfg, args.seed + rank, dev, names=("x", "dy")))
     d = moe.Dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.r, cfg.scale)
-    layer = moe.MoELoRALayer(d, ts, dev)
+    if args.base != "bf16" and not args.steps_only:
+        raise SystemExit("--base applies to --steps-only runs")
+    layer = moe.MoELoRALayer(d, ts if args.base == "bf16" else moe.quantize_expert_weights(ts, fmt=args.base), dev)
     t_idx = torch.from_numpy(idx).to(dev)
     t_w = torch.from_numpy(w).to(dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -584,7 +588,8 @@ def main():
         clocks.stop()
         assert int(layer.dev_status.item()) == 0, "device status flag set"
         if rank == 0:
-            print(json.dumps({"steps_only": True, "config": config_dict(cfg), "ms_per_step": total_ms / args.steps,
+            print(json.dumps({"steps_only": True, "config": config_dict(cfg), "base": args.base,
+                              "ms_per_step": total_ms / args.steps,
                               "value": value, "unit": UNIT}), flush=True)
         if world > 1:
             dist.destroy_process_group()
