@@ -36,21 +36,23 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BK = 64;
-constexpr int kEpiWarps = 8;                 // 2 per TMEM lane quarter, each half the columns
-constexpr int kConvWarps = 8;                 // FP8 weights: dequantising warps (2 per scheduler)
-// the converter warps form groups; group g owns the stages s with s % kConvGroups == g,
-// so that several stages are dequantised at once and one group's proxy fence overlaps
-// another's work.  Owning whole stages keeps every mbarrier phase wait of a group within
-// one phase of the barrier (a stage cannot move on before its owner has arrived).
-#ifndef MOE_CONV_GROUPS
-#define MOE_CONV_GROUPS 2
-#endif
-constexpr int kConvGroups = MOE_CONV_GROUPS;
-constexpr int kSignalBytes = 4;                // FP8 pairs: the peer's "B half converted" store
+// epilogue warps: with bf16 weights 2 per TMEM lane quarter, each half the columns; with
+// quantised weights 1 per lane quarter, so that 12 warps can dequantise within the same
+// 576 threads (the register budget: 96 registers a thread)
+__host__ __device__ constexpr int epi_warps(bool quant) { return quant ? 4 : 8; }
+constexpr int kConvWarps = 12;                // quantised weights: dequantising warps
+// the converter warps form groups of 4; group g owns the stages s with s % kConvGroups == g,
+// so that several stages are dequantised at once and each stage's fixed costs (the wait,
+// two group barriers, the proxy fence, the signal) overlap other groups' work.  Owning
+// whole stages keeps every mbarrier phase wait of a group within one phase of the barrier
+// (a stage cannot move on before its owner has arrived).
+constexpr int kConvGroups = 3;
+constexpr int kSignalBytes = 4;                // quantised pairs: the peer's "B half converted" store
 constexpr unsigned kPaceNs = 500;              // epilogue store pacing (see the epilogue)
-static_assert(kConvWarps % kConvGroups == 0 && (kConvGroups & (kConvGroups - 1)) == 0, "converter groups");
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-__host__ __device__ constexpr int threads_of(bool q8) { return kThreads + (q8 ? 32 * kConvWarps : 0); }
+static_assert(kConvWarps == 4 * kConvGroups, "converter groups of 4 warps");
+__host__ __device__ constexpr int threads_of(bool quant) {
+    return 64 + 32 * epi_warps(quant) + (quant ? 32 * kConvWarps : 0);
+}
 constexpr int kABytes = BM * BK * 2;         // 16 KB
 constexpr int kBoxMN = 64 * BK * 2;          // one 64-column MN-major box of B: 8 KB
 
@@ -284,6 +286,7 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
     constexpr bool PAIRED = (EPI == EPI_SWIGLU);
     using G = Geo<BN, PAIR, QB>;
     constexpr bool QW = QB != 0;                    // quantised weights (e4m3 or NF4 codes)
+    constexpr int kEpiWarps = epi_warps(QW);
     static_assert(QB == 0 || QB == 8 || QB == 4, "e4m3 or NF4 codes");
     static_assert(!QW || BN == 256, "quantised weights are for the expert GEMMs");
     static_assert(!QW || PAIR, "quantised weights run on SM pairs (each CTA dequantises half of the B tile)");
@@ -308,10 +311,13 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
     volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     uint32_t* sig_slot = tmem_slot + 2;             // FP8 pairs: target of the peer's stage signals
     // what the roles issued, read by the abort drain: [0] the producer's stage fills,
-    // [1 + g] the stages converter group g signalled (FP8); [3] debug build: bad offsets
+    // [1 + g] the stages converter group g signalled (quantised B); [kDebugSlot] debug
+    // build: bad offsets
     volatile int* s_issued = reinterpret_cast<volatile int*>(tmem_slot + 4);
-    int32_t* s_off = reinterpret_cast<int32_t*>(tmem_slot + 8);
-    static_assert((3 * kStages + 6) * 8 + 32 <= 256, "barriers and flags fit the 256-byte tail");
+    constexpr int kDebugSlot = 1 + kConvGroups;
+    int32_t* s_off = reinterpret_cast<int32_t*>(tmem_slot + 12);
+    static_assert(4 + kDebugSlot < 12, "issue counters fit before the offsets");
+    static_assert((3 * kStages + 6) * 8 + 48 <= 256, "barriers and flags fit the 256-byte tail");
     const GroupedGemm& g = P.g;
     const int E = g.E;
     int32_t* s_toff = s_off + (E + 1);
@@ -392,10 +398,10 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
     if constexpr (MOE_DEBUG) {
         // debug build: offsets that do not describe N rows schedule no tile
         if (threadIdx.x == 0)
-            s_issued[3] = dbg_offsets_ok(s_off, PAIR ? nullptr : s_toff, E, g.N, BM, g.dev_status) ? 0 : 1;
+            s_issued[kDebugSlot] = dbg_offsets_ok(s_off, PAIR ? nullptr : s_toff, E, g.N, BM, g.dev_status) ? 0 : 1;
         __syncthreads();
     }
-    const int total_tiles = (MOE_DEBUG && s_issued[3]) ? 0 : s_toff[E] * P.n_tiles;
+    const int total_tiles = (MOE_DEBUG && s_issued[kDebugSlot]) ? 0 : s_toff[E] * P.n_tiles;
     const uint64_t lim = P.wait_ns;
     int fills = 0;                                  // the producer's stage fills (lane 0 of warp 0)
     constexpr int KB2 = G::KB2;                     // 64-deep k-blocks per ring stage
@@ -778,14 +784,15 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // warp w reads TMEM lanes 32*(w%4)..+31 (one row per thread); the two warps of a
-        // lane quarter split the columns in halves.  Half tiles (SM pairs, M = 128): lane L
-        // holds row L mod 64, lanes 64-127 the upper half of the columns in the same TMEM
-        // columns, so each warp covers half as many TMEM columns.
+        // warp w reads TMEM lanes 32*(w%4)..+31 (one row per thread); with 8 epilogue warps
+        // the two warps of a lane quarter split the columns in halves, with 4 one warp takes
+        // them all.  Half tiles (SM pairs, M = 128): lane L holds row L mod 64, lanes 64-127
+        // the upper half of the columns in the same TMEM columns, so each warp covers half as
+        // many TMEM columns.
         const int q = warp & 3;
-        const int hw = (warp - 2) >> 2;
+        const int hw = (warp - 2) >> 2;                                 // 0 with 4 epilogue warps
         const int row = q * 32 + lane;
-        constexpr int kSpan = PAIRED ? BN / 4 : (BN >= 32 ? BN / 2 : BN);   // columns per warp
+        constexpr int kSpan = (PAIRED ? BN / 4 : (BN >= 32 ? BN / 2 : BN)) * (8 / kEpiWarps);   // columns per warp
         const int c0 = (BN >= 32 || PAIRED) ? hw * kSpan : 0;
         const bool active = (BN >= 32 || PAIRED) || hw == 0;
         int it = 0;
