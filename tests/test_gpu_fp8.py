@@ -44,6 +44,10 @@ CASES = {
     # ~3 tiles per SM pair: the converters carry their stage parity across tiles and
     # LoRA steps
     "multi_tile": mi.MoEConfig("multitile", T=8192, H=512, E=8, k=2, I=512, r=16, alpha=32),
+    # LoRA rank 64: the unconverted LoRA stage carries four 16-deep MMA slices
+    "pairs_r64": mi.MoEConfig("pairs_r64", T=1000, H=256, E=4, k=2, I=320, r=64, alpha=128),
+    # every token routed to every expert (k = E), rank 32
+    "k_equals_e_r32": mi.MoEConfig("keqe", T=400, H=192, E=4, k=4, I=256, r=32, alpha=64),
 }
 
 
