@@ -20,6 +20,9 @@
 //   warps 2..9  epilogue (two per TMEM lane quarter, each half the columns):
 //               tcgen05.ld 32 lanes x 16 columns, fused SwiGLU / routing-weight
 //               scale / SwiGLU backward, masked stores
+// Quantised base weights (e4m3 or NF4 codes, SM pairs only): 18 warps, warps 2..5
+// the epilogue (one per lane quarter) and warps 6..17 three groups of converters that
+// expand each stage's codes into bf16 B tiles in shared memory.
 // Every mbarrier wait is bounded; a wait that gives up sets MOE_DEV_TIMEOUT.
 #include "common.cuh"
 #include "epilogue.cuh"
@@ -304,12 +307,12 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
     uint64_t* empty_bar = full_bar + kStages;
     uint64_t* tfull_bar = empty_bar + kStages;
     uint64_t* tempty_bar = tfull_bar + 2;
-    uint64_t* staged_bar = tempty_bar + 2;          // FP8 codes landed in the staging slot
+    uint64_t* staged_bar = tempty_bar + 2;          // quantised B: codes (and NF4 scales) landed
     uint64_t* drain_bar = staged_bar + kStages;     // after an abort: the MMA issuer's last commit
     uint64_t* stall_bar = drain_bar + 1;            // diagnostics: nothing ever arrives on it
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stall_bar + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    uint32_t* sig_slot = tmem_slot + 2;             // FP8 pairs: target of the peer's stage signals
+    uint32_t* sig_slot = tmem_slot + 2;             // quantised pairs: target of the peer's stage signals
     // what the roles issued, read by the abort drain: [0] the producer's stage fills,
     // [1 + g] the stages converter group g signalled (quantised B); [kDebugSlot] debug
     // build: bad offsets
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            // with FP8 weights the B half of a stage is complete when the converter group
+            // with quantised weights the B half of a stage is complete when the converter group
             // that owns the stage has arrived (and, in a pair, the peer's group has completed
             // kSignalBytes transaction bytes on it)
             tc::mbar_init(tc::smem_u32(&full_bar[s]), QW ? 2 : 1);
@@ -478,7 +481,7 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
                         } else {
                             if (rank == 0) {
                                 tc::mbar_arrive_expect_tx(fb_local, 2 * (a2_bytes + 2 * P.b2_box_bytes));
-                                // FP8: the LoRA step needs no conversion; the producer makes both arrivals
+                                // quantised B: the LoRA step needs no conversion; the producer makes both arrivals
                                 if (QW) tc::mbar_arrive(fb_local);
                             }
                             tc::tma_load_2d_pair(sa, tma2, fb, 0, m0);
@@ -560,7 +563,7 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
                 const int nkb = G::KW > 1 ? (P.num_kb + G::KW - 1) / G::KW : nmain + (P.lora_k16 ? 1 : 0);
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb) {
-                    // FP8 pairs: the peer's converted half is published by a cluster-scope release
+                    // quantised pairs: the peer's converted half is published by a cluster-scope release
                     if (!tc::mbar_wait<QW && PAIR>(tc::smem_u32(&full_bar[stage]), phase, lim)) {
                         set_timeout(g, s_abort);
                         ok = false;
@@ -938,7 +941,7 @@ __global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel
     // of stages nobody consumed, a pair's loads and stage signals towards the leader's full
     // barriers, MMAs of tiles whose accumulators nobody read.  Every one of them has landed
     // before the shared memory and TMEM are released: each producer waits for its own code
-    // stages (FP8), the leader completes on behalf of the side that issued nothing every
+    // stages (quantised B), the leader completes on behalf of the side that issued nothing every
     // full-barrier phase that received any copy and waits for it, and the MMA issuer waits
     // for a last commit.  These waits use the full limit.  Both CTAs of a pair read both
     // abort flags, so they take the branch together.
