@@ -103,10 +103,10 @@ def kernel_work(cfg: mi.MoEConfig, ridge: float | None = None) -> dict:
 # DRAM bytes (read + write) per launch from ncu captures of the current kernels
 # (profiles/), keyed by (workload, kernel); None where no capture of the current code exists.
 MEASURED_TRAFFIC = {
-    ("gptoss20b", "gemm_gate_up_fwd"): 1.1666e9 + 0.2620e9,
-    ("gptoss20b", "gemm_down_fwd"): 0.6311e9 + 0.0796e9,
-    ("gptoss20b", "gemm_down_bwd"): 0.8360e9 + 0.1637e9,
-    ("gptoss20b", "gemm_gate_up_bwd"): 1.3162e9 + 0.0861e9,
+    ("gptoss20b", "gemm_gate_up_fwd"): 1.1715e9 + 0.2616e9,
+    ("gptoss20b", "gemm_down_fwd"): 0.6333e9 + 0.0799e9,
+    ("gptoss20b", "gemm_down_bwd"): 0.8380e9 + 0.1637e9,
+    ("gptoss20b", "gemm_gate_up_bwd"): 1.3208e9 + 0.0864e9,
 }
 
 
