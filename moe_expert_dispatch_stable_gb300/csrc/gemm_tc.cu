@@ -39,23 +39,19 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BK = 64;
-// epilogue warps: with bf16 weights 2 per TMEM lane quarter, each half the columns; with
-// quantised weights 1 per lane quarter, so that 12 warps can dequantise within the same
-// 576 threads (the register budget: 96 registers a thread)
-__host__ __device__ constexpr int epi_warps(bool quant) { return quant ? 4 : 8; }
-constexpr int kConvWarps = 12;                // quantised weights: dequantising warps
-// the converter warps form groups of 4; group g owns the stages s with s % kConvGroups == g,
-// so that several stages are dequantised at once and each stage's fixed costs (the wait,
-// two group barriers, the proxy fence, the signal) overlap other groups' work.  Owning
-// whole stages keeps every mbarrier phase wait of a group within one phase of the barrier
-// (a stage cannot move on before its owner has arrived).
-constexpr int kConvGroups = 3;
+// Quantised weights add CG groups of 4 converter warps (CG = 0 with bf16 weights).  A group
+// g owns the stages s with s % CG == g, so that several stages are dequantised at once and
+// each stage's fixed costs (the wait, two group barriers, the proxy fence, the signal)
+// overlap other groups' work; owning whole stages keeps every mbarrier phase wait of a
+// group within one phase of the barrier (a stage cannot move on before its owner has
+// arrived).  Epilogue warps: 2 per TMEM lane quarter, each half the columns, except with 3
+// converter groups: 1 per lane quarter, so that the CTA stays at 576 threads (the register
+// budget: 96 registers a thread).  Three groups suit long k loops, whose tiles give the
+// slower 4-warp epilogue time to finish (see launch_impl).
+__host__ __device__ constexpr int epi_warps(int cg) { return cg == 3 ? 4 : 8; }
+__host__ __device__ constexpr int threads_of(int cg) { return 64 + 32 * epi_warps(cg) + 128 * cg; }
 constexpr int kSignalBytes = 4;                // quantised pairs: the peer's "B half converted" store
 constexpr unsigned kPaceNs = 500;              // epilogue store pacing (see the epilogue)
-static_assert(kConvWarps == 4 * kConvGroups, "converter groups of 4 warps");
-__host__ __device__ constexpr int threads_of(bool quant) {
-    return 64 + 32 * epi_warps(quant) + (quant ? 32 * kConvWarps : 0);
-}
 constexpr int kABytes = BM * BK * 2;         // 16 KB
 constexpr int kBoxMN = 64 * BK * 2;          // one 64-column MN-major box of B: 8 KB
 
@@ -283,13 +279,16 @@ __device__ __forceinline__ uint4 nf4x8_to_bf16(uint32_t q, const uint32_t* lo, c
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-template <int EPI, bool B_MN, int BN, bool PAIR, int QB>
-__global__ void __launch_bounds__(threads_of(QB != 0), 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams P) {
+template <int EPI, bool B_MN, int BN, bool PAIR, int QB, int CG>
+__global__ void __launch_bounds__(threads_of(CG), 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams P) {
     pdl_wait();      // no early trigger: dependents launch when this long kernel completes
     constexpr bool PAIRED = (EPI == EPI_SWIGLU);
     using G = Geo<BN, PAIR, QB>;
     constexpr bool QW = QB != 0;                    // quantised weights (e4m3 or NF4 codes)
-    constexpr int kEpiWarps = epi_warps(QW);
+    static_assert(QW == (CG != 0) && (CG == 0 || CG == 2 || CG == 3), "converter groups with quantised weights");
+    constexpr int kEpiWarps = epi_warps(CG);
+    constexpr int kConvGroups = QW ? CG : 1;       // (1 sizes the drain's per-group arrays)
+    constexpr int kConvWarps = 4 * CG;
     static_assert(QB == 0 || QB == 8 || QB == 4, "e4m3 or NF4 codes");
     static_assert(!QW || BN == 256, "quantised weights are for the expert GEMMs");
     static_assert(!QW || PAIR, "quantised weights run on SM pairs (each CTA dequantises half of the B tile)");
@@ -1077,10 +1076,10 @@ int sm_count() {
 
 // One CTA per SM (grid = min(#SMs, tiles)); SM pairs: as many 2-CTA clusters as can be
 // resident at once (so that no pair waits for another to finish), at most one per tile.
-template <int EPI, bool B_MN, int BN, bool PAIR, int QB = 0>
+template <int EPI, bool B_MN, int BN, bool PAIR, int QB = 0, int CG = 0>
 cudaError_t launch_tc(const TcParams& P, int64_t max_tiles, size_t smem, cudaStream_t s) {
-    auto k = grouped_gemm_tc_kernel<EPI, B_MN, BN, PAIR, QB>;
-    constexpr int kThr = threads_of(QB != 0);
+    auto k = grouped_gemm_tc_kernel<EPI, B_MN, BN, PAIR, QB, CG>;
+    constexpr int kThr = threads_of(CG);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if constexpr (!PAIR) {
@@ -1109,6 +1108,20 @@ cudaError_t launch_tc(const TcParams& P, int64_t max_tiles, size_t smem, cudaStr
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.numAttrs = 2;
         return cudaLaunchKernelEx(&cfg, k, P);
+    }
+}
+
+// The layer's four expert GEMMs with quantised weights (QB-bit codes, CG converter groups)
+template <int QB, int CG>
+cudaError_t launch_quant(const TcParams& P, const GroupedGemm& g, int64_t max_tiles, size_t offs_bytes,
+                         cudaStream_t s) {
+    const size_t smem = Geo<256, true, QB>::kSmem + offs_bytes;
+    switch (g.epi) {
+        case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256, true, QB, CG>(P, max_tiles, smem, s);
+        case EPI_BF16:
+            return g.b_mn_major ? launch_tc<EPI_BF16, true, 256, true, QB, CG>(P, max_tiles, smem, s)
+                                : launch_tc<EPI_BF16, false, 256, true, QB, CG>(P, max_tiles, smem, s);
+        default: return launch_tc<EPI_DSWIGLU, false, 256, true, QB, CG>(P, max_tiles, smem, s);
     }
 }
 
@@ -1229,27 +1242,16 @@ cudaError_t launch_impl(const GroupedGemm& g, bool allow_pairs, cudaStream_t s) 
     // The layer's expert GEMMs: gate_up forward (SwiGLU, MN-major B), down forward (bf16,
     // MN-major B), down backward (SwiGLU backward, K-major B: W_d read transposed) and
     // gate_up backward (bf16, K-major B: W_gu read transposed).
-    if (qb == 8) {
+    if (qb != 0) {
         if (!pair) return cudaErrorNotSupported;   // quantised weights run on SM pairs only
-        const size_t smem = Geo<256, true, 8>::kSmem + offs_bytes;
-        switch (g.epi) {
-            case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256, true, 8>(P, max_tiles, smem, s);
-            case EPI_BF16:
-                return mn ? launch_tc<EPI_BF16, true, 256, true, 8>(P, max_tiles, smem, s)
-                          : launch_tc<EPI_BF16, false, 256, true, 8>(P, max_tiles, smem, s);
-            default: return launch_tc<EPI_DSWIGLU, false, 256, true, 8>(P, max_tiles, smem, s);
-        }
-    }
-    if (qb == 4) {
-        if (!pair) return cudaErrorNotSupported;
-        const size_t smem = Geo<256, true, 4>::kSmem + offs_bytes;
-        switch (g.epi) {
-            case EPI_SWIGLU: return launch_tc<EPI_SWIGLU, true, 256, true, 4>(P, max_tiles, smem, s);
-            case EPI_BF16:
-                return mn ? launch_tc<EPI_BF16, true, 256, true, 4>(P, max_tiles, smem, s)
-                          : launch_tc<EPI_BF16, false, 256, true, 4>(P, max_tiles, smem, s);
-            default: return launch_tc<EPI_DSWIGLU, false, 256, true, 4>(P, max_tiles, smem, s);
-        }
+        // three converter groups (and a 4-warp epilogue) for long k loops, or for half tiles
+        // (experts of under 256 rows on average) with k >= 2048; two groups (8 epilogue warps)
+        // where each tile's epilogue must hide behind a short k loop
+        const bool three = g.K >= 2560 || (g.N < 256 * (int64_t)g.E && g.K >= 2048);
+        if (qb == 8) return three ? launch_quant<8, 3>(P, g, max_tiles, offs_bytes, s)
+                                  : launch_quant<8, 2>(P, g, max_tiles, offs_bytes, s);
+        return three ? launch_quant<4, 3>(P, g, max_tiles, offs_bytes, s)
+                     : launch_quant<4, 2>(P, g, max_tiles, offs_bytes, s);
     }
     if (pair) {
         const size_t smem = Geo<256, true>::kSmem + offs_bytes;

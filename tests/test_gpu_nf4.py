@@ -52,6 +52,11 @@ CASES = {
     "pairs_r64": mi.MoEConfig("pairs_r64", T=1000, H=256, E=4, k=2, I=320, r=64, alpha=128),
     # every token routed to every expert (k = E), rank 32
     "k_equals_e_r32": mi.MoEConfig("keqe", T=400, H=192, E=4, k=4, I=256, r=32, alpha=64),
+    # three converter groups for the k = 2560 GEMMs (gate_up forward, down backward), two
+    # for the others
+    "long_k_three_groups": mi.MoEConfig("longk", T=600, H=2560, E=4, k=2, I=256, r=16, alpha=32),
+    # half tiles (64 rows per expert) with k = 2048: three groups except the down forward
+    "half_tiles_three_groups": mi.MoEConfig("halfk", T=256, H=2048, E=8, k=2, I=1024, r=16, alpha=32),
 }
 
 
