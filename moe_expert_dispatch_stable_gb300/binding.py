@@ -579,6 +579,8 @@ def moe_timing_read() -> dict:
 class MoELoRALayer:
     """Preallocated buffers for repeated route + forward + backward calls on one
     stream (no allocation inside a step, so a step can be graph-captured).
+    `weights`: the bf16 expert weights, or those of quantize_expert_weights (FP8 or NF4
+    base; the layer then calls the _fp8 / _nf4 entry points).
     h_from_gu: bf16 weights only; the forward forms h from the stored bf16 GU
     (moe_lora_fwd_h_from_gu), as the offloaded stack does."""
 
