@@ -590,6 +590,8 @@ class MoELoRALayer:
         self.h_from_gu = h_from_gu
         self.fp8 = "Wq_gu" in weights          # FP8 base weights (quantize_expert_weights)
         self.nf4 = "W4_gu" in weights          # NF4 base weights (quantize_expert_weights, fmt="nf4")
+        if h_from_gu and (self.fp8 or self.nf4):
+            raise MoEError("h_from_gu is a forward of the bf16 weights only")
         dev = torch.device(device)
         self.rt = Routing.empty(d.T, d.k, d.E, dev)
         self.route_ws = torch.empty(moe_route_workspace_size(d.T, d.k, d.E), dtype=torch.uint8, device=dev)
