@@ -278,3 +278,13 @@ def test_forced_timeout_hook_checks_its_limit(lib):
     assert lib.moe_diag_force_timeout(-1, 0) == 0
     assert lib.moe_diag_force_timeout(3, 1_000_000) == 0
     assert lib.moe_diag_force_timeout(-1, 0) == 0
+
+
+def test_layer_rejects_h_from_gu_with_quantised_weights():
+    """The h-from-GU forward exists for bf16 weights only; a layer over quantised weights
+    refuses the flag before allocating anything."""
+    from moe_expert_dispatch_stable_gb300 import binding as b
+    d = b.Dims(8, 64, 64, 4, 2, 4, 2.0)
+    for key in ("Wq_gu", "W4_gu"):
+        with pytest.raises(b.MoEError):
+            b.MoELoRALayer(d, {key: None}, device="cpu", h_from_gu=True)
